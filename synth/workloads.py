@@ -1,0 +1,49 @@
+"""The synthetic workloads: one tiny layer, and DeepSeek-V4.1-Flash-shaped
+MoE layers (hidden 5120, expert intermediate 2304, 384 routed experts top-6
+plus one shared expert) at decode, verification-block, prefill and
+8-layer-stack sizes.  Geometry from the FreeToken issue #444 ("Architecture
+delta vs deepseek_v4": 384 routed + 1 shared, top-6, 3 x 5120 x 2304 FP4) and
+the ai.rs article's table "What V4.1 Flash is, in bytes".
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    hidden: int
+    inter: int
+    n_experts: int
+    top_k: int
+    n_shared: int
+    tokens: int
+    seed: int
+    layers: int = 1
+    scale_lo: int = -8      # UE8M0 exponents uniform on [scale_lo, scale_hi]
+    scale_hi: int = -4
+    zipf: float | None = None   # router-bias Zipf exponent, None = unbiased
+    rmsnorm: bool = False   # stack: normalise each layer's input
+
+    def with_tokens(self, t: int) -> "Workload":
+        return replace(self, tokens=t)
+
+    @property
+    def expert_bytes(self) -> int:
+        """Bytes of one expert: codes (1/2 B) plus scales (1/32 B) per weight."""
+        n = 3 * self.hidden * self.inter
+        return n // 2 + n // 32
+
+
+_V41 = dict(hidden=5120, inter=2304, n_experts=384, top_k=6, n_shared=1)
+
+TINY = Workload("tiny_h256_e16_t4", 256, 128, 16, 2, 1, 4, seed=0, scale_lo=-6, scale_hi=-2)
+DECODE_T1 = Workload("v41_layer_decode_t1", tokens=1, seed=1, **_V41)
+VERIFY_T5 = Workload("v41_layer_verify_t5_zipf", tokens=5, seed=2, zipf=1.1, **_V41)
+VERIFY_T32 = Workload("v41_layer_verify_t32_zipf", tokens=32, seed=3, zipf=1.1, **_V41)
+PREFILL_T4096 = Workload("v41_layer_prefill_t4096", tokens=4096, seed=4, **_V41)
+STACK8_T64 = Workload("v41_stack8_decode_t64_zipf", tokens=64, seed=5, layers=8, zipf=1.1,
+                      rmsnorm=True, **_V41)
+
+WORKLOADS = {w.name: w for w in (TINY, DECODE_T1, VERIFY_T5, VERIFY_T32, PREFILL_T4096, STACK8_T64)}
