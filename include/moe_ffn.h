@@ -1,0 +1,185 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 (sm_103a) routed MXFP4 mixture-of-experts
+ * FFN layer.
+ *
+ * The layer (DeepSeek-V4.1-Flash MoE block geometry: 384 routed experts plus
+ * one shared expert, top-6, hidden 5120, expert intermediate 2304; FreeToken
+ * issue #444, "Architecture delta vs deepseek_v4") computes, per token t with
+ * bf16 input x[t]:
+ *
+ *   logits  l = W_r x + b                       (fp32)
+ *   routing idx = top-k of l (value desc, index asc), w = softmax over them
+ *   x^      = FP8 E4M3 per-32 with UE8M0 scale (dynamic activation scheme,
+ *             FreeToken issue #444 "Is the quantization already supported")
+ *   expert  o_e = Wd_e Q8( silu(Wg_e x^) * (Wu_e x^) )   (MXFP4 weights)
+ *   y       = bf16( sum_shared o_s + sum_j w_j o_idx_j )  [+ residual]
+ *
+ * MXFP4 matrices use one canonical layout (packed E2M1 + one UE8M0 per 32,
+ * FreeToken issue #444, janit's comment item 2 "Routed expert bytes per
+ * token"): a matrix with N output rows and K inputs is
+ *   codes  [N][K/2] bytes, row-major; element k of a row is the low nibble of
+ *          byte k/2 when k is even and the high nibble when k is odd;
+ *   scales [N][K/32] bytes, UE8M0 (value 2^(s-127)) for elements 32j..32j+31.
+ * A bank of E experts stacks E such matrices contiguously.
+ *
+ * Conventions for every call:
+ *  - Pointers named x, y, residual, logits, topk_* and the weight pointers are
+ *    DEVICE pointers on the layer's device unless the name ends in _host.
+ *  - bf16 tensors are passed as void* holding IEEE bfloat16 bit patterns,
+ *    row-major [T][H].
+ *  - Calls are asynchronous on the caller's CUDA stream (cudaStream_t passed
+ *    as void*, NULL = legacy default stream).  Argument errors are returned
+ *    synchronously and nothing is launched.  A launch failure returns
+ *    MOE_ERR_CUDA and clears the CUDA error state.  Errors the kernels record
+ *    on the device (an expert id out of range) are returned by moe_sync (and
+ *    by moe_forward_host, which synchronises).
+ *  - A layer must not be used from two streams at the same time: calls share
+ *    the layer's workspace.
+ *  - No call allocates device memory except moe_layer_create.
+ *  - No call exits or aborts the process.
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, T > max_tokens, ... */
+  MOE_ERR_UNSUPPORTED = 2, /* shape outside the supported envelope        */
+  MOE_ERR_OOM = 3,         /* workspace allocation failed                 */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed        */
+  MOE_ERR_TIMEOUT = 5,     /* a bounded device wait gave up               */
+  MOE_ERR_INTERNAL = 6     /* a device-side check failed (index range)    */
+} moe_status;
+
+/* One MXFP4 matrix or bank of matrices in the canonical layout above. */
+typedef struct {
+  const uint8_t* codes;
+  const uint8_t* scales;
+} moe_mx_mat;
+
+/* Shapes.  hidden and inter: multiples of 128 (128..16384); n_experts 1..512;
+ * top_k 1..8 and <= n_experts; n_shared 0..4; max_tokens 1..65535 bounds T
+ * of every call and sizes the workspace.  Anything else returns
+ * MOE_ERR_UNSUPPORTED. */
+typedef struct {
+  int32_t hidden;
+  int32_t inter;
+  int32_t n_experts;
+  int32_t top_k;
+  int32_t n_shared;
+  int32_t max_tokens;
+} moe_config;
+
+/* Weights, all borrowed device pointers that must outlive the layer.
+ * gate/up: banks of n_experts matrices with N = inter, K = hidden;
+ * down: N = hidden, K = inter.  s_gate/s_up/s_down: the shared experts, same
+ * shapes, n_shared of them (ignored when n_shared = 0).
+ * router_w: fp32 [n_experts][hidden]; router_b: fp32 [n_experts] or NULL.
+ * Code and scale pointers must be 32-byte aligned, router_w 16-byte aligned. */
+typedef struct {
+  moe_mx_mat gate, up, down;
+  moe_mx_mat s_gate, s_up, s_down;
+  const float* router_w;
+  const float* router_b;
+} moe_weights;
+
+typedef struct moe_layer moe_layer;
+
+/* Creates a layer on `device`: validates the shapes, allocates the workspace
+ * for max_tokens (the only allocation the library makes) and builds any
+ * derived layout.  On failure *out is NULL and nothing is left allocated. */
+moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int device,
+                            moe_layer** out);
+
+/* Synchronises the layer's device, frees its workspace and the handle. */
+moe_status moe_layer_destroy(moe_layer* layer);
+
+/* Router (ai.rs, "What remains is the reference rounding itself": the gate is
+ * a switch over the top-6 scores; llama.cpp discussion #28766, "Correctness").
+ *  x          bf16 [T][H]
+ *  logits_in  fp32 [T][E] or NULL.  When given, the logits are not computed:
+ *             selection and weights use these values (so two implementations
+ *             given the same logits must select identically).
+ *  logits_out fp32 [T][E] or NULL: receives the logits used.
+ *  topk_idx   int32 [T][k]: expert ids by rank (larger logit first, equal
+ *             logits by lower index, NaN ranks as -infinity).
+ *  topk_w     fp32 [T][k]: softmax over the k selected logits (sums to 1).
+ * T = 0 is a no-op. */
+moe_status moe_route(moe_layer* layer, const void* x, int32_t T, const float* logits_in,
+                     float* logits_out, int32_t* topk_idx, float* topk_w, void* stream);
+
+/* Expert FFN and combine for T tokens routed by (topk_idx, topk_w):
+ *  y[t] = bf16( sum_shared o_s + sum_j topk_w[t][j] * o_{topk_idx[t][j]} ),
+ * summed in fixed order (shared experts, then j = 0..k-1); with a residual
+ * (bf16 [T][H] or NULL) y[t] = bf16(residual[t] + y[t]).  y may alias
+ * residual but not x.  Expert ids outside [0, n_experts) are skipped and
+ * make the next moe_sync return MOE_ERR_INTERNAL.  A repeated id in one row is
+ * computed once per slot.  x, y and residual must be 16-byte aligned.  T = 0
+ * is a no-op. */
+moe_status moe_forward(moe_layer* layer, const void* x, int32_t T, const int32_t* topk_idx,
+                       const float* topk_w, const void* residual, void* y, void* stream);
+
+/* moe_route followed by moe_forward, with x and y in HOST memory: copies x to
+ * the device, runs the layer and copies y back, all on `stream`; returns
+ * after y_host is written (the call synchronises the stream).  For full copy
+ * speed x_host and y_host should be page-locked.  T <= max_tokens. */
+moe_status moe_forward_host(moe_layer* layer, const void* x_host, int32_t T, void* y_host,
+                            void* stream);
+
+/* The activation quantiser alone: q [T][H] E4M3 codes and s [T][H/32] UE8M0
+ * bytes, by the rule: per block of 32, e = the smallest integer with
+ * max|x| <= 448 * 2^e (e = 0 for an all-zero block, limited to [-127, 127]),
+ * s = e + 127, q = E4M3(x / 2^e) rounded to nearest, ties to even, sign kept
+ * for zero results.  Inputs must be finite. */
+moe_status moe_quantize_act(moe_layer* layer, const void* x, int32_t T, uint8_t* q, uint8_t* s,
+                            void* stream);
+
+/* The expert segments the forward pass builds from topk_idx [T][k]:
+ * offsets [E+1] (offsets[e] = number of slots routed to experts below e) and
+ * perm [T*k], the slots s = t*k + j listed expert by expert, in increasing
+ * slot order within an expert. */
+moe_status moe_segments(moe_layer* layer, const int32_t* topk_idx, int32_t T, int32_t* offsets,
+                        int32_t* perm, void* stream);
+
+/* Row RMS normalisation used between the layers of a stack:
+ * out[t] = bf16( x[t] / sqrt(mean(x[t]^2) + eps) ), computed in fp32.
+ * out may alias x.  H a multiple of 8, at most 65536. */
+moe_status moe_rmsnorm(const void* x, int32_t T, int32_t H, float eps, void* out, void* stream);
+
+/* Waits for the stream and reports any device error the layer's kernels
+ * recorded (MOE_ERR_INTERNAL / MOE_ERR_TIMEOUT) or CUDA reported; clears the
+ * layer's recorded error. */
+moe_status moe_sync(moe_layer* layer, void* stream);
+
+/* Options (moe_set_option):
+ *  MOE_OPT_PATH    0 = automatic by per-expert load, 1 = always the SIMT
+ *                  streaming kernels, 2 = always the tensor-core kernels
+ *                  (MOE_ERR_UNSUPPORTED if the build has none).
+ *  MOE_OPT_TIMING  1 = record CUDA events around each kernel the layer
+ *                  launches (read with moe_get_kernel_times), 0 = off.   */
+enum { MOE_OPT_PATH = 1, MOE_OPT_TIMING = 2 };
+moe_status moe_set_option(moe_layer* layer, int32_t option, int64_t value);
+
+/* Per-kernel timing gathered while MOE_OPT_TIMING is on (synchronises the
+ * layer's device).  Fills up to `cap` entries: names[i] points to a static
+ * string, ms[i] is the summed event time and launches[i] the count.  Stores
+ * the number of kernels in *n, then resets the counters. */
+moe_status moe_get_kernel_times(moe_layer* layer, const char** names, double* ms,
+                                int64_t* launches, int32_t cap, int32_t* n);
+
+const char* moe_status_string(moe_status s);
+int32_t moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H */

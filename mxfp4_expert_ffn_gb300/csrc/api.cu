@@ -1,0 +1,458 @@
+// The C ABI (include/moe_ffn.h): validation, workspace, launch sequencing,
+// error reporting, optional per-kernel timing and host-side fault injection.
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+cudaError_t prepare_segments_kernel(int E);
+cudaError_t prepare_ffn_simt(int H, int I);
+}  // namespace moe
+
+namespace {
+
+using namespace moe;
+
+// Host-side fault injection for tests: MOE_FAULT=alloc makes
+// moe_layer_create fail before allocating, MOE_FAULT=launch makes
+// moe_forward / moe_route fail before launching, MOE_FAULT=arg makes them
+// reject their arguments.  Nothing is injected on the device.
+bool fault(const char* what) {
+  const char* f = getenv("MOE_FAULT");
+  return f && strcmp(f, what) == 0;
+}
+
+moe_status cuda_fail(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  cudaGetLastError();  // clear the (non-sticky) error state
+  return MOE_ERR_CUDA;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Carver {
+  char* base;
+  size_t off = 0;
+  template <class T>
+  T* take(size_t n) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off = align_up(off + n * sizeof(T), 256);
+    return p;
+  }
+};
+
+// Lays out the workspace in one allocation (base = nullptr: sizing pass).
+size_t carve(const moe_config& c, char* base, Workspace& ws) {
+  const size_t T = (size_t)c.max_tokens, H = (size_t)c.hidden, I = (size_t)c.inter;
+  const size_t k = (size_t)c.top_k, E = (size_t)c.n_experts, ns = (size_t)c.n_shared;
+  const size_t NE = E + ns, S = T * k, P = S + ns * T;
+  Carver cv{base};
+  ws.xq = cv.take<uint8_t>(T * H);
+  ws.xs = cv.take<uint8_t>(T * H / 32);
+  ws.cnt = cv.take<int32_t>(NE);
+  ws.off = cv.take<int32_t>(NE + 1);
+  ws.perm = cv.take<int32_t>(S);
+  ws.slot_pos = cv.take<int32_t>(S);
+  ws.pos_tok = cv.take<int32_t>(P);
+  ws.active = cv.take<int32_t>(NE);
+  ws.n_active = cv.take<int32_t>(1);
+  ws.hq = cv.take<uint8_t>(P * I);
+  ws.hs = cv.take<uint8_t>(P * I / 32);
+  ws.o = cv.take<float>(P * H);
+  ws.logits = cv.take<float>(T * E);
+  ws.idx = cv.take<int32_t>(T * k);
+  ws.w = cv.take<float>(T * k);
+  ws.x = cv.take<uint16_t>(T * H);
+  ws.y = cv.take<uint16_t>(T * H);
+  ws.err = cv.take<int32_t>(1);
+  return cv.off;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+moe_status validate_config(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  const bool ok = c->hidden >= 128 && c->hidden <= 16384 && c->hidden % 128 == 0 &&
+                  c->inter >= 128 && c->inter <= 16384 && c->inter % 128 == 0 &&
+                  c->n_experts >= 1 && c->n_experts <= 512 && c->top_k >= 1 && c->top_k <= 8 &&
+                  c->top_k <= c->n_experts && c->n_shared >= 0 && c->n_shared <= 4 &&
+                  c->max_tokens >= 1 && c->max_tokens <= 65535;
+  return ok ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+moe_status validate_weights(const moe_config* c, const moe_weights* w) {
+  if (!w || !w->router_w) return MOE_ERR_INVALID_ARG;
+  const moe_mx_mat* routed[3] = {&w->gate, &w->up, &w->down};
+  const moe_mx_mat* shared[3] = {&w->s_gate, &w->s_up, &w->s_down};
+  for (int i = 0; i < 3; ++i) {
+    if (!routed[i]->codes || !routed[i]->scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned(routed[i]->codes, 32) || !aligned(routed[i]->scales, 32)) return MOE_ERR_INVALID_ARG;
+    if (c->n_shared > 0) {
+      if (!shared[i]->codes || !shared[i]->scales) return MOE_ERR_INVALID_ARG;
+      if (!aligned(shared[i]->codes, 32) || !aligned(shared[i]->scales, 32)) return MOE_ERR_INVALID_ARG;
+    }
+  }
+  if (!aligned(w->router_w, 16)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+ExpertBank bank_of(const moe_layer* L) {
+  ExpertBank b;
+  b.gc = L->w.gate.codes;
+  b.gs = L->w.gate.scales;
+  b.uc = L->w.up.codes;
+  b.us = L->w.up.scales;
+  b.dc = L->w.down.codes;
+  b.ds = L->w.down.scales;
+  b.sgc = L->w.s_gate.codes;
+  b.sgs = L->w.s_gate.scales;
+  b.suc = L->w.s_up.codes;
+  b.sus = L->w.s_up.scales;
+  b.sdc = L->w.s_down.codes;
+  b.sds = L->w.s_down.scales;
+  b.E = L->cfg.n_experts;
+  b.H = L->cfg.hidden;
+  b.I = L->cfg.inter;
+  return b;
+}
+
+// Makes the layer's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  cudaError_t status = cudaSuccess;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) status = cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+// Records a pair of events around one launch while timing is on.
+struct TimedScope {
+  moe_layer* L;
+  cudaStream_t st;
+  int pair = -1;
+  TimedScope(moe_layer* layer, cudaStream_t s, const char* name) : L(layer), st(s) {
+    if (!L || !L->timing || L->ev_used >= 64) return;
+    int t = 0;
+    while (t < L->n_timers && strcmp(L->timers[t].name, name) != 0) ++t;
+    if (t == L->n_timers) {
+      if (t == kMaxTimed) return;
+      L->timers[t].name = name;
+      L->n_timers++;
+    }
+    pair = L->ev_used++;
+    L->ev_pending_timer[pair] = t;
+    cudaEventRecord(L->ev_pool[2 * pair], st);
+  }
+  ~TimedScope() {
+    if (pair >= 0) cudaEventRecord(L->ev_pool[2 * pair + 1], st);
+  }
+};
+
+void collect_times(moe_layer* L) {
+  for (int p = 0; p < L->ev_used; ++p) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, L->ev_pool[2 * p], L->ev_pool[2 * p + 1]) == cudaSuccess) {
+      L->timers[L->ev_pending_timer[p]].ms += ms;
+      L->timers[L->ev_pending_timer[p]].launches += 1;
+    }
+  }
+  cudaGetLastError();
+  L->ev_used = 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case MOE_ERR_OOM: return "device memory allocation failed";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_INTERNAL: return "device-side check failed (expert id out of range)";
+  }
+  return "unknown status";
+}
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int device,
+                            moe_layer** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  moe_status st = validate_config(cfg);
+  if (st != MOE_OK) return st;
+  if ((st = validate_weights(cfg, w)) != MOE_OK) return st;
+  if (fault("alloc")) return MOE_ERR_OOM;
+  DeviceGuard g(device);
+  if (g.status != cudaSuccess) return cuda_fail(g.status);
+  moe_layer* L = new (std::nothrow) moe_layer();
+  if (!L) return MOE_ERR_OOM;
+  L->cfg = *cfg;
+  L->w = *w;
+  L->device = device;
+  if (cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    delete L;
+    return cuda_fail(cudaErrorInvalidDevice);
+  }
+  Workspace sizing;
+  const size_t bytes = carve(*cfg, nullptr, sizing);
+  void* base = nullptr;
+  if (cudaMalloc(&base, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete L;
+    return MOE_ERR_OOM;
+  }
+  carve(*cfg, static_cast<char*>(base), L->ws);
+  L->ws.base = base;
+  L->ws.bytes = bytes;
+  cudaError_t e = cudaMemset(L->ws.err, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMallocHost(&L->ws.err_host, sizeof(int32_t));
+  if (e == cudaSuccess) e = prepare_segments_kernel(cfg->n_experts);
+  if (e == cudaSuccess) e = prepare_ffn_simt(cfg->hidden, cfg->inter);
+  if (e != cudaSuccess) {
+    if (L->ws.err_host) cudaFreeHost(L->ws.err_host);
+    cudaFree(base);
+    delete L;
+    return cuda_fail(e);
+  }
+  *out = L;
+  return MOE_OK;
+}
+
+moe_status moe_layer_destroy(moe_layer* L) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  for (int i = 0; i < 128; ++i)
+    if (L->ev_pool[i]) cudaEventDestroy(L->ev_pool[i]);
+  if (L->ws.err_host) cudaFreeHost(L->ws.err_host);
+  cudaFree(L->ws.base);
+  delete L;
+  return cuda_fail(e);
+}
+
+moe_status moe_set_option(moe_layer* L, int32_t option, int64_t value) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (option == MOE_OPT_PATH) {
+    if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+    if (value == 2) return MOE_ERR_UNSUPPORTED;
+    L->path = (int)value;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_TIMING) {
+    DeviceGuard g(L->device);
+    if (value && !L->ev_pool[0]) {
+      for (int i = 0; i < 128; ++i)
+        if (cudaEventCreate(&L->ev_pool[i]) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+    }
+    L->timing = value != 0;
+    return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+moe_status moe_get_kernel_times(moe_layer* L, const char** names, double* ms, int64_t* launches,
+                                int32_t cap, int32_t* n) {
+  if (!L || !n || cap < 0 || (cap > 0 && (!names || !ms || !launches))) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  collect_times(L);
+  *n = L->n_timers;
+  for (int i = 0; i < L->n_timers && i < cap; ++i) {
+    names[i] = L->timers[i].name;
+    ms[i] = L->timers[i].ms;
+    launches[i] = L->timers[i].launches;
+  }
+  for (int i = 0; i < L->n_timers; ++i) {
+    L->timers[i].ms = 0.0;
+    L->timers[i].launches = 0;
+  }
+  return cuda_fail(e);
+}
+
+moe_status moe_sync(moe_layer* L, void* stream) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(L->ws.err_host, L->ws.err, sizeof(int32_t),
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int32_t bits = *L->ws.err_host;
+  if (bits) {
+    e = cudaMemsetAsync(L->ws.err, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return (bits & kErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_INTERNAL;
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+moe_status check_tokens(const moe_layer* L, int32_t T) {
+  if (!L || T < 0 || T > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (fault("arg")) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status route_impl(moe_layer* L, const void* x, int32_t T, const float* logits_in,
+                      float* logits_out, int32_t* idx, float* w, cudaStream_t st) {
+  const moe_config& c = L->cfg;
+  cudaError_t e = cudaSuccess;
+  const float* lg = logits_in;
+  if (!lg) {
+    float* dst = logits_out ? logits_out : L->ws.logits;
+    TimedScope ts(L, st, "router_logits");
+    e = launch_router_logits(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts,
+                             L->w.router_w, L->w.router_b, dst, L->num_sms, st);
+    lg = dst;
+  } else if (logits_out && logits_out != logits_in) {
+    e = cudaMemcpyAsync(logits_out, logits_in, sizeof(float) * (size_t)T * c.n_experts,
+                        cudaMemcpyDeviceToDevice, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    TimedScope ts(L, st, "topk");
+    e = launch_topk(lg, T, c.n_experts, c.top_k, idx, w, st);
+  }
+  return cuda_fail(e);
+}
+
+moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* idx,
+                        const float* w, const void* residual, void* y, cudaStream_t st) {
+  const moe_config& c = L->cfg;
+  const ExpertBank bank = bank_of(L);
+  cudaError_t e;
+  {
+    TimedScope ts(L, st, "segments");
+    e = launch_segments(idx, T, c.top_k, c.n_experts, c.n_shared, L->ws, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    TimedScope ts(L, st, "quantize_act");
+    e = launch_quantize_act(static_cast<const uint16_t*>(x), T, c.hidden, L->ws.xq, L->ws.xs, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    TimedScope ts(L, st, "ffn_up_simt");
+    e = launch_ffn_up_simt(bank, T, c.top_k, c.n_shared, L->ws, L->num_sms, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    TimedScope ts(L, st, "ffn_down_simt");
+    e = launch_ffn_down_simt(bank, T, c.top_k, c.n_shared, L->ws, L->num_sms, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    TimedScope ts(L, st, "combine");
+    e = launch_combine(L->ws, T, c.hidden, c.top_k, c.n_shared, w,
+                       static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(y), st);
+  }
+  return cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_route(moe_layer* L, const void* x, int32_t T, const float* logits_in,
+                     float* logits_out, int32_t* topk_idx, float* topk_w, void* stream) {
+  moe_status s = check_tokens(L, T);
+  if (s != MOE_OK || T == 0) return s;
+  if (!topk_idx || !topk_w || (!logits_in && !x)) return MOE_ERR_INVALID_ARG;
+  if (x && !aligned(x, 16)) return MOE_ERR_INVALID_ARG;
+  if (fault("launch")) return MOE_ERR_CUDA;
+  DeviceGuard g(L->device);
+  if (g.status != cudaSuccess) return cuda_fail(g.status);
+  return route_impl(L, x, T, logits_in, logits_out, topk_idx, topk_w,
+                    static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward(moe_layer* L, const void* x, int32_t T, const int32_t* topk_idx,
+                       const float* topk_w, const void* residual, void* y, void* stream) {
+  moe_status s = check_tokens(L, T);
+  if (s != MOE_OK || T == 0) return s;
+  if (!x || !topk_idx || !topk_w || !y || x == y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || (residual && !aligned(residual, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if (fault("launch")) return MOE_ERR_CUDA;
+  DeviceGuard g(L->device);
+  if (g.status != cudaSuccess) return cuda_fail(g.status);
+  return forward_impl(L, x, T, topk_idx, topk_w, residual, y, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_host(moe_layer* L, const void* x_host, int32_t T, void* y_host,
+                            void* stream) {
+  moe_status s = check_tokens(L, T);
+  if (s != MOE_OK || T == 0) return s;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  if (fault("launch")) return MOE_ERR_CUDA;
+  DeviceGuard g(L->device);
+  if (g.status != cudaSuccess) return cuda_fail(g.status);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)T * L->cfg.hidden * sizeof(uint16_t);
+  cudaError_t e = cudaMemcpyAsync(L->ws.x, x_host, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((s = route_impl(L, L->ws.x, T, nullptr, nullptr, L->ws.idx, L->ws.w, st)) != MOE_OK) return s;
+  if ((s = forward_impl(L, L->ws.x, T, L->ws.idx, L->ws.w, nullptr, L->ws.y, st)) != MOE_OK) return s;
+  e = cudaMemcpyAsync(y_host, L->ws.y, bytes, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return moe_sync(L, stream);
+}
+
+moe_status moe_quantize_act(moe_layer* L, const void* x, int32_t T, uint8_t* q, uint8_t* s,
+                            void* stream) {
+  moe_status st = check_tokens(L, T);
+  if (st != MOE_OK || T == 0) return st;
+  if (!x || !q || !s || !aligned(x, 16) || !aligned(q, 8)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  if (g.status != cudaSuccess) return cuda_fail(g.status);
+  TimedScope ts(L, static_cast<cudaStream_t>(stream), "quantize_act");
+  return cuda_fail(launch_quantize_act(static_cast<const uint16_t*>(x), T, L->cfg.hidden, q, s,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_segments(moe_layer* L, const int32_t* topk_idx, int32_t T, int32_t* offsets,
+                        int32_t* perm, void* stream) {
+  moe_status s = check_tokens(L, T);
+  if (s != MOE_OK) return s;
+  if (!topk_idx || !offsets || !perm) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  if (g.status != cudaSuccess) return cuda_fail(g.status);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const moe_config& c = L->cfg;
+  cudaError_t e = launch_segments(topk_idx, T, c.top_k, c.n_experts, c.n_shared, L->ws, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(offsets, L->ws.off, sizeof(int32_t) * (c.n_experts + 1),
+                        cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && T > 0)
+    e = cudaMemcpyAsync(perm, L->ws.perm, sizeof(int32_t) * (size_t)T * c.top_k,
+                        cudaMemcpyDeviceToDevice, st);
+  return cuda_fail(e);
+}
+
+moe_status moe_rmsnorm(const void* x, int32_t T, int32_t H, float eps, void* out, void* stream) {
+  if (T < 0 || H <= 0 || H % 8 != 0 || H > 65536 || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !out || !aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  return cuda_fail(launch_rmsnorm(static_cast<const uint16_t*>(x), T, H, eps,
+                                  static_cast<uint16_t*>(out), static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// Internal declarations: the layer handle and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_ffn.h"
+
+namespace moe {
+
+constexpr int kMaxTimed = 16;
+
+// Device workspace, sized at create time for cfg.max_tokens.
+// Positions: the T*k routed slots grouped expert by expert (stable in slot
+// order), then n_shared blocks of T positions for the shared experts
+// (position S + s*T + t is token t of shared expert s).
+struct Workspace {
+  uint8_t* xq = nullptr;      // [T][H]     E4M3 codes of x
+  uint8_t* xs = nullptr;      // [T][H/32]  UE8M0 scale bytes of x
+  int32_t* cnt = nullptr;     // [NE]       tokens per expert (NE = E + n_shared)
+  int32_t* off = nullptr;     // [NE+1]     first position of each expert
+  int32_t* perm = nullptr;    // [T*k]      slot of each routed position
+  int32_t* slot_pos = nullptr;// [T*k]      position of each slot (-1: invalid id)
+  int32_t* pos_tok = nullptr; // [P]        token of each position
+  int32_t* active = nullptr;  // [NE]       experts with tokens, routed then shared
+  int32_t* n_active = nullptr;// [1]
+  uint8_t* hq = nullptr;      // [P][I]     E4M3 codes of h
+  uint8_t* hs = nullptr;      // [P][I/32]  UE8M0 scale bytes of h
+  float* o = nullptr;         // [P][H]     expert outputs per position
+  float* logits = nullptr;    // [T][E]     router logits scratch
+  int32_t* idx = nullptr;     // [T][k]     routing scratch (host entry point)
+  float* w = nullptr;         // [T][k]
+  uint16_t* x = nullptr;      // [T][H]     bf16 staging (host entry point)
+  uint16_t* y = nullptr;      // [T][H]
+  int32_t* err = nullptr;     // [1]        device error word
+  int32_t* err_host = nullptr;// pinned copy of err
+  void* base = nullptr;       // single allocation holding all of the above
+  size_t bytes = 0;
+};
+
+struct Timer {
+  const char* name = nullptr;
+  double ms = 0.0;
+  int64_t launches = 0;
+};
+
+}  // namespace moe
+
+struct moe_layer {
+  moe_config cfg;
+  moe_weights w;
+  int device = 0;
+  int num_sms = 0;
+  int path = 0;
+  bool timing = false;
+  moe::Workspace ws;
+  moe::Timer timers[moe::kMaxTimed];
+  int n_timers = 0;
+  cudaEvent_t ev_pool[2 * 64] = {};
+  int ev_used = 0;
+  int ev_pending_timer[64] = {};
+};
+
+namespace moe {
+
+// Expert weight pointers for expert id e (routed 0..E-1, shared E..E+ns-1).
+struct ExpertBank {
+  const uint8_t *gc, *gs, *uc, *us, *dc, *ds;       // routed banks
+  const uint8_t *sgc, *sgs, *suc, *sus, *sdc, *sds; // shared banks
+  int E, H, I;
+};
+
+// --- launchers (return the launch's cudaError_t) ---------------------------
+cudaError_t launch_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s,
+                                cudaStream_t st);
+cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared,
+                            const Workspace& ws, cudaStream_t st);
+cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const float* W,
+                                 const float* b, float* logits, int num_sms, cudaStream_t st);
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                        cudaStream_t st);
+cudaError_t launch_ffn_up_simt(const ExpertBank& bank, int T, int k, int n_shared,
+                               const Workspace& ws, int num_sms, cudaStream_t st);
+cudaError_t launch_ffn_down_simt(const ExpertBank& bank, int T, int k, int n_shared,
+                                 const Workspace& ws, int num_sms, cudaStream_t st);
+cudaError_t launch_combine(const Workspace& ws, int T, int H, int k, int n_shared,
+                           const float* w, const uint16_t* residual, uint16_t* y,
+                           cudaStream_t st);
+cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out,
+                           cudaStream_t st);
+
+}  // namespace moe

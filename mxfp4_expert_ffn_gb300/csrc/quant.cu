@@ -1,0 +1,277 @@
+// Activation quantisation, expert segments, combine and RMS normalisation.
+//
+// Quantisation: the dynamic per-32 FP8 activation scheme of the checkpoint
+// (FreeToken issue #444, "Is the quantization already supported":
+// activation_scheme dynamic, scale_fmt ue8m0).  Segments and combine: the
+// routed MoE block (384 routed + 1 shared, top-6; same issue, "Architecture
+// delta vs deepseek_v4").  All four are HBM- or latency-bound and run on the
+// SIMT pipes with 128-bit accesses.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// One thread per 8 bf16 values; four consecutive threads form one 32-block.
+__global__ void quantize_act_kernel(const uint4* __restrict__ x, int n8, uint2* __restrict__ q,
+                                    uint8_t* __restrict__ s) {
+  const int lane = threadIdx.x & 31;
+  const unsigned quad = 0xFu << (lane & ~3);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += gridDim.x * blockDim.x) {
+    const uint4 v = x[i];
+    float f[8];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 2));
+    const int e = fp8_block_exponent(amax);
+    uint32_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      c[j] = e4m3x2(scale_pow2_neg(f[2 * j], e), scale_pow2_neg(f[2 * j + 1], e));
+    q[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    if ((lane & 3) == 0) s[i >> 2] = (uint8_t)(e + 127);
+  }
+}
+
+// Builds the expert segments in one CTA of 1024 threads.  Each warp owns a
+// contiguous range of slots; pass 1 counts its slots per expert, pass 2 turns
+// the counts into per-warp bases (warps in slot order), pass 3 places each
+// slot at base + rank among the warp's equal-expert lanes.  The result is a
+// stable counting sort, identical on every run.
+__global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restrict__ idx, int T,
+                                                        int k, int E, int ns, Workspace ws) {
+  extern __shared__ int32_t sm[];
+  const int NE = E + ns;
+  int32_t* wcnt = sm;            // [32][E]  per-warp counts, then running bases
+  int32_t* stot = sm + 32 * E;   // [E]      totals, then exclusive offsets
+  const int S = T * k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int per = (S + 31) / 32;
+  const int lo = min(S, warp * per), hi = min(S, lo + per);
+  for (int b = lo; b < hi; b += 32) {
+    const int s = b + lane;
+    int e = -1;
+    if (s < hi) {
+      e = idx[s];
+      if (e < 0 || e >= E) {
+        raise_error(ws.err, kErrExpertRange);
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+    stot[e] = run;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scan of the E totals and of the "has tokens" flags
+    const int chunk = (E + 31) / 32;
+    const int c0 = min(E, lane * chunk), c1 = min(E, c0 + chunk);
+    int sum = 0, nf = 0;
+    for (int e = c0; e < c1; ++e) {
+      sum += stot[e];
+      nf += stot[e] > 0;
+    }
+    int isum = sum, inf = nf;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xFFFFFFFFu, isum, o);
+      const int f = __shfl_up_sync(0xFFFFFFFFu, inf, o);
+      if (lane >= o) {
+        isum += a;
+        inf += f;
+      }
+    }
+    int run = isum - sum, fr = inf - nf;
+    for (int e = c0; e < c1; ++e) {
+      const int c = stot[e];
+      ws.cnt[e] = c;
+      ws.off[e] = run;
+      stot[e] = run;
+      if (c > 0) ws.active[fr++] = e;
+      run += c;
+    }
+    const int n_routed_active = __shfl_sync(0xFFFFFFFFu, inf, 31);
+    if (lane == 0) {
+      for (int sh = 0; sh < ns; ++sh) {
+        ws.cnt[E + sh] = T;
+        ws.off[E + sh] = S + sh * T;
+        if (T > 0) ws.active[n_routed_active + sh] = E + sh;
+      }
+      ws.off[NE] = S + ns * T;
+      *ws.n_active = n_routed_active + (T > 0 ? ns : 0);
+    }
+  }
+  __syncthreads();
+  for (int b = lo; b < hi; b += 32) {
+    const int s = b + lane;
+    int e = -1;
+    if (s < hi) {
+      e = idx[s];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (e >= 0) {
+      const int p = stot[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
+      ws.perm[p] = s;
+      ws.slot_pos[s] = p;
+      ws.pos_tok[p] = s / k;
+    } else if (s < hi) {
+      ws.slot_pos[s] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  for (int i = threadIdx.x; i < ns * T; i += blockDim.x) ws.pos_tok[S + i] = i % T;
+}
+
+// y[t] = bf16( sum_s o[S + s*T + t] + sum_j w[t][j] * o[slot_pos[t*k + j]] ),
+// accumulated in fp32 in that fixed order; optional residual added to the
+// bf16-rounded sum.  Four consecutive h per thread.
+__global__ void combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_pos,
+                               const float* __restrict__ w, int T, int H, int k, int ns,
+                               const uint16_t* __restrict__ res, uint16_t* __restrict__ y) {
+  const int t = blockIdx.y;
+  const int h = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (h >= H) return;
+  const size_t S = (size_t)T * k;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < ns; ++s) {
+    const float4 v = *reinterpret_cast<const float4*>(o + (S + (size_t)s * T + t) * H + h);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  for (int j = 0; j < k; ++j) {
+    const int p = slot_pos[(size_t)t * k + j];
+    if (p < 0) continue;
+    const float wj = w[(size_t)t * k + j];
+    const float4 v = *reinterpret_cast<const float4*>(o + (size_t)p * H + h);
+    acc.x = fmaf(wj, v.x, acc.x);
+    acc.y = fmaf(wj, v.y, acc.y);
+    acc.z = fmaf(wj, v.z, acc.z);
+    acc.w = fmaf(wj, v.w, acc.w);
+  }
+  float r[4] = {acc.x, acc.y, acc.z, acc.w};
+  uint16_t b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) b[i] = __bfloat16_as_ushort(__float2bfloat16_rn(r[i]));
+  if (res) {
+    const uint2 rv = *reinterpret_cast<const uint2*>(res + (size_t)t * H + h);
+    const uint16_t rb[4] = {(uint16_t)(rv.x & 0xFFFF), (uint16_t)(rv.x >> 16),
+                            (uint16_t)(rv.y & 0xFFFF), (uint16_t)(rv.y >> 16)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      b[i] = __bfloat16_as_ushort(
+          __float2bfloat16_rn(bf16_bits_to_float(rb[i]) + bf16_bits_to_float(b[i])));
+  }
+  *reinterpret_cast<uint2*>(y + (size_t)t * H + h) =
+      make_uint2(b[0] | ((uint32_t)b[1] << 16), b[2] | ((uint32_t)b[3] << 16));
+}
+
+// out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)); fixed-order block reduction.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* __restrict__ x, int H,
+                                                      float eps, uint16_t* __restrict__ out) {
+  __shared__ float red[256];
+  const int t = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
+    const uint4 v = xr[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
+      ss = fmaf(a, a, ss);
+      ss = fmaf(b, b, ss);
+    }
+  }
+  red[threadIdx.x] = ss;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  const float inv = 1.0f / sqrtf(red[0] / (float)H + eps);
+  uint4* outr = reinterpret_cast<uint4*>(out + (size_t)t * H);
+  for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
+    const uint4 v = xr[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = __uint_as_float(w[j] << 16) * inv;
+      const float b = __uint_as_float(w[j] & 0xFFFF0000u) * inv;
+      r[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+    }
+    // out may alias x: each thread writes only the elements it reads here, and
+    // every read of the sum-of-squares pass finished before the reduction.
+    outr[i] = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s,
+                                cudaStream_t st) {
+  const int n8 = T * (H / 8);
+  if (n8 == 0) return cudaSuccess;
+  int blocks = (n8 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  quantize_act_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), n8,
+                                               reinterpret_cast<uint2*>(q), s);
+  return cudaGetLastError();
+}
+
+size_t segments_smem_bytes(int E) { return (size_t)(33 * E) * sizeof(int32_t); }
+
+cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared,
+                            const Workspace& ws, cudaStream_t st) {
+  segments_kernel<<<1, 1024, segments_smem_bytes(E), st>>>(idx, T, k, E, n_shared, ws);
+  return cudaGetLastError();
+}
+
+cudaError_t prepare_segments_kernel(int E) {
+  return cudaFuncSetAttribute(segments_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)segments_smem_bytes(E));
+}
+
+cudaError_t launch_combine(const Workspace& ws, int T, int H, int k, int n_shared, const float* w,
+                           const uint16_t* residual, uint16_t* y, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  dim3 grid((H / 4 + 255) / 256, T);
+  combine_kernel<<<grid, 256, 0, st>>>(ws.o, ws.slot_pos, w, T, H, k, n_shared, residual, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out,
+                           cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  rmsnorm_kernel<<<T, 256, 0, st>>>(x, H, eps, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

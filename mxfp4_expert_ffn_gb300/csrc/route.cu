@@ -1,0 +1,134 @@
+// Router: fp32 logits l = W_r x + b, then per-token top-k with ties to the
+// lower expert index and a softmax over the selected logits.
+//
+// The gate is a discrete switch (ai.rs, "What remains is the reference
+// rounding itself"; llama.cpp discussion #28766, "Correctness": 6th-to-7th
+// margin about 1 %), so the selection is exact given the fp32 logits.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kRouterWarps = 8;
+
+// One warp per (expert, group of TT tokens).  Lanes stride over H four
+// elements at a time: a float4 of the expert's row and four bf16 per token.
+template <int TT>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+    router_logits_kernel(const uint16_t* __restrict__ x, int T, int H, int E,
+                         const float* __restrict__ W, const float* __restrict__ b,
+                         float* __restrict__ logits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRouterWarps + warp;
+  if (e >= E) return;
+  const int t0 = blockIdx.y * TT;
+  const int nt = min(TT, T - t0);
+  float acc[TT];
+#pragma unroll
+  for (int i = 0; i < TT; ++i) acc[i] = 0.f;
+  const float4* wr = reinterpret_cast<const float4*>(W + (size_t)e * H);
+  for (int h4 = lane; h4 < H / 4; h4 += 32) {
+    const float4 wv = __ldg(wr + h4);
+#pragma unroll
+    for (int i = 0; i < TT; ++i) {
+      if (i < nt) {
+        const uint2 xv = *reinterpret_cast<const uint2*>(x + (size_t)(t0 + i) * H + 4 * h4);
+        acc[i] = fmaf(wv.x, __uint_as_float(xv.x << 16), acc[i]);
+        acc[i] = fmaf(wv.y, __uint_as_float(xv.x & 0xFFFF0000u), acc[i]);
+        acc[i] = fmaf(wv.z, __uint_as_float(xv.y << 16), acc[i]);
+        acc[i] = fmaf(wv.w, __uint_as_float(xv.y & 0xFFFF0000u), acc[i]);
+      }
+    }
+  }
+  const float bias = b ? b[e] : 0.f;
+#pragma unroll
+  for (int i = 0; i < TT; ++i) {
+    const float s = warp_sum(acc[i]);
+    if (lane == 0 && i < nt) logits[(size_t)(t0 + i) * E + e] = s + bias;
+  }
+}
+
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// One warp per token; lane l holds logits l, l+32, ... (E <= 512).  k rounds
+// of a warp arg-max over (value desc, index asc); NaN counts as -infinity.
+__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                            int32_t* __restrict__ idx, float* __restrict__ w) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int e = lane + 32 * i;
+    float f = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+    v[i] = isnan(f) ? -INFINITY : f;
+  }
+  uint32_t taken = 0;
+  float sv[8];
+  int si[8];
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && ranks_before(v[i], e, bv, bi)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      if (ranks_before(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    sv[r] = bv;
+    si[r] = bi;
+  }
+  if (lane == 0) {
+    const float m = sv[0];
+    float den = 0.f;
+    for (int r = 0; r < k; ++r) den += expf(sv[r] - m);
+    for (int r = 0; r < k; ++r) {
+      idx[(size_t)t * k + r] = si[r];
+      w[(size_t)t * k + r] = expf(sv[r] - m) / den;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const float* W,
+                                 const float* b, float* logits, int num_sms, cudaStream_t st) {
+  (void)num_sms;
+  if (T == 0) return cudaSuccess;
+  const int gx = (E + kRouterWarps - 1) / kRouterWarps;
+  if (T <= 2) {
+    router_logits_kernel<2><<<dim3(gx, (T + 1) / 2), kRouterWarps * 32, 0, st>>>(x, T, H, E, W, b,
+                                                                                logits);
+  } else {
+    router_logits_kernel<8><<<dim3(gx, (T + 7) / 8), kRouterWarps * 32, 0, st>>>(x, T, H, E, W, b,
+                                                                                logits);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                        cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, k, idx, w);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
