@@ -1,0 +1,370 @@
+"""Benchmark of one MXFP4 MoE layer step on GB300.
+
+A step is one pass of the whole hot path over one batch: router logits,
+top-k, segments, FP8 activation quantisation, gate/up + SwiGLU + h
+quantisation, down, combine.  The default workload is one
+DeepSeek-V4.1-shaped layer at decode batch 1 (hidden 5120, intermediate 2304,
+384 routed experts top-6 + 1 shared, all experts resident); other workloads
+are selectable with --workload for profiling.
+
+Prints ONE JSON line (rank 0).  `value` is layer tokens/s with inputs
+resident in HBM; each step gets a fresh token and the L2 is flushed between
+steps (outside the timed events).  `e2e` is the same metric through
+moe_forward_host with pinned host buffers (copies inside the timed region).
+`--impl reference` times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from synth.workloads import WORKLOADS  # noqa: E402
+
+DEFAULT = "v41_layer_decode_t1"
+METRIC = "MoE-layer tokens/s; decode HBM GB/s vs peak; prefill FP4 TFLOPS vs peak"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    p.add_argument("--path", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor cores")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        if self.p:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        self.f.flush()
+        rows = []
+        try:
+            for line in open(self.f.name):
+                parts = [s.strip() for s in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        except Exception:
+            pass
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def layer_bytes(wl, n_experts_touched: int, T: int) -> dict:
+    """Algorithmic HBM bytes of one layer step and of its two FFN kernels."""
+    H, I, E, k, ns = wl.hidden, wl.inter, wl.n_experts, wl.top_k, wl.n_shared
+    P = T * k + ns * T
+    per_mat = H * I // 2 + H * I // 32
+    n = n_experts_touched + ns
+    up = n * 2 * per_mat + T * (H + H // 32) + P * (I + I // 32)
+    down = n * per_mat + P * (I + I // 32) + P * H * 4
+    layer = n * wl.expert_bytes + E * H * 4 + E * 4 + 2 * T * H * 2
+    return {"layer": layer, "ffn_up_simt": up, "ffn_down_simt": down,
+            "ffn_up_mma": up, "ffn_down_mma": down}
+
+
+def layer_flops(wl, T: int) -> int:
+    return (T * wl.top_k + wl.n_shared * T) * 3 * 2 * wl.hidden * wl.inter
+
+
+def oracle_tokens_per_s(wl, n_tokens: int, threads: int, stream: int = 50):
+    """Times the fp64 oracle (routing + layer) on n_tokens seeded tokens.
+    Expert bytes are regenerated before the clock starts (input generation)."""
+    import oracle
+    import synth
+    nl = wl.layers
+    x = synth.activations(wl, tokens=n_tokens, stream=stream)
+    # pre-generate the experts the sample touches, layer by layer
+    banks, t_total = [], 0.0
+    cur = x
+    for layer in range(nl):
+        xin = oracle.rmsnorm(cur, 1e-6) if wl.rmsnorm else cur
+        Wr, b = synth.router_weights(wl, layer), synth.router_bias(wl, layer)
+        t0 = time.perf_counter()
+        lg = oracle.router_logits(xin, Wr, b, threads=threads)
+        idx, w = oracle.topk(lg, wl.top_k)
+        t_total += time.perf_counter() - t0
+        ex = {int(e): synth.host_expert(wl, layer, int(e)) for e in np.unique(idx)}
+        sh = [synth.host_expert(wl, layer, wl.n_experts + s) for s in range(wl.n_shared)]
+        t0 = time.perf_counter()
+        y, _ = oracle.moe_layer(xin, idx, w, ex, sh, wl.n_experts, wl.inter,
+                                residual=cur if wl.rmsnorm else None, threads=threads)
+        t_total += time.perf_counter() - t0
+        if wl.rmsnorm:
+            t0 = time.perf_counter()
+            oracle.rmsnorm(cur, 1e-6)
+            t_total += time.perf_counter() - t0
+        cur = y
+        banks.append(len(ex))
+    return n_tokens / t_total, t_total
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    wl = WORKLOADS[args.workload]
+    cores = os.cpu_count() or 1
+    threads = min(cores, oracle.max_threads())
+    n_tok = max(1, min(threads, 8 if wl.tokens < 512 else 16))
+    for i in range(args.warmup):
+        oracle_tokens_per_s(wl, n_tok, threads, stream=200 + i)
+    total_t, total_n = 0.0, 0
+    for i in range(args.steps):
+        _, t = oracle_tokens_per_s(wl, n_tok, threads, stream=300 + i)
+        total_t += t
+        total_n += n_tok
+    v = total_n / total_t
+    sample = f"{n_tok} seeded tokens per step of workload {wl.name} (routing + layer, fp64 oracle)"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * total_t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "tokens": wl.tokens, "layers": wl.layers},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import mxfp4_expert_ffn_gb300 as m
+    import synth
+    from synth import gpu as sg
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+        pg = dist
+    wl = WORKLOADS[args.workload]
+    T, H, E, k = wl.tokens, wl.hidden, wl.n_experts, wl.top_k
+    nl = wl.layers
+    W = [sg.device_layer(wl, l, dev) for l in range(nl)]
+    Ls = [m.Layer(H, wl.inter, E, k, wl.n_shared, T, W[l]) for l in range(nl)]
+    for L in Ls:
+        L.set_option(m.MOE_OPT_PATH, args.path)
+    n_in = args.steps + args.warmup
+    xs = sg.bf16_tensor(synth.activations(wl, tokens=n_in * T, stream=100 + rank), dev).view(n_in, T, H)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wt = torch.empty((T, k), dtype=torch.float32, device=dev)
+    bufs = [torch.empty((T, H), dtype=torch.int16, device=dev) for _ in range(3)]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > 126 MB L2
+    st = torch.cuda.current_stream()
+
+    def step(i, y_out=None):
+        x = xs[i]
+        if nl == 1:
+            Ls[0].route(x, T, idx, wt)
+            Ls[0].forward(x, T, idx, wt, bufs[0] if y_out is None else y_out)
+            return
+        cur = x
+        for layer in range(nl):
+            xn, nxt = bufs[layer % 2], bufs[2] if layer == nl - 1 else bufs[(layer + 1) % 2]
+            if layer == 0:
+                nxt = bufs[1]
+            m.moe_rmsnorm(cur, T, H, 1e-6, xn)
+            Ls[layer].route(xn, T, idx, wt)
+            Ls[layer].forward(xn, T, idx, wt, nxt, residual=cur)
+            cur = nxt
+
+    def timed_loop():
+        times = []
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        for i in range(args.warmup, n_in):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            step(i)
+            e1.record(st)
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        return [a.elapsed_time(b) for a, b in times]
+
+    with ClockSampler(local) as clk:
+        ms = timed_loop()
+    clocks = clk.summary()
+    total_ms = sum(ms)
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = t.item()
+    ms_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    # union of experts per step (for byte accounting), outside the timed region
+    unions = []
+    for i in range(args.warmup, n_in):
+        if nl == 1:
+            Ls[0].route(xs[i], T, idx, wt)
+            torch.cuda.synchronize()
+            unions.append(len(np.unique(idx.cpu().numpy())))
+    mean_union = float(np.mean(unions)) if unions else None
+
+    # per-kernel times: the same loop again with the library's event timing on
+    for L in Ls:
+        L.set_option(m.MOE_OPT_TIMING, 1)
+        L.kernel_times()
+    timed_loop()
+    ktimes = {}
+    for L in Ls:
+        for name, kms, n in L.kernel_times():
+            a = ktimes.setdefault(name, [0.0, 0])
+            a[0] += kms
+            a[1] += n
+        L.set_option(m.MOE_OPT_TIMING, 0)
+    launches = sum(n for _, n in ktimes.values())
+    per_step_launches = launches // max(1, args.steps)
+    dom = max(ktimes, key=lambda n: ktimes[n][0])
+    dom_ms = ktimes[dom][0] / ktimes[dom][1]
+
+    pk = peaks()
+    roofline = None
+    if mean_union is not None:
+        b = layer_bytes(wl, mean_union, T)
+        if dom in b:
+            ach = b[dom] / (dom_ms / 1e3) / 1e9
+            roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": pk["hbm_gbs"],
+                        "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None,
+                        "algorithmic_bytes_per_launch": b[dom], "avg_launch_ms": dom_ms,
+                        "peak_src": pk["src"]}
+        layer_gbs = b["layer"] / (ms_step / 1e3) / 1e9
+    else:
+        layer_gbs = None
+
+    # end to end through the host entry point (copies inside the timed region)
+    e2e = None
+    if nl == 1:
+        xh = torch.empty((n_in, T, H), dtype=torch.int16).pin_memory()
+        xh.copy_(xs.cpu())
+        yh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+        for i in range(args.warmup):
+            Ls[0].forward_host(xh[i], T, yh)
+        tt = 0.0
+        for i in range(args.warmup, n_in):
+            flush.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            Ls[0].forward_host(xh[i], T, yh)
+            tt += time.perf_counter() - t0
+        e2e = {"value": world * T * args.steps / tt, "unit": "tokens/s",
+               "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        threads = min(os.cpu_count() or 1, oracle.max_threads())
+        n_tok = max(1, min(threads, 8))
+        v, t = oracle_tokens_per_s(wl, n_tok, threads, stream=400)
+        cpu = {"value": v, "unit": "tokens/s", "cores": min(threads, n_tok), "kind": "oracle",
+               "sample": f"{n_tok} seeded tokens of {wl.name}, routing + layer, fp64 oracle, "
+                         f"{t:.1f} s"}
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "fp4xfp8->f32", "data": "synthetic",
+                "config": {"workload": wl.name, "tokens": T, "hidden": H, "inter": wl.inter,
+                           "experts": E, "top_k": k, "shared": wl.n_shared, "layers": nl,
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                           "l2": "flushed between steps (512 MB write), fresh token each step",
+                           "mean_expert_union": mean_union},
+                "layer_gbs": layer_gbs,
+                "kernels": {n: {"ms_per_launch": a[0] / a[1], "launches": a[1]}
+                            for n, a in ktimes.items()},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": per_step_launches * args.steps, "clocks": clocks}
+        if wl.tokens >= 512:
+            line["tflops"] = layer_flops(wl, T) / (ms_step / 1e3) / 1e12
+        print(json.dumps(line), flush=True)
+    for L in Ls:
+        L.close()
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

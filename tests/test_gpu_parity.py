@@ -1,0 +1,270 @@
+"""GPU parity against the fp64 oracle through the C ABI, on small layers
+that span several work units and ragged token chunks.  Routing, x codes and
+segments are compared bit for bit; layer outputs within the layer tolerance."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import mxfp4_expert_ffn_gb300 as m
+import oracle
+import synth
+from synth import gpu as sg
+from synth.workloads import TINY, Workload
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    TINY,
+    Workload("ragged_h384_i256_e16_k2_t37", 384, 256, 16, 2, 1, 37, seed=11, scale_lo=-6, scale_hi=-2),
+    Workload("h512_i384_e40_k6_s2_t13", 512, 384, 40, 6, 2, 13, seed=12, scale_lo=-7, scale_hi=-3),
+    Workload("h256_i256_e8_k8_s0_t9", 256, 256, 8, 8, 0, 9, seed=13, scale_lo=-6, scale_hi=-2),
+]
+
+
+def _x(wl, T=None, stream=0):
+    return synth.activations(wl, tokens=T, stream=stream)
+
+
+# ------------------------------------------------------------- quantiser
+def test_quantize_act_bit_exact_exhaustive_bf16():
+    # every finite bf16 bit pattern, 32 per block, plus blocks with mixed
+    # magnitudes so each value is quantised under many block scales
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = synth.bf16_bits_to_f32(bits)
+    fin = bits[np.isfinite(vals)]
+    rng = np.random.default_rng(0)
+    a = fin[: fin.size // 256 * 256].reshape(-1, 256)
+    b = rng.permutation(fin)[: fin.size // 256 * 256].reshape(-1, 256)
+    x = np.concatenate([a, b, np.zeros((1, 256), np.uint16), np.full((1, 256), 0x8000, np.uint16)])
+    wl = TINY
+    L, _ = gu.make_layer(wl, max_tokens=x.shape[0])
+    q = torch.empty(x.shape, dtype=torch.uint8, device=gu.DEV)
+    s = torch.empty((x.shape[0], x.shape[1] // 32), dtype=torch.uint8, device=gu.DEV)
+    L.quantize_act(sg.bf16_tensor(x), x.shape[0], q, s)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quantize_act(x)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    qq = q.cpu().numpy()
+    bad = np.argwhere(qq != rq)
+    assert bad.size == 0, [(x[i, j], qq[i, j], rq[i, j]) for i, j in bad[:5]]
+    L.close()
+
+
+# ------------------------------------------------------------- routing
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_route_bit_exact_given_oracle_logits(wl):
+    L, W = gu.make_layer(wl)
+    x = _x(wl)
+    lg = oracle.router_logits(x, synth.router_weights(wl), synth.router_bias(wl))
+    ridx, rw = oracle.topk(lg, wl.top_k)
+    idx, w, lo = gu.run_route(L, x, wl.tokens, wl.n_experts, wl.top_k, logits_in=lg)
+    assert np.array_equal(idx, ridx)
+    assert np.array_equal(lo, lg)
+    assert np.allclose(w, rw, rtol=2e-6, atol=1e-7)
+    L.close()
+
+
+def test_route_ties_nan_and_signed_zero():
+    wl = Workload("ties_e384_k6", 256, 128, 384, 6, 1, 16, seed=14)
+    L, _ = gu.make_layer(wl)
+    rng = np.random.default_rng(5)
+    lg = rng.standard_normal((16, 384)).astype(np.float32)
+    lg[1, :] = 0.25
+    lg[2, ::2], lg[2, 1::2] = 0.0, -0.0
+    lg[3, :200] = np.nan
+    lg[4, :] = np.round(lg[4] * 2) / 2
+    lg[5, 383] = np.inf
+    lg[6, :] = -np.inf
+    lg[6, 300] = 1.0
+    ridx, _ = oracle.topk(lg, 6)
+    idx, _, _ = gu.run_route(L, _x(wl), 16, 384, 6, logits_in=lg)
+    assert np.array_equal(idx, ridx)
+    L.close()
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_router_logits_and_selection(wl):
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    lg = oracle.router_logits(x, synth.router_weights(wl), synth.router_bias(wl))
+    idx, w, lo = gu.run_route(L, x, wl.tokens, wl.n_experts, wl.top_k)
+    tol = 1e-5 * np.abs(lg).max(axis=1, keepdims=True)
+    assert (np.abs(lo - lg) <= tol).all()
+    # selections agree wherever the oracle's k-th / (k+1)-th margin exceeds
+    # twice the logit tolerance (the gate is a switch near ties)
+    srt = -np.sort(-lg, axis=1)
+    margin = srt[:, wl.top_k - 1] - (srt[:, wl.top_k] if wl.top_k < wl.n_experts else -np.inf)
+    ridx, _ = oracle.topk(lg, wl.top_k)
+    sure = margin > 2 * tol[:, 0]
+    assert np.array_equal(np.sort(idx[sure], 1), np.sort(ridx[sure], 1))
+    L.close()
+
+
+# ------------------------------------------------------------- segments
+@pytest.mark.parametrize("T,E,k", [(1, 384, 6), (37, 16, 2), (4096, 384, 6), (700, 512, 8)])
+def test_segments_bit_exact(T, E, k):
+    wl = Workload("seg", 128, 128, E, k, 1, T, seed=15)
+    L, _ = gu.make_layer(wl)
+    rng = np.random.default_rng(T + E)
+    idx = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    idx[0] = np.arange(k)  # a few heavy experts
+    off = torch.empty(E + 1, dtype=torch.int32, device=gu.DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=gu.DEV)
+    L.segments(torch.from_numpy(idx).to(gu.DEV), T, off, perm)
+    torch.cuda.synchronize()
+    roff, rperm = oracle.segments(idx, E)
+    assert np.array_equal(off.cpu().numpy(), roff)
+    assert np.array_equal(perm.cpu().numpy(), rperm)
+    L.close()
+
+
+# ------------------------------------------------------------- layer
+def _oracle_routing(wl, x, layer=0):
+    lg = oracle.router_logits(x, synth.router_weights(wl, layer), synth.router_bias(wl, layer))
+    return oracle.topk(lg, wl.top_k)
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_SIMT])
+def test_layer_matches_oracle(wl, path):
+    L, _ = gu.make_layer(wl)
+    L.set_option(m.MOE_OPT_PATH, path)
+    x = _x(wl)
+    idx, w = _oracle_routing(wl, x)
+    y = gu.run_forward(L, x, idx, w)
+    ref = gu.oracle_layer(wl, 0, x, idx, w)
+    gu.assert_y_close(y, ref)
+    L.close()
+
+
+def test_layer_with_residual_matches_oracle():
+    wl = SMALL[1]
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    r = _x(wl, stream=3)
+    idx, w = _oracle_routing(wl, x)
+    y = gu.run_forward(L, x, idx, w, residual_bits=r)
+    gu.assert_y_close(y, gu.oracle_layer(wl, 0, x, idx, w, residual=r))
+    L.close()
+
+
+def test_heavy_expert_duplicates_and_zero_weights():
+    # every token on the same experts (long token chunks), a repeated id in a
+    # row, and zero combine weights
+    wl = SMALL[1]
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    T = wl.tokens
+    idx = np.tile(np.array([[3, 3]], np.int32), (T, 1))
+    idx[::5, 1] = 7
+    w = np.tile(np.array([[0.6, 0.4]]), (T, 1))
+    w[::3] = 0.0
+    y = gu.run_forward(L, x, idx, w)
+    gu.assert_y_close(y, gu.oracle_layer(wl, 0, x, idx, w))
+    L.close()
+
+
+def test_deterministic_and_permutation_equivariant():
+    wl = SMALL[2]
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    idx, w = _oracle_routing(wl, x)
+    y1 = gu.run_forward(L, x, idx, w)
+    y2 = gu.run_forward(L, x, idx, w)
+    assert np.array_equal(y1, y2)
+    p = np.random.default_rng(2).permutation(wl.tokens)
+    yp = gu.run_forward(L, x[p], idx[p], w[p])
+    assert np.array_equal(yp, y1[p])
+    L.close()
+
+
+def test_token_count_edges():
+    wl = SMALL[1]
+    L, _ = gu.make_layer(wl, max_tokens=wl.tokens)
+    x = _x(wl)
+    idx, w = _oracle_routing(wl, x)
+    # T = 0 is a no-op, T = max_tokens works, T = max_tokens + 1 is rejected
+    L.forward(sg.bf16_tensor(x), 0, torch.zeros(1, dtype=torch.int32, device=gu.DEV),
+              torch.zeros(1, device=gu.DEV), torch.zeros(8, dtype=torch.int16, device=gu.DEV))
+    with pytest.raises(m.MoeError) as e:
+        L.forward(sg.bf16_tensor(x), wl.tokens + 1, torch.zeros(1, device=gu.DEV),
+                  torch.zeros(1, device=gu.DEV), torch.zeros(8, device=gu.DEV))
+    assert e.value.status == m.MOE_ERR_INVALID_ARG
+    for T in (1, wl.tokens):
+        y = gu.run_forward(L, x[:T], idx[:T], w[:T])
+        gu.assert_y_close(y, gu.oracle_layer(wl, 0, x[:T], idx[:T], w[:T]))
+    L.close()
+
+
+def test_expert_id_out_of_range_is_reported_and_recovers():
+    wl = TINY
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    idx, w = _oracle_routing(wl, x)
+    bad = idx.copy()
+    bad[1, 0] = wl.n_experts + 3
+    xt = sg.bf16_tensor(x)
+    y = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    L.forward(xt, wl.tokens, torch.from_numpy(bad).to(gu.DEV),
+              torch.from_numpy(w.astype(np.float32)).to(gu.DEV), y)
+    assert L.sync() == m.MOE_ERR_INTERNAL
+    assert L.sync() == m.MOE_OK  # the error word is cleared
+    gu.assert_y_close(gu.run_forward(L, x, idx, w), gu.oracle_layer(wl, 0, x, idx, w))
+    L.close()
+
+
+def test_fault_injection_launch_and_arg(monkeypatch):
+    wl = TINY
+    L, _ = gu.make_layer(wl)
+    x = sg.bf16_tensor(_x(wl))
+    z = torch.zeros((wl.tokens, wl.top_k), dtype=torch.int32, device=gu.DEV)
+    zf = torch.zeros((wl.tokens, wl.top_k), device=gu.DEV)
+    y = torch.empty_like(x)
+    for mode, status in (("launch", m.MOE_ERR_CUDA), ("arg", m.MOE_ERR_INVALID_ARG)):
+        monkeypatch.setenv("MOE_FAULT", mode)
+        with pytest.raises(m.MoeError) as e:
+            L.forward(x, wl.tokens, z, zf, y)
+        assert e.value.status == status
+    monkeypatch.delenv("MOE_FAULT")
+    L.forward(x, wl.tokens, z, zf, y)
+    assert L.sync() == m.MOE_OK
+    L.close()
+
+
+def test_forward_host_matches_device_path():
+    wl = SMALL[2]
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    L.forward_host(xh, wl.tokens, yh)
+    idx, w, _ = gu.run_route(L, x, wl.tokens, wl.n_experts, wl.top_k)
+    yd = gu.run_forward(L, x, idx, w)
+    assert np.array_equal(yh.numpy().view(np.uint16), yd)
+    L.close()
+
+
+def test_rmsnorm_matches_oracle():
+    rng = np.random.default_rng(8)
+    x = synth.f32_to_bf16_bits((rng.standard_normal((33, 5120)) * 200).astype(np.float32))
+    out = torch.empty((33, 5120), dtype=torch.int16, device=gu.DEV)
+    m.moe_rmsnorm(sg.bf16_tensor(x), 33, 5120, 1e-6, out)
+    torch.cuda.synchronize()
+    got = gu.bits_to_f64(out)
+    ref = gu.bits_to_f64(oracle.rmsnorm(x, 1e-6))
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7)  # within one bf16 ulp
+    assert (got != ref).mean() < 0.01
+
+
+def test_gpu_bank_fill_equals_host_generator():
+    wl = SMALL[2]
+    W = sg.device_layer(wl, 1, gu.DEV)
+    for e in (0, 17, wl.n_experts - 1):
+        ex = synth.host_expert(wl, 1, e)
+        for k in ("gate_codes", "gate_scales", "up_codes", "up_scales", "down_codes", "down_scales"):
+            assert np.array_equal(W[k][e].cpu().numpy(), ex[k]), (e, k)
+    sh = synth.host_expert(wl, 1, wl.n_experts + 1)
+    assert np.array_equal(W["s_down_codes"][1].cpu().numpy(), sh["down_codes"])
