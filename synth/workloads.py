@@ -46,4 +46,10 @@ PREFILL_T4096 = Workload("v41_layer_prefill_t4096", tokens=4096, seed=4, **_V41)
 STACK8_T64 = Workload("v41_stack8_decode_t64_zipf", tokens=64, seed=5, layers=8, zipf=1.1,
                       rmsnorm=True, **_V41)
 
-WORKLOADS = {w.name: w for w in (TINY, DECODE_T1, VERIFY_T5, VERIFY_T32, PREFILL_T4096, STACK8_T64)}
+# V4.1 expert shapes with a 24-expert bank (~450 MB, above the 126 MB L2): small
+# enough for an ncu capture with memory save/restore; not a benchmark line.
+NCU_DECODE_T1 = Workload("ncu_v41_e24_decode_t1", tokens=1, seed=6, **{**_V41, "n_experts": 24})
+NCU_PREFILL = Workload("ncu_v41_e24_prefill_t512", tokens=512, seed=7, **{**_V41, "n_experts": 24})
+
+WORKLOADS = {w.name: w for w in (TINY, DECODE_T1, VERIFY_T5, VERIFY_T32, PREFILL_T4096, STACK8_T64,
+                                 NCU_DECODE_T1, NCU_PREFILL)}
