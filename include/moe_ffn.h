@@ -154,6 +154,29 @@ moe_status moe_segments(moe_layer* layer, const int32_t* topk_idx, int32_t T, in
  * out may alias x.  H a multiple of 8, at most 65536. */
 moe_status moe_rmsnorm(const void* x, int32_t T, int32_t H, float eps, void* out, void* stream);
 
+/* Router without any device allocation, for callers that cannot call
+ * cudaMalloc: a runtime whose device memory pool is entirely reserved by its
+ * own allocator, or a step that must not make a call which can synchronise
+ * the device or fail for lack of memory.  The pages describe no such entry
+ * point; it has no counterpart there.
+ *
+ * Same result as moe_route(layer, x, T, NULL, NULL, topk_idx, topk_w, stream)
+ * on a layer with these shapes, but without a layer handle: the logits
+ * scratch is a fixed array of MOE_ROUTE_STATIC_MAX_LOGITS floats (128 KB)
+ * built into the library, which every GPU that loads the library holds until
+ * the process exits.  T * E above that limit returns MOE_ERR_UNSUPPORTED;
+ * H must be a multiple of 128 (at most 16384), E <= 512, 1 <= k <= min(8, E);
+ * x and router_w 16-byte aligned.
+ * The first call on a device looks up the array's device address (set-up,
+ * done once per device with that device current); make that first call
+ * before any stream capture.  All calls share the one array: calls whose
+ * work overlaps on the GPU (two streams, or two host threads) race on it and
+ * must be serialised by the caller.  No call allocates or frees memory. */
+#define MOE_ROUTE_STATIC_MAX_LOGITS (64 * 512)
+moe_status moe_route_static(const void* x, int32_t T, int32_t H, int32_t E, int32_t k,
+                            const float* router_w, const float* router_b, int32_t* topk_idx,
+                            float* topk_w, void* stream);
+
 /* Waits for the stream and reports any device error the layer's kernels
  * recorded (MOE_ERR_INTERNAL / MOE_ERR_TIMEOUT) or CUDA reported; clears the
  * layer's recorded error. */

@@ -21,7 +21,9 @@ PATH_AUTO, PATH_SIMT, PATH_MMA = 0, 1, 2
 # every symbol include/moe_ffn.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
            "moe_forward_host", "moe_quantize_act", "moe_segments", "moe_rmsnorm", "moe_sync",
-           "moe_set_option", "moe_get_kernel_times", "moe_status_string", "moe_abi_version")
+           "moe_set_option", "moe_get_kernel_times", "moe_status_string", "moe_abi_version",
+           "moe_route_static")
+ROUTE_STATIC_MAX_LOGITS = 64 * 512
 
 
 class MoeError(RuntimeError):
@@ -71,6 +73,7 @@ def lib():
         L.moe_set_option.argtypes = [P, I32, C.c_int64]
         L.moe_get_kernel_times.argtypes = [P, C.POINTER(C.c_char_p), C.POINTER(C.c_double),
                                            C.POINTER(C.c_int64), I32, C.POINTER(I32)]
+        L.moe_route_static.argtypes = [P, I32, I32, I32, I32, P, P, P, P, P]
         L.moe_status_string.argtypes = [C.c_int]
         L.moe_status_string.restype = C.c_char_p
         L.moe_abi_version.restype = I32
@@ -155,6 +158,12 @@ def moe_segments(h, topk_idx, T, offsets, perm, stream=None) -> None:
 
 def moe_rmsnorm(x, T, H, eps, out, stream=None) -> None:
     _check(lib().moe_rmsnorm(ptr(x), T, H, eps, ptr(out), stream_handle(stream)), "moe_rmsnorm")
+
+
+def moe_route_static(x, T, H, E, k, router_w, router_b, topk_idx, topk_w, stream=None) -> None:
+    """Router that allocates nothing (logits scratch built into the library)."""
+    _check(lib().moe_route_static(ptr(x), T, H, E, k, ptr(router_w), ptr(router_b), ptr(topk_idx),
+                                  ptr(topk_w), stream_handle(stream)), "moe_route_static")
 
 
 def moe_sync(h, stream=None) -> int:
