@@ -60,6 +60,9 @@ size_t carve(const moe_config& c, char* base, Workspace& ws) {
   ws.pos_tok = cv.take<int32_t>(P);
   ws.active = cv.take<int32_t>(NE);
   ws.n_active = cv.take<int32_t>(1);
+  ws.tile_prefix = cv.take<int32_t>(NE + 1);
+  ws.xg = cv.take<uint8_t>(P * H);
+  ws.xgs = cv.take<uint8_t>(P * H / 32);
   ws.hq = cv.take<uint8_t>(P * I);
   ws.hs = cv.take<uint8_t>(P * I / 32);
   ws.o = cv.take<float>(P * H);
@@ -218,10 +221,14 @@ moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int dev
   carve(*cfg, static_cast<char*>(base), L->ws);
   L->ws.base = base;
   L->ws.bytes = bytes;
-  cudaError_t e = cudaMemset(L->ws.err, 0, sizeof(int32_t));
+  cudaError_t e = cudaMemset(base, 0, bytes);
   if (e == cudaSuccess) e = cudaMallocHost(&L->ws.err_host, sizeof(int32_t));
   if (e == cudaSuccess) e = prepare_segments_kernel(cfg->n_experts);
   if (e == cudaSuccess) e = prepare_ffn_simt(cfg->hidden, cfg->inter);
+  if (e == cudaSuccess) {
+    L->maps = mma_maps_create(*cfg, *w, L->ws);  // NULL: tensor-core path unavailable
+    cudaGetLastError();
+  }
   if (e != cudaSuccess) {
     if (L->ws.err_host) cudaFreeHost(L->ws.err_host);
     cudaFree(base);
@@ -240,6 +247,7 @@ moe_status moe_layer_destroy(moe_layer* L) {
     if (L->ev_pool[i]) cudaEventDestroy(L->ev_pool[i]);
   if (L->ws.err_host) cudaFreeHost(L->ws.err_host);
   cudaFree(L->ws.base);
+  mma_maps_destroy(L->maps);
   delete L;
   return cuda_fail(e);
 }
@@ -248,7 +256,7 @@ moe_status moe_set_option(moe_layer* L, int32_t option, int64_t value) {
   if (!L) return MOE_ERR_INVALID_ARG;
   if (option == MOE_OPT_PATH) {
     if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
-    if (value == 2) return MOE_ERR_UNSUPPORTED;
+    if (value == 2 && !L->maps) return MOE_ERR_UNSUPPORTED;
     L->path = (int)value;
     return MOE_OK;
   }
@@ -334,31 +342,63 @@ moe_status route_impl(moe_layer* L, const void* x, int32_t T, const float* logit
   return cuda_fail(e);
 }
 
+// Path choice: the SIMT streaming kernels for a single token (every expert
+// sees at most one row), the tensor-core kernels otherwise; MOE_OPT_PATH
+// forces either.
+bool use_mma(const moe_layer* L, int T) {
+  if (!L->maps) return false;
+  if (L->path == 1) return false;
+  if (L->path == 2) return true;
+  return T > 1;
+}
+
 moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* idx,
                         const float* w, const void* residual, void* y, cudaStream_t st) {
   const moe_config& c = L->cfg;
   const ExpertBank bank = bank_of(L);
+  const bool mma = use_mma(L, T);
+  const int bn = mma ? mma_tile_for_tokens(T) : 0;
   cudaError_t e;
   {
     TimedScope ts(L, st, "segments");
-    e = launch_segments(idx, T, c.top_k, c.n_experts, c.n_shared, L->ws, st);
+    e = launch_segments(idx, T, c.top_k, c.n_experts, c.n_shared, bn, L->ws, st);
   }
   if (e != cudaSuccess) return cuda_fail(e);
-  {
-    TimedScope ts(L, st, "quantize_act");
-    e = launch_quantize_act(static_cast<const uint16_t*>(x), T, c.hidden, L->ws.xq, L->ws.xs, st);
+  if (mma) {
+    const int P = T * (c.top_k + c.n_shared);
+    {
+      TimedScope ts(L, st, "quantize_gather");
+      e = launch_quantize_gather(static_cast<const uint16_t*>(x), P, c.hidden, L->ws.pos_tok,
+                                 L->ws.xg, L->ws.xgs, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    {
+      TimedScope ts(L, st, "ffn_up_mma");
+      e = launch_ffn_mma(*L->maps, bank, 0, bn, L->ws, L->num_sms, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    {
+      TimedScope ts(L, st, "ffn_down_mma");
+      e = launch_ffn_mma(*L->maps, bank, 1, bn, L->ws, L->num_sms, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+  } else {
+    {
+      TimedScope ts(L, st, "quantize_act");
+      e = launch_quantize_act(static_cast<const uint16_t*>(x), T, c.hidden, L->ws.xq, L->ws.xs, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    {
+      TimedScope ts(L, st, "ffn_up_simt");
+      e = launch_ffn_up_simt(bank, T, c.top_k, c.n_shared, L->ws, L->num_sms, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    {
+      TimedScope ts(L, st, "ffn_down_simt");
+      e = launch_ffn_down_simt(bank, T, c.top_k, c.n_shared, L->ws, L->num_sms, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
   }
-  if (e != cudaSuccess) return cuda_fail(e);
-  {
-    TimedScope ts(L, st, "ffn_up_simt");
-    e = launch_ffn_up_simt(bank, T, c.top_k, c.n_shared, L->ws, L->num_sms, st);
-  }
-  if (e != cudaSuccess) return cuda_fail(e);
-  {
-    TimedScope ts(L, st, "ffn_down_simt");
-    e = launch_ffn_down_simt(bank, T, c.top_k, c.n_shared, L->ws, L->num_sms, st);
-  }
-  if (e != cudaSuccess) return cuda_fail(e);
   {
     TimedScope ts(L, st, "combine");
     e = launch_combine(L->ws, T, c.hidden, c.top_k, c.n_shared, w,
@@ -437,7 +477,7 @@ moe_status moe_segments(moe_layer* L, const int32_t* topk_idx, int32_t T, int32_
   if (g.status != cudaSuccess) return cuda_fail(g.status);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const moe_config& c = L->cfg;
-  cudaError_t e = launch_segments(topk_idx, T, c.top_k, c.n_experts, c.n_shared, L->ws, st);
+  cudaError_t e = launch_segments(topk_idx, T, c.top_k, c.n_experts, c.n_shared, 0, L->ws, st);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(offsets, L->ws.off, sizeof(int32_t) * (c.n_experts + 1),
                         cudaMemcpyDeviceToDevice, st);

@@ -24,6 +24,9 @@ struct Workspace {
   int32_t* pos_tok = nullptr; // [P]        token of each position
   int32_t* active = nullptr;  // [NE]       experts with tokens, routed then shared
   int32_t* n_active = nullptr;// [1]
+  int32_t* tile_prefix = nullptr; // [NE+1] token tiles before each active expert
+  uint8_t* xg = nullptr;      // [P][H]     E4M3 codes of x, gathered by position
+  uint8_t* xgs = nullptr;     // [P][H/32]
   uint8_t* hq = nullptr;      // [P][I]     E4M3 codes of h
   uint8_t* hs = nullptr;      // [P][I/32]  UE8M0 scale bytes of h
   float* o = nullptr;         // [P][H]     expert outputs per position
@@ -37,6 +40,8 @@ struct Workspace {
   void* base = nullptr;       // single allocation holding all of the above
   size_t bytes = 0;
 };
+
+struct MmaMaps;
 
 struct Timer {
   const char* name = nullptr;
@@ -54,6 +59,7 @@ struct moe_layer {
   int path = 0;
   bool timing = false;
   moe::Workspace ws;
+  moe::MmaMaps* maps = nullptr;  // TMA descriptors of the tensor-core path
   moe::Timer timers[moe::kMaxTimed];
   int n_timers = 0;
   cudaEvent_t ev_pool[2 * 64] = {};
@@ -73,8 +79,10 @@ struct ExpertBank {
 // --- launchers (return the launch's cudaError_t) ---------------------------
 cudaError_t launch_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s,
                                 cudaStream_t st);
-cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared,
+cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared, int bn,
                             const Workspace& ws, cudaStream_t st);
+cudaError_t launch_quantize_gather(const uint16_t* x, int P, int H, const int32_t* pos_tok,
+                                   uint8_t* xg, uint8_t* xgs, cudaStream_t st);
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const float* W,
                                  const float* b, float* logits, int num_sms, cudaStream_t st);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
@@ -86,6 +94,11 @@ cudaError_t launch_ffn_down_simt(const ExpertBank& bank, int T, int k, int n_sha
 cudaError_t launch_combine(const Workspace& ws, int T, int H, int k, int n_shared,
                            const float* w, const uint16_t* residual, uint16_t* y,
                            cudaStream_t st);
+MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Workspace& ws);
+void mma_maps_destroy(MmaMaps* m);
+int mma_tile_for_tokens(int T);
+cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn,
+                           const Workspace& ws, int num_sms, cudaStream_t st);
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out,
                            cudaStream_t st);
 

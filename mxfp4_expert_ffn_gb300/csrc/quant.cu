@@ -12,32 +12,58 @@
 namespace moe {
 namespace {
 
+// Quantises 8 consecutive bf16 values; the four lanes of a quad (one 32-block)
+// agree on the block exponent.  Returns the 8 codes; *e gets the exponent.
+__device__ __forceinline__ uint2 quant8(const uint4 v, unsigned quad, int* e_out) {
+  float f[8];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 2));
+  const int e = fp8_block_exponent(amax);
+  uint32_t c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    c[j] = e4m3x2(scale_pow2_neg(f[2 * j], e), scale_pow2_neg(f[2 * j + 1], e));
+  *e_out = e;
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
 // One thread per 8 bf16 values; four consecutive threads form one 32-block.
 __global__ void quantize_act_kernel(const uint4* __restrict__ x, int n8, uint2* __restrict__ q,
                                     uint8_t* __restrict__ s) {
   const int lane = threadIdx.x & 31;
   const unsigned quad = 0xFu << (lane & ~3);
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += gridDim.x * blockDim.x) {
-    const uint4 v = x[i];
-    float f[8];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[2 * j] = __uint_as_float(w[j] << 16);
-      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 2));
-    const int e = fp8_block_exponent(amax);
-    uint32_t c[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      c[j] = e4m3x2(scale_pow2_neg(f[2 * j], e), scale_pow2_neg(f[2 * j + 1], e));
-    q[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    int e;
+    q[i] = quant8(x[i], quad, &e);
     if ((lane & 3) == 0) s[i >> 2] = (uint8_t)(e + 127);
+  }
+}
+
+// Same quantisation, written once per position (row p of xg is token
+// pos_tok[p]), so that each expert's activation rows are contiguous.
+__global__ void quantize_gather_kernel(const uint16_t* __restrict__ x, int P, int H,
+                                       const int32_t* __restrict__ pos_tok, uint2* __restrict__ xg,
+                                       uint8_t* __restrict__ xgs) {
+  const int lane = threadIdx.x & 31;
+  const unsigned quad = 0xFu << (lane & ~3);
+  const int per_row = H / 8;
+  const long long n8 = (long long)P * per_row;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int p = (int)(i / per_row), j = (int)(i - (long long)p * per_row);
+    const uint4 v = reinterpret_cast<const uint4*>(x + (size_t)pos_tok[p] * H)[j];
+    int e;
+    xg[i] = quant8(v, quad, &e);
+    if ((lane & 3) == 0) xgs[i >> 2] = (uint8_t)(e + 127);
   }
 }
 
@@ -47,11 +73,12 @@ __global__ void quantize_act_kernel(const uint4* __restrict__ x, int n8, uint2* 
 // slot at base + rank among the warp's equal-expert lanes.  The result is a
 // stable counting sort, identical on every run.
 __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restrict__ idx, int T,
-                                                        int k, int E, int ns, Workspace ws) {
+                                                        int k, int E, int ns, int bn, Workspace ws) {
   extern __shared__ int32_t sm[];
   const int NE = E + ns;
   int32_t* wcnt = sm;            // [32][E]  per-warp counts, then running bases
   int32_t* stot = sm + 32 * E;   // [E]      totals, then exclusive offsets
+  __shared__ int routed_total;
   const int S = T * k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
@@ -87,39 +114,57 @@ __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restric
     // exclusive scan of the E totals and of the "has tokens" flags
     const int chunk = (E + 31) / 32;
     const int c0 = min(E, lane * chunk), c1 = min(E, c0 + chunk);
-    int sum = 0, nf = 0;
+    // (and of the token tiles of width bn, for the tensor-core path)
+    const int tb = bn > 0 ? bn : 1;
+    int sum = 0, nf = 0, nt = 0;
     for (int e = c0; e < c1; ++e) {
       sum += stot[e];
       nf += stot[e] > 0;
+      nt += (stot[e] + tb - 1) / tb;
     }
-    int isum = sum, inf = nf;
+    int isum = sum, inf = nf, intl = nt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int a = __shfl_up_sync(0xFFFFFFFFu, isum, o);
       const int f = __shfl_up_sync(0xFFFFFFFFu, inf, o);
+      const int t = __shfl_up_sync(0xFFFFFFFFu, intl, o);
       if (lane >= o) {
         isum += a;
         inf += f;
+        intl += t;
       }
     }
-    int run = isum - sum, fr = inf - nf;
+    int run = isum - sum, fr = inf - nf, tr = intl - nt;
     for (int e = c0; e < c1; ++e) {
       const int c = stot[e];
       ws.cnt[e] = c;
       ws.off[e] = run;
       stot[e] = run;
-      if (c > 0) ws.active[fr++] = e;
+      if (c > 0) {
+        ws.tile_prefix[fr] = tr;
+        ws.active[fr++] = e;
+        tr += (c + tb - 1) / tb;
+      }
       run += c;
     }
     const int n_routed_active = __shfl_sync(0xFFFFFFFFu, inf, 31);
+    const int routed_tiles = __shfl_sync(0xFFFFFFFFu, intl, 31);
+    const int valid = __shfl_sync(0xFFFFFFFFu, isum, 31);
     if (lane == 0) {
+      routed_total = valid;
+      int tiles = routed_tiles;
       for (int sh = 0; sh < ns; ++sh) {
         ws.cnt[E + sh] = T;
         ws.off[E + sh] = S + sh * T;
-        if (T > 0) ws.active[n_routed_active + sh] = E + sh;
+        if (T > 0) {
+          ws.active[n_routed_active + sh] = E + sh;
+          ws.tile_prefix[n_routed_active + sh] = tiles;
+          tiles += (T + tb - 1) / tb;
+        }
       }
       ws.off[NE] = S + ns * T;
       *ws.n_active = n_routed_active + (T > 0 ? ns : 0);
+      ws.tile_prefix[n_routed_active + (T > 0 ? ns : 0)] = tiles;
     }
   }
   __syncthreads();
@@ -144,6 +189,9 @@ __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restric
     __syncwarp();
   }
   for (int i = threadIdx.x; i < ns * T; i += blockDim.x) ws.pos_tok[S + i] = i % T;
+  // positions left free by invalid expert ids still name a real token, so
+  // that every position's row can be read safely
+  for (int p = routed_total + threadIdx.x; p < S; p += blockDim.x) ws.pos_tok[p] = 0;
 }
 
 // y[t] = bf16( sum_s o[S + s*T + t] + sum_j w[t][j] * o[slot_pos[t*k + j]] ),
@@ -248,9 +296,19 @@ cudaError_t launch_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uin
 
 size_t segments_smem_bytes(int E) { return (size_t)(33 * E) * sizeof(int32_t); }
 
-cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared,
+cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared, int bn,
                             const Workspace& ws, cudaStream_t st) {
-  segments_kernel<<<1, 1024, segments_smem_bytes(E), st>>>(idx, T, k, E, n_shared, ws);
+  segments_kernel<<<1, 1024, segments_smem_bytes(E), st>>>(idx, T, k, E, n_shared, bn, ws);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_gather(const uint16_t* x, int P, int H, const int32_t* pos_tok,
+                                   uint8_t* xg, uint8_t* xgs, cudaStream_t st) {
+  const long long n8 = (long long)P * (H / 8);
+  if (n8 == 0) return cudaSuccess;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 8192) blocks = 8192;
+  quantize_gather_kernel<<<(int)blocks, 256, 0, st>>>(x, P, H, pos_tok, reinterpret_cast<uint2*>(xg), xgs);
   return cudaGetLastError();
 }
 

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import mxfp4_expert_ffn_gb300 as m
 import oracle
 import synth
 from synth import gpu as sg
@@ -43,9 +44,11 @@ def _check_layer(wl, layer, L, x, sample):
     return gu.assert_y_close(y[sample], ref)
 
 
+@pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_SIMT, m.PATH_MMA])
 @pytest.mark.parametrize("wl", [DECODE_T1, VERIFY_T5, VERIFY_T32], ids=lambda w: w.name)
-def test_decode_and_verification_layers(wl):
+def test_decode_and_verification_layers(wl, path):
     L, W = gu.make_layer(wl)
+    L.set_option(m.MOE_OPT_PATH, path)
     x = synth.activations(wl)
     sample = np.arange(wl.tokens) if wl.tokens <= 8 else np.random.default_rng(0).choice(
         wl.tokens, 8, replace=False)

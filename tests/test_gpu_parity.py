@@ -128,7 +128,7 @@ def _oracle_routing(wl, x, layer=0):
 
 
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
-@pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_SIMT])
+@pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_SIMT, m.PATH_MMA])
 def test_layer_matches_oracle(wl, path):
     L, _ = gu.make_layer(wl)
     L.set_option(m.MOE_OPT_PATH, path)
@@ -151,11 +151,13 @@ def test_layer_with_residual_matches_oracle():
     L.close()
 
 
-def test_heavy_expert_duplicates_and_zero_weights():
+@pytest.mark.parametrize("path", [m.PATH_SIMT, m.PATH_MMA])
+def test_heavy_expert_duplicates_and_zero_weights(path):
     # every token on the same experts (long token chunks), a repeated id in a
     # row, and zero combine weights
     wl = SMALL[1]
     L, _ = gu.make_layer(wl)
+    L.set_option(m.MOE_OPT_PATH, path)
     x = _x(wl)
     T = wl.tokens
     idx = np.tile(np.array([[3, 3]], np.int32), (T, 1))
@@ -167,9 +169,11 @@ def test_heavy_expert_duplicates_and_zero_weights():
     L.close()
 
 
-def test_deterministic_and_permutation_equivariant():
+@pytest.mark.parametrize("path", [m.PATH_SIMT, m.PATH_MMA])
+def test_deterministic_and_permutation_equivariant(path):
     wl = SMALL[2]
     L, _ = gu.make_layer(wl)
+    L.set_option(m.MOE_OPT_PATH, path)
     x = _x(wl)
     idx, w = _oracle_routing(wl, x)
     y1 = gu.run_forward(L, x, idx, w)
@@ -199,9 +203,11 @@ def test_token_count_edges():
     L.close()
 
 
-def test_expert_id_out_of_range_is_reported_and_recovers():
-    wl = TINY
+@pytest.mark.parametrize("path", [m.PATH_SIMT, m.PATH_MMA])
+def test_expert_id_out_of_range_is_reported_and_recovers(path):
+    wl = SMALL[1]
     L, _ = gu.make_layer(wl)
+    L.set_option(m.MOE_OPT_PATH, path)
     x = _x(wl)
     idx, w = _oracle_routing(wl, x)
     bad = idx.copy()
