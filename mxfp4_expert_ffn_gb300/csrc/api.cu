@@ -61,12 +61,15 @@ size_t carve(const moe_config& c, char* base, Workspace& ws) {
   ws.active = cv.take<int32_t>(NE);
   ws.n_active = cv.take<int32_t>(1);
   ws.tile_prefix = cv.take<int32_t>(NE + 1);
+  // sum over experts of ceil(tokens / 16) <= slots / 16 + experts
+  ws.tile_info = cv.take<int4>(P / 16 + NE + 16);
   ws.xg = cv.take<uint8_t>(P * H);
   ws.xgs = cv.take<uint8_t>(P * H / 32);
   ws.hq = cv.take<uint8_t>(P * I);
   ws.hs = cv.take<uint8_t>(P * I / 32);
   ws.o = cv.take<float>(P * H);
   ws.logits = cv.take<float>(T * E);
+  ws.rpart = cv.take<float>(8 * (T < kRouterSplitMaxT ? T : kRouterSplitMaxT) * E);
   ws.idx = cv.take<int32_t>(T * k);
   ws.w = cv.take<float>(T * k);
   ws.x = cv.take<uint16_t>(T * H);
@@ -324,6 +327,13 @@ moe_status route_impl(moe_layer* L, const void* x, int32_t T, const float* logit
   const moe_config& c = L->cfg;
   cudaError_t e = cudaSuccess;
   const float* lg = logits_in;
+  if (!lg && T <= kRouterSplitMaxT) {
+    // small T: split-K logits (W_r streamed by ~E/8 x 8 CTAs), summed in the top-k pass
+    TimedScope ts(L, st, "router_split");
+    return cuda_fail(launch_router_split(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts,
+                                         c.top_k, L->w.router_w, L->w.router_b, L->ws.rpart,
+                                         logits_out, idx, w, st));
+  }
   if (!lg) {
     float* dst = logits_out ? logits_out : L->ws.logits;
     TimedScope ts(L, st, "router_logits");

@@ -8,19 +8,23 @@
 // the quantization already supported"; janit's comment item 2).
 //
 // One persistent CTA per SM, ten warps:
-//   warp 0      TMA producer: weight tiles through the 4-bit-unpacking tensor
-//               map type (packed in HBM, one byte per element in shared memory,
-//               as the f8f6f4 MMA reads them), activation tiles by position;
+//   warp 0      TMA producer.  Weights go through a 3-D view (128-element
+//               chunk, row, chunk index) of the canonical [row][K] bank with
+//               the 4-bit-unpacking tensor-map type, so that one TMA op moves
+//               128 rows x CH chunks (16 KB of HBM for CH = 2) and lands as CH
+//               standard 128-row swizzled tiles, one byte per element, as the
+//               f8f6f4 MMA reads them.  Large ops matter: a TMA unit completes
+//               a roughly fixed number of ops per second.
 //   warp 1      MMA issuer and TMEM owner;
 //   warps 2..5  epilogue (one TMEM lane quadrant each);
 //   warps 6..9  scale-factor writers: per stage they copy the UE8M0 bytes of
-//               the weight rows and tokens into TMEM (tcgen05.st), row r at
-//               lane r / column r/32, k-block j in byte j.
-// Work unit = (active expert, tile of weight rows, tile of BN tokens); for
-// gate/up a tile holds 64 gate rows and the same 64 up rows (M = 128), so the
-// epilogue has g and u of 64 intermediate rows and writes h = silu(g) * u as
-// FP8 per 32 rows; for down a tile is 128 rows of the hidden dimension and
-// the epilogue writes fp32 expert outputs per position.
+//               the weight rows and tokens into TMEM (tcgen05.st): row r at
+//               lane r, column r/32 of its group, k-block j in byte j.
+// Work unit = (active expert, 128 weight rows, token tile of BN).  gate/up
+// units hold 128 gate rows and the same 128 up rows in two accumulators, so
+// every epilogue warp has g and u of its 32 intermediate rows: it writes
+// h = silu(g) * u as FP8 with one scale per 32 rows.  down units write fp32
+// expert outputs per position.
 #include <math.h>
 
 #include "common.cuh"
@@ -34,17 +38,15 @@ enum { kModeUp = 0, kModeDown = 1 };
 struct MmaParams {
   CUtensorMap a_routed[2];   // up mode: gate, up banks; down mode: down bank in [0]
   CUtensorMap a_shared[2];
-  CUtensorMap b;             // activations by position, [P][K] E4M3
+  CUtensorMap b;             // activations by position, 3-D view of [P][K] E4M3
   const uint8_t* sa_routed[2];
   const uint8_t* sa_shared[2];
   const uint8_t* sb;         // activation scales by position, [P][K/32]
   int E, K, rows;            // rows per expert of the weight matrices (I up, H down)
   int out_cols;              // I (h row length) in up mode, H in down mode
-  const int32_t* active;
   const int32_t* n_active;
-  const int32_t* off;
-  const int32_t* cnt;
   const int32_t* tile_prefix;
+  const int4* tile_info;
   uint8_t* hq;
   uint8_t* hs;
   float* o;
@@ -57,68 +59,67 @@ using namespace sm100;
 
 constexpr int kThreadsMma = 320;
 constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kSmemBudget = 227 * 1024 - 2048;
 
-template <int BN>
+constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
+
+template <int MODE, int BN, int CH>
 struct Cfg {
-  static constexpr int kStages = BN >= 128 ? 5 : (BN >= 64 ? 7 : 10);
-  static constexpr int kATile = 16384;         // 128 rows x 128 bytes
-  static constexpr int kBTile = BN * 128;
-  static constexpr int kStageBytes = kATile + kBTile;
-  static constexpr int kUbufStride = BN + 1;  // floats per u row (padded)
-  static constexpr int kUbufBytes = 2 * 32 * kUbufStride * 4;
-  static constexpr int kSfCols = 8;           // per stage: 4 A columns, 4 B columns
-  static constexpr int kTmemCols = 2 * BN + kStages * kSfCols;
-  static constexpr int kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kUbufBytes;
+  static constexpr int kNA = MODE == kModeUp ? 2 : 1;     // weight matrices per unit
+  static constexpr int kATile = 128 * 128 * CH;           // one matrix, one stage
+  static constexpr int kBTile = BN * 128 * CH;
+  static constexpr int kStageBytes = kNA * kATile + kBTile;
+  static constexpr int kStages = (kSmemBudget - 1024) / kStageBytes > 6 ? 6 : (kSmemBudget - 1024) / kStageBytes;
+  static constexpr int kAccCols = kNA * BN;               // g then u (up) or o (down)
+  static constexpr int kNAcc = (MODE == kModeUp && BN >= 128) ? 1 : 2;
+  static constexpr int kSfCols = (kNA + 1) * 4 * CH;      // 4 columns per (matrix, chunk)
+  static constexpr int kTmemCols = kNAcc * kAccCols + kStages * kSfCols;
+  static constexpr int kTmemAlloc = pow2_cols(kTmemCols);
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes;
+  static constexpr uint32_t kTxBytes = kNA * 128 * 64 * CH + BN * 128 * CH;
+  static_assert(kStages >= 2, "pipeline depth");
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct Unit {
-  int e, p0, n0, m_tile, row0;
+  int e, pos0, m_tile, row0;
 };
 
-// Unit u -> (active expert, token tile, row tile); row tiles innermost so
-// that consecutive units share the activation tile.
-template <int BN>
-__device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_per_expert,
-                                            int row_tile, int n_act) {
+// Unit u -> (token tile v, 128-row tile); row tiles innermost so consecutive
+// units share the activation tile.
+__device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_per_expert) {
   const int v = u / mt_per_expert;
-  const int mt = u - v * mt_per_expert;
-  int lo = 0, hi = n_act;  // largest a with tile_prefix[a] <= v
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (p.tile_prefix[mid] <= v) lo = mid;
-    else hi = mid;
-  }
-  Unit r;
-  r.e = p.active[lo];
-  const int j = v - p.tile_prefix[lo];
-  r.n0 = j * BN;
-  r.p0 = p.off[r.e];
-  r.m_tile = min(BN, p.cnt[r.e] - r.n0);
-  r.row0 = mt * row_tile;
-  return r;
+  const int4 t = __ldg(p.tile_info + v);
+  return Unit{t.x, t.y, t.z, (u - v * mt_per_expert) * 128};
 }
 
-template <int MODE, int BN>
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            int32_t c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <int MODE, int BN, int CH>
 __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_constant__ MmaParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<MODE, BN, CH>;
+  constexpr int NA = C::kNA;
+  constexpr int NC = (BN + 31) / 32;  // 32-token groups of the B scale factors
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* stage_base = smem;
-  float* ubuf = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  uint8_t* stage_base = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full_bar[C::kStages], sf_bar[C::kStages], empty_bar[C::kStages];
   __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row_tile = MODE == kModeUp ? 64 : 128;
-  const int mt_per_expert = p.rows / row_tile;
-  const int n_act = *p.n_active;
-  const int total = p.tile_prefix[n_act] * mt_per_expert;
-  const int k_stages = p.K / 128;
+  const int mt_per_expert = p.rows / 128;
+  const int total = p.tile_prefix[*p.n_active] * mt_per_expert;
+  const int k_stages = p.K / (128 * CH);
+  const uint32_t sf_col0 = C::kNAcc * C::kAccCols;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -138,7 +139,6 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t sf_col0 = 2 * BN;
 
   auto give_up = [&]() {
     atomicOr(p.err, kErrTimeout);
@@ -151,31 +151,30 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     if (lane == 0) {
       uint32_t g = 0;
       int last_parity[C::kStages];
+#pragma unroll
       for (int s = 0; s < C::kStages; ++s) last_parity[s] = -1;
       for (int u = blockIdx.x; u < total && !aborted(); u += gridDim.x) {
-        const Unit un = decode_unit<BN>(p, u, mt_per_expert, row_tile, n_act);
+        const Unit un = decode_unit(p, u, mt_per_expert);
         const bool sh = un.e >= p.E;
         const int erow = (sh ? un.e - p.E : un.e) * p.rows + un.row0;
-        const CUtensorMap* a0 = sh ? &p.a_shared[0] : &p.a_routed[0];
-        const CUtensorMap* a1 = sh ? &p.a_shared[1] : &p.a_routed[1];
         for (int s = 0; s < k_stages; ++s, ++g) {
           const int slot = g % C::kStages;
           const uint32_t ph = (g / C::kStages) & 1;
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); break; }
           uint8_t* sa = stage_base + slot * C::kStageBytes;
-          uint8_t* sb = sa + C::kATile;
-          mbar_expect_tx(&full_bar[slot], 8192 + BN * 128);
-          if (MODE == kModeUp) {
-            tma_load_2d(sa, a0, s * 128, erow, &full_bar[slot]);
-            tma_load_2d(sa + 8192, a1, s * 128, erow, &full_bar[slot]);
-          } else {
-            tma_load_2d(sa, a0, s * 128, erow, &full_bar[slot]);
-          }
-          tma_load_2d(sb, &p.b, s * 128, un.p0 + un.n0, &full_bar[slot]);
-          last_parity[slot] = (int)ph;
+          mbar_expect_tx(&full_bar[slot], C::kTxBytes);
+#pragma unroll
+          for (int m = 0; m < NA; ++m)
+            tma_load_3d(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
+                        &full_bar[slot]);
+          tma_load_3d(sa + NA * C::kATile, &p.b, 0, un.pos0, s * CH, &full_bar[slot]);
+#pragma unroll
+          for (int i = 0; i < C::kStages; ++i)
+            if (i == slot) last_parity[i] = (int)ph;
         }
       }
       // never leave with copies in flight: wait for the last load into each slot
+#pragma unroll
       for (int s = 0; s < C::kStages; ++s)
         if (last_parity[s] >= 0) mbar_wait(&full_bar[s], (uint32_t)last_parity[s], kWaitLimit);
     }
@@ -183,11 +182,13 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       uint32_t g = 0, it = 0;
+      const uint32_t idesc_base = idesc_e2m1_e4m3(128, BN, 0);
       for (int u = blockIdx.x; u < total && !aborted(); u += gridDim.x, ++it) {
-        const int buf = it & 1;
-        if (!mbar_wait(&acce_bar[buf], ((it >> 1) & 1) ^ 1, kWaitLimit)) { give_up(); break; }
+        const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
+        const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
+        if (!mbar_wait(&acce_bar[buf], ph_acc ^ 1, kWaitLimit)) { give_up(); break; }
         fence_after();
-        const uint32_t d_tmem = tmem + buf * BN;
+        const uint32_t d_tmem = tmem + buf * C::kAccCols;
         bool ok = true;
         for (int s = 0; s < k_stages; ++s, ++g) {
           const int slot = g % C::kStages;
@@ -199,12 +200,19 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           }
           fence_after();
           const uint32_t sa = smem_u32(stage_base + slot * C::kStageBytes);
-          const uint32_t sb = sa + C::kATile;
-          const uint32_t sfa = tmem + sf_col0 + slot * C::kSfCols;
+          const uint32_t sb = sa + NA * C::kATile;
+          const uint32_t sf = tmem + sf_col0 + slot * C::kSfCols;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_mxf8f6f4(d_tmem, sw128_desc(sa + 32 * k), sw128_desc(sb + 32 * k),
-                         idesc_e2m1_e4m3(128, BN, (uint32_t)k), sfa, sfa + 4, (s | k) ? 1u : 0u);
+          for (int c = 0; c < CH; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
+              const uint64_t bdesc = sw128_desc(sb + c * BN * 128 + 32 * k);
+#pragma unroll
+              for (int m = 0; m < NA; ++m)
+                mma_mxf8f6f4(d_tmem + m * BN, sw128_desc(sa + m * C::kATile + c * 16384 + 32 * k), bdesc,
+                             idesc, sf + (m * CH + c) * 4, sf + (NA * CH + c) * 4, (s | c | k) ? 1u : 0u);
+            }
           mma_commit(&empty_bar[slot]);
         }
         if (!ok) break;
@@ -213,112 +221,112 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     }
   } else if (warp >= 6) {
     // ------------------------------------------------------- scale factors
+    // The scale words of NB stages are fetched at once (double-buffered in
+    // registers), so a global-load latency is paid per NB stages.
+    constexpr int NB = 4, NW = NA * CH + NC * CH;  // words per stage
     const int q = warp & 3;
     uint32_t g = 0;
-    for (int u = blockIdx.x; u < total && !aborted(); u += gridDim.x) {
-      const Unit un = decode_unit<BN>(p, u, mt_per_expert, row_tile, n_act);
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok && !aborted(); u += gridDim.x) {
+      const Unit un = decode_unit(p, u, mt_per_expert);
       const bool sh = un.e >= p.E;
-      const int r = 32 * q + lane;  // weight row of this lane within the tile
-      const uint8_t* sa_row;
-      if (MODE == kModeUp) {
-        const uint8_t* base = sh ? p.sa_shared[r >= 64] : p.sa_routed[r >= 64];
-        const int erow = (sh ? un.e - p.E : un.e) * p.rows + un.row0 + (r & 63);
-        sa_row = base + (size_t)erow * (p.K / 32);
-      } else {
-        const uint8_t* base = sh ? p.sa_shared[0] : p.sa_routed[0];
-        const int erow = (sh ? un.e - p.E : un.e) * p.rows + un.row0 + r;
-        sa_row = base + (size_t)erow * (p.K / 32);
-      }
-      bool ok = true;
-      for (int s = 0; s < k_stages; ++s, ++g) {
-        const int slot = g % C::kStages;
-        const uint32_t ph = (g / C::kStages) & 1;
-        if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); ok = false; break; }
-        fence_after();
-        const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + sf_col0 + slot * C::kSfCols;
-        tmem_st_x1(col + q, *reinterpret_cast<const uint32_t*>(sa_row + 4 * s));
+      const size_t erow = (size_t)(sh ? un.e - p.E : un.e) * p.rows + un.row0 + 32 * q + lane;
+      const uint8_t* sa_row[NA];
 #pragma unroll
-        for (int c = 0; c < (BN + 31) / 32; ++c) {
-          const int n = lane + 32 * c;
-          uint32_t w = 0x7F7F7F7Fu;  // 1.0 for tokens outside the tile
-          if (n < un.m_tile)
-            w = *reinterpret_cast<const uint32_t*>(p.sb + (size_t)(un.p0 + un.n0 + n) * (p.K / 32) + 4 * s);
-          tmem_st_x1(col + 4 + c, w);
-        }
-        tmem_st_wait();
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sf_bar[slot]);
+      for (int m = 0; m < NA; ++m) sa_row[m] = (sh ? p.sa_shared[m] : p.sa_routed[m]) + erow * (p.K / 32);
+      const uint8_t* sb_row[NC];
+#pragma unroll
+      for (int cb = 0; cb < NC; ++cb) {
+        const int n = lane + 32 * cb;
+        sb_row[cb] = n < un.m_tile ? p.sb + (size_t)(un.pos0 + n) * (p.K / 32) : nullptr;
       }
-      if (!ok) break;
+      auto load = [&](uint32_t (&w)[NB][NW], int s0) {
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          if (s0 + i < k_stages) {
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+              const int kb = 4 * ((s0 + i) * CH + c);  // first k-block of the chunk
+#pragma unroll
+              for (int m = 0; m < NA; ++m) w[i][m * CH + c] = __ldg(reinterpret_cast<const uint32_t*>(sa_row[m] + kb));
+#pragma unroll
+              for (int cb = 0; cb < NC; ++cb)
+                w[i][NA * CH + c * NC + cb] =
+                    sb_row[cb] ? __ldg(reinterpret_cast<const uint32_t*>(sb_row[cb] + kb)) : 0x7F7F7F7Fu;
+            }
+          }
+        }
+      };
+      auto store = [&](const uint32_t (&w)[NB][NW], int s0) -> bool {
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          if (s0 + i >= k_stages) break;
+          const int slot = g % C::kStages;
+          const uint32_t ph = (g / C::kStages) & 1;
+          if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); return false; }
+          fence_after();
+          const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + sf_col0 + slot * C::kSfCols;
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+#pragma unroll
+            for (int m = 0; m < NA; ++m) tmem_st_x1(col + (m * CH + c) * 4 + q, w[i][m * CH + c]);
+#pragma unroll
+            for (int cb = 0; cb < NC; ++cb) tmem_st_x1(col + (NA * CH + c) * 4 + cb, w[i][NA * CH + c * NC + cb]);
+          }
+          tmem_st_wait();
+          fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sf_bar[slot]);
+          ++g;
+        }
+        return true;
+      };
+      uint32_t w0[NB][NW], w1[NB][NW];
+      load(w0, 0);
+      for (int s0 = 0; s0 < k_stages; s0 += 2 * NB) {
+        if (s0 + NB < k_stages) load(w1, s0 + NB);
+        if (!(ok = store(w0, s0))) break;
+        if (s0 + NB >= k_stages) break;
+        if (s0 + 2 * NB < k_stages) load(w0, s0 + 2 * NB);
+        if (!(ok = store(w1, s0 + NB))) break;
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant of this warp
     uint32_t it = 0;
     for (int u = blockIdx.x; u < total && !aborted(); u += gridDim.x, ++it) {
-      const Unit un = decode_unit<BN>(p, u, mt_per_expert, row_tile, n_act);
-      const int buf = it & 1;
-      if (!mbar_wait(&accf_bar[buf], (it >> 1) & 1, kWaitLimit)) { give_up(); break; }
+      const Unit un = decode_unit(p, u, mt_per_expert);
+      const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
+      const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
+      if (!mbar_wait(&accf_bar[buf], ph_acc, kWaitLimit)) { give_up(); break; }
       fence_after();
-      const uint32_t t_base = tmem + ((uint32_t)(32 * q) << 16) + buf * BN;
-      if (MODE == kModeDown) {
-        float* orow = p.o + (size_t)(un.p0 + un.n0) * p.out_cols + un.row0 + 32 * q + lane;
+      const uint32_t t_base = tmem + ((uint32_t)(32 * q) << 16) + buf * C::kAccCols;
+      const int row = un.row0 + 32 * q + lane;  // weight row (I row for up, H row for down)
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(t_base + c, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c + j < un.m_tile) orow[(size_t)(c + j) * p.out_cols] = __uint_as_float(v[j]);
-        }
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce_bar[buf]);
-      } else {
-        float* ub = ubuf + (q & 1) * 32 * C::kUbufStride + lane * C::kUbufStride;
-        if (q >= 2) {
-          // u rows: park them in shared memory for the g warps
-#pragma unroll 1
-          for (int c = 0; c < BN; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(t_base + c, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) ub[c + j] = __uint_as_float(v[j]);
-          }
+      for (int c = 0; c < BN; c += 16) {
+        uint32_t v[16], vu[16];
+        tmem_ld16(t_base + c, v);
+        if (MODE == kModeUp) tmem_ld16(t_base + BN + c, vu);
+        tmem_ld_wait();
+        if (c + 16 >= BN) {
           fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[buf]);
-          named_bar_sync(1, 128);
-          named_bar_sync(1, 128);
-        } else {
-          named_bar_sync(1, 128);
-          const int irow = un.row0 + 32 * q;  // first intermediate row of this warp
-#pragma unroll 1
-          for (int c = 0; c < BN; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(t_base + c, v);
-            tmem_ld_wait();
-            if (c + 16 >= BN) {
-              fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&acce_bar[buf]);
-            }
+        }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (c + j >= un.m_tile) break;  // warp-uniform
-              const float gg = __uint_as_float(v[j]);
-              const float h = gg / (1.0f + expf(-gg)) * ub[c + j];
-              const int ex = fp8_block_exponent(warp_max(fabsf(h)));
-              const uint32_t code = e4m3x2(scale_pow2_neg(h, ex), 0.f) & 0xFFu;
-              const size_t pos = (size_t)(un.p0 + un.n0 + c + j);
-              p.hq[pos * p.out_cols + irow + lane] = (uint8_t)code;
-              if (lane == 0) p.hs[pos * (p.out_cols / 32) + irow / 32] = (uint8_t)(ex + 127);
-            }
+        for (int j = 0; j < 16; ++j) {
+          if (c + j >= un.m_tile) break;  // warp-uniform
+          const size_t pos = (size_t)(un.pos0 + c + j);
+          if (MODE == kModeDown) {
+            p.o[pos * p.out_cols + row] = __uint_as_float(v[j]);
+          } else {
+            const float gg = __uint_as_float(v[j]);
+            const float h = gg / (1.0f + expf(-gg)) * __uint_as_float(vu[j]);
+            const int ex = fp8_block_exponent(warp_max(fabsf(h)));
+            p.hq[pos * p.out_cols + row] = (uint8_t)(e4m3x2(scale_pow2_neg(h, ex), 0.f) & 0xFFu);
+            if (lane == 0) p.hs[pos * (p.out_cols / 32) + (un.row0 + 32 * q) / 32] = (uint8_t)(ex + 127);
           }
-          named_bar_sync(1, 128);
         }
       }
     }
@@ -331,20 +339,27 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   }
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, int CH>
 cudaError_t launch_one(const MmaParams& p, int num_sms, cudaStream_t st) {
-  using C = Cfg<BN>;
+  using C = Cfg<MODE, BN, CH>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_mma_kernel<MODE, BN>,
+    cudaError_t e = cudaFuncSetAttribute(ffn_mma_kernel<MODE, BN, CH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  ffn_mma_kernel<MODE, BN><<<num_sms, kThreadsMma, C::kSmemBytes, st>>>(p);
+  ffn_mma_kernel<MODE, BN, CH><<<num_sms, kThreadsMma, C::kSmemBytes, st>>>(p);
   return cudaGetLastError();
+}
+
+template <int MODE, int CH>
+cudaError_t launch_bn(const MmaParams& p, int bn, int num_sms, cudaStream_t st) {
+  if (bn == 16) return launch_one<MODE, 16, CH>(p, num_sms, st);
+  if (bn == 64) return launch_one<MODE, 64, CH>(p, num_sms, st);
+  return launch_one<MODE, 128, CH>(p, num_sms, st);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -366,38 +381,33 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Weight bank [rows][K] of packed E2M1, loaded as boxes of 128 elements x
-// box_rows rows and expanded to one byte per element in shared memory.
-bool map_fp4(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+// 3-D view {128-element chunk, row, chunk index} of a row-major [rows][K]
+// matrix; a box is {128, box_rows, ch}: box_rows rows of ch consecutive
+// chunks, stored in shared memory chunk-major (one swizzled tile per chunk).
+// fp4: packed E2M1, expanded to one byte per element in shared memory.
+bool map_3d(CUtensorMap* m, bool fp4, const void* base, uint64_t K, uint64_t rows,
+            uint32_t box_rows, uint32_t ch) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !base) return false;
-  cuuint64_t dims[2] = {K, rows};
-  cuuint64_t strides[1] = {K / 2};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t row_bytes = fp4 ? K / 2 : K, chunk_bytes = fp4 ? 64 : 128;
+  cuuint64_t dims[3] = {128, rows, K / 128};
+  cuuint64_t strides[2] = {row_bytes, chunk_bytes};
+  cuuint32_t box[3] = {128, box_rows, ch};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Activations by position [rows][K] of E4M3 bytes, boxes of 128 x box_rows.
-bool map_u8(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc || !base) return false;
-  cuuint64_t dims[2] = {K, rows};
-  cuuint64_t strides[1] = {K};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
+int chunks_per_stage(int K) { return K % 256 == 0 ? 2 : 1; }
 
 }  // namespace
 
 struct MmaMaps {
   CUtensorMap gate, up, down, s_gate, s_up, s_down;
   CUtensorMap xg[3], hq[3];  // per token tile width: 16, 64, 128
+  int ch_up, ch_down;
 };
 
 static int bn_index(int bn) { return bn == 16 ? 0 : (bn == 64 ? 1 : 2); }
@@ -408,15 +418,19 @@ MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Worksp
   MmaMaps* m = new MmaMaps();
   const uint64_t H = c.hidden, I = c.inter, E = c.n_experts, ns = c.n_shared;
   const uint64_t P = (uint64_t)c.max_tokens * (c.top_k + c.n_shared);
-  bool ok = map_fp4(&m->gate, w.gate.codes, H, E * I, 64) && map_fp4(&m->up, w.up.codes, H, E * I, 64) &&
-            map_fp4(&m->down, w.down.codes, I, E * H, 128);
+  m->ch_up = chunks_per_stage((int)H);
+  m->ch_down = chunks_per_stage((int)I);
+  bool ok = map_3d(&m->gate, true, w.gate.codes, H, E * I, 128, m->ch_up) &&
+            map_3d(&m->up, true, w.up.codes, H, E * I, 128, m->ch_up) &&
+            map_3d(&m->down, true, w.down.codes, I, E * H, 128, m->ch_down);
   if (ok && ns > 0)
-    ok = map_fp4(&m->s_gate, w.s_gate.codes, H, ns * I, 64) &&
-         map_fp4(&m->s_up, w.s_up.codes, H, ns * I, 64) &&
-         map_fp4(&m->s_down, w.s_down.codes, I, ns * H, 128);
+    ok = map_3d(&m->s_gate, true, w.s_gate.codes, H, ns * I, 128, m->ch_up) &&
+         map_3d(&m->s_up, true, w.s_up.codes, H, ns * I, 128, m->ch_up) &&
+         map_3d(&m->s_down, true, w.s_down.codes, I, ns * H, 128, m->ch_down);
   const uint32_t bns[3] = {16, 64, 128};
   for (int i = 0; ok && i < 3; ++i)
-    ok = map_u8(&m->xg[i], ws.xg, H, P, bns[i]) && map_u8(&m->hq[i], ws.hq, I, P, bns[i]);
+    ok = map_3d(&m->xg[i], false, ws.xg, H, P, bns[i], m->ch_up) &&
+         map_3d(&m->hq[i], false, ws.hq, I, P, bns[i], m->ch_down);
   if (!ok) {
     delete m;
     return nullptr;
@@ -431,6 +445,7 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
   MmaParams p;
   memset(&p, 0, sizeof(p));
   const int bi = bn_index(bn);
+  int ch;
   if (mode == kModeUp) {
     p.a_routed[0] = mm.gate;
     p.a_routed[1] = mm.up;
@@ -445,6 +460,7 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
     p.K = bk.H;
     p.rows = bk.I;
     p.out_cols = bk.I;
+    ch = mm.ch_up;
   } else {
     p.a_routed[0] = mm.down;
     p.a_shared[0] = mm.s_down;
@@ -455,25 +471,19 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
     p.K = bk.I;
     p.rows = bk.H;
     p.out_cols = bk.H;
+    ch = mm.ch_down;
   }
   p.E = bk.E;
-  p.active = ws.active;
   p.n_active = ws.n_active;
-  p.off = ws.off;
-  p.cnt = ws.cnt;
   p.tile_prefix = ws.tile_prefix;
+  p.tile_info = ws.tile_info;
   p.hq = ws.hq;
   p.hs = ws.hs;
   p.o = ws.o;
   p.err = ws.err;
-  if (mode == kModeUp) {
-    if (bn == 16) return launch_one<kModeUp, 16>(p, num_sms, st);
-    if (bn == 64) return launch_one<kModeUp, 64>(p, num_sms, st);
-    return launch_one<kModeUp, 128>(p, num_sms, st);
-  }
-  if (bn == 16) return launch_one<kModeDown, 16>(p, num_sms, st);
-  if (bn == 64) return launch_one<kModeDown, 64>(p, num_sms, st);
-  return launch_one<kModeDown, 128>(p, num_sms, st);
+  if (mode == kModeUp)
+    return ch == 2 ? launch_bn<kModeUp, 2>(p, bn, num_sms, st) : launch_bn<kModeUp, 1>(p, bn, num_sms, st);
+  return ch == 2 ? launch_bn<kModeDown, 2>(p, bn, num_sms, st) : launch_bn<kModeDown, 1>(p, bn, num_sms, st);
 }
 
 }  // namespace moe

@@ -25,12 +25,14 @@ struct Workspace {
   int32_t* active = nullptr;  // [NE]       experts with tokens, routed then shared
   int32_t* n_active = nullptr;// [1]
   int32_t* tile_prefix = nullptr; // [NE+1] token tiles before each active expert
+  int4* tile_info = nullptr;  // [tiles]    (expert, first position, tokens, 0) per token tile
   uint8_t* xg = nullptr;      // [P][H]     E4M3 codes of x, gathered by position
   uint8_t* xgs = nullptr;     // [P][H/32]
   uint8_t* hq = nullptr;      // [P][I]     E4M3 codes of h
   uint8_t* hs = nullptr;      // [P][I/32]  UE8M0 scale bytes of h
   float* o = nullptr;         // [P][H]     expert outputs per position
   float* logits = nullptr;    // [T][E]     router logits scratch
+  float* rpart = nullptr;     // [8][min(T,64)][E] split-K router partial sums
   int32_t* idx = nullptr;     // [T][k]     routing scratch (host entry point)
   float* w = nullptr;         // [T][k]
   uint16_t* x = nullptr;      // [T][H]     bf16 staging (host entry point)
@@ -85,6 +87,11 @@ cudaError_t launch_quantize_gather(const uint16_t* x, int P, int H, const int32_
                                    uint8_t* xg, uint8_t* xgs, cudaStream_t st);
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const float* W,
                                  const float* b, float* logits, int num_sms, cudaStream_t st);
+int router_ksplit(int H);
+constexpr int kRouterSplitMaxT = 64;
+cudaError_t launch_router_split(const uint16_t* x, int T, int H, int E, int k, const float* W,
+                                const float* b, float* part, float* logits_out, int32_t* idx,
+                                float* w, cudaStream_t st);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t st);
 cudaError_t launch_ffn_up_simt(const ExpertBank& bank, int T, int k, int n_shared,

@@ -189,6 +189,15 @@ __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restric
     __syncwarp();
   }
   for (int i = threadIdx.x; i < ns * T; i += blockDim.x) ws.pos_tok[S + i] = i % T;
+  // token tiles of width bn for the tensor-core path: (expert, first position, tokens)
+  if (bn > 0) {
+    const int na = *ws.n_active;
+    for (int a = threadIdx.x; a < na; a += blockDim.x) {
+      const int e = ws.active[a], c = ws.cnt[e], p0 = ws.off[e], t0 = ws.tile_prefix[a];
+      for (int j = 0; j * bn < c; ++j)
+        ws.tile_info[t0 + j] = make_int4(e, p0 + j * bn, min(bn, c - j * bn), 0);
+    }
+  }
   // positions left free by invalid expert ids still name a real token, so
   // that every position's row can be read safely
   for (int p = routed_total + threadIdx.x; p < S; p += blockDim.x) ws.pos_tok[p] = 0;

@@ -55,20 +55,10 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
-// One warp per token; lane l holds logits l, l+32, ... (E <= 512).  k rounds
-// of a warp arg-max over (value desc, index asc); NaN counts as -infinity.
-__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                            int32_t* __restrict__ idx, float* __restrict__ w) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (t >= T) return;
-  float v[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int e = lane + 32 * i;
-    float f = e < E ? logits[(size_t)t * E + e] : -INFINITY;
-    v[i] = isnan(f) ? -INFINITY : f;
-  }
+// k rounds of a warp arg-max over (value desc, index asc) on the 16 values
+// per lane (v[i] is expert lane + 32 i), then the softmax over the k chosen.
+__device__ __forceinline__ void select_topk(const float (&v)[16], int t, int E, int k, int lane,
+                                            int32_t* __restrict__ idx, float* __restrict__ w) {
   uint32_t taken = 0;
   float sv[8];
   int si[8];
@@ -107,7 +97,112 @@ __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int 
   }
 }
 
+// One warp per token; lane l holds logits l, l+32, ... (E <= 512).  k rounds
+// of a warp arg-max over (value desc, index asc); NaN counts as -infinity.
+__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                            int32_t* __restrict__ idx, float* __restrict__ w) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int e = lane + 32 * i;
+    float f = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+    v[i] = isnan(f) ? -INFINITY : f;
+  }
+  select_topk(v, t, E, k, lane, idx, w);
+}
+
+// Split-K variant for small T: warp = (expert, K chunk); partial sums go to
+// part[ks][t][e] and are added in fixed ks order by topk_sum_kernel.
+template <int TT>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+    router_partial_kernel(const uint16_t* __restrict__ x, int T, int H, int E, int kc,
+                          const float* __restrict__ W, float* __restrict__ part) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRouterWarps + warp;
+  if (e >= E) return;
+  const int t0 = blockIdx.y * TT, ks = blockIdx.z;
+  const int nt = min(TT, T - t0);
+  float acc[TT];
+#pragma unroll
+  for (int i = 0; i < TT; ++i) acc[i] = 0.f;
+  const int k0 = ks * kc;
+  const float4* wr = reinterpret_cast<const float4*>(W + (size_t)e * H + k0);
+  for (int h4 = lane; h4 < kc / 4; h4 += 32) {
+    const float4 wv = __ldg(wr + h4);
+#pragma unroll
+    for (int i = 0; i < TT; ++i) {
+      if (i < nt) {
+        const uint2 xv = *reinterpret_cast<const uint2*>(x + (size_t)(t0 + i) * H + k0 + 4 * h4);
+        acc[i] = fmaf(wv.x, __uint_as_float(xv.x << 16), acc[i]);
+        acc[i] = fmaf(wv.y, __uint_as_float(xv.x & 0xFFFF0000u), acc[i]);
+        acc[i] = fmaf(wv.z, __uint_as_float(xv.y << 16), acc[i]);
+        acc[i] = fmaf(wv.w, __uint_as_float(xv.y & 0xFFFF0000u), acc[i]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < TT; ++i) {
+    const float sum = warp_sum(acc[i]);
+    if (lane == 0 && i < nt) part[((size_t)ks * T + t0 + i) * E + e] = sum;
+  }
+}
+
+// One CTA per token: all threads add the split-K partials of the token's
+// logits (fixed ks order, plus bias) in parallel, then one warp selects.
+__global__ void __launch_bounds__(256) topk_sum_kernel(const float* __restrict__ part, int ksplit,
+                                                       const float* __restrict__ b, int T, int E,
+                                                       int k, float* __restrict__ logits_out,
+                                                       int32_t* __restrict__ idx,
+                                                       float* __restrict__ w) {
+  __shared__ float lg[512];
+  const int t = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float f = 0.f;
+    for (int s = 0; s < ksplit; ++s) f += part[((size_t)s * T + t) * E + e];
+    f += b ? b[e] : 0.f;
+    lg[e] = f;
+    if (logits_out) logits_out[(size_t)t * E + e] = f;
+  }
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int e = lane + 32 * i;
+    const float f = e < E ? lg[e] : -INFINITY;
+    v[i] = isnan(f) ? -INFINITY : f;
+  }
+  select_topk(v, t, E, k, lane, idx, w);
+}
+
 }  // namespace
+
+int router_ksplit(int H) {
+  const int chunks = H / 128;
+  for (int ks = 8; ks > 1; --ks)
+    if (chunks % ks == 0) return ks;
+  return 1;
+}
+
+cudaError_t launch_router_split(const uint16_t* x, int T, int H, int E, int k, const float* W,
+                                const float* b, float* part, float* logits_out, int32_t* idx,
+                                float* w, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int ks = router_ksplit(H);
+  const int gx = (E + kRouterWarps - 1) / kRouterWarps;
+  if (T <= 2)
+    router_partial_kernel<2><<<dim3(gx, (T + 1) / 2, ks), kRouterWarps * 32, 0, st>>>(x, T, H, E, H / ks, W, part);
+  else
+    router_partial_kernel<8><<<dim3(gx, (T + 7) / 8, ks), kRouterWarps * 32, 0, st>>>(x, T, H, E, H / ks, W, part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  topk_sum_kernel<<<T, 256, 0, st>>>(part, ks, b, T, E, k, logits_out, idx, w);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const float* W,
                                  const float* b, float* logits, int num_sms, cudaStream_t st) {
