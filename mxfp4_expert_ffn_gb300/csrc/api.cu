@@ -69,7 +69,9 @@ size_t carve(const moe_config& c, char* base, Workspace& ws) {
   ws.hs = cv.take<uint8_t>(P * I / 32);
   ws.o = cv.take<float>(P * H);
   ws.logits = cv.take<float>(T * E);
-  ws.rpart = cv.take<float>(8 * (T < kRouterSplitMaxT ? T : kRouterSplitMaxT) * E);
+  const size_t split_rows = 8 * (T < (size_t)kRouterSplitMaxT ? T : (size_t)kRouterSplitMaxT);
+  ws.rpart = cv.take<float>((split_rows > 4 * T ? split_rows : 4 * T) * E);
+  ws.w3 = cv.take<uint16_t>(3 * E * H);
   ws.idx = cv.take<int32_t>(T * k);
   ws.w = cv.take<float>(T * k);
   ws.x = cv.take<uint16_t>(T * H);
@@ -231,6 +233,10 @@ moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int dev
   if (e == cudaSuccess) {
     L->maps = mma_maps_create(*cfg, *w, L->ws);  // NULL: tensor-core path unavailable
     cudaGetLastError();
+    e = router_split_weights(w->router_w, cfg->n_experts, cfg->hidden, L->ws.w3, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+      L->router_mma = router_map_weights(&L->router_map, L->ws.w3, cfg->n_experts, cfg->hidden);
   }
   if (e != cudaSuccess) {
     if (L->ws.err_host) cudaFreeHost(L->ws.err_host);
@@ -333,6 +339,16 @@ moe_status route_impl(moe_layer* L, const void* x, int32_t T, const float* logit
     return cuda_fail(launch_router_split(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts,
                                          c.top_k, L->w.router_w, L->w.router_b, L->ws.rpart,
                                          logits_out, idx, w, st));
+  }
+  if (!lg && L->router_mma && L->path != 1) {
+    // many tokens: tensor-core logits (three bf16 parts of W_r), K split over CTAs
+    TimedScope ts(L, st, "router_mma");
+    e = launch_router_mma(L->router_map, static_cast<const uint16_t*>(x), T, c.n_experts, c.hidden,
+                          L->ws.rpart, L->ws.err, L->num_sms, st);
+    if (e == cudaSuccess)
+      e = launch_topk_sum(L->ws.rpart, router_mma_ksplit(c.hidden), L->w.router_b, T, c.n_experts,
+                          c.top_k, logits_out, idx, w, st);
+    return cuda_fail(e);
   }
   if (!lg) {
     float* dst = logits_out ? logits_out : L->ws.logits;

@@ -1,6 +1,7 @@
 // Internal declarations: the layer handle and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,7 +33,8 @@ struct Workspace {
   uint8_t* hs = nullptr;      // [P][I/32]  UE8M0 scale bytes of h
   float* o = nullptr;         // [P][H]     expert outputs per position
   float* logits = nullptr;    // [T][E]     router logits scratch
-  float* rpart = nullptr;     // [8][min(T,64)][E] split-K router partial sums
+  float* rpart = nullptr;     // split-K router partial sums ([8][min(T,64)][E] or [4][T][E])
+  uint16_t* w3 = nullptr;     // [3][E][H]  router weights as three bf16 parts
   int32_t* idx = nullptr;     // [T][k]     routing scratch (host entry point)
   float* w = nullptr;         // [T][k]
   uint16_t* x = nullptr;      // [T][H]     bf16 staging (host entry point)
@@ -62,6 +64,8 @@ struct moe_layer {
   bool timing = false;
   moe::Workspace ws;
   moe::MmaMaps* maps = nullptr;  // TMA descriptors of the tensor-core path
+  CUtensorMap router_map;        // the bf16 router parts, for the tensor-core router
+  bool router_mma = false;
   moe::Timer timers[moe::kMaxTimed];
   int n_timers = 0;
   cudaEvent_t ev_pool[2 * 64] = {};
@@ -92,6 +96,13 @@ constexpr int kRouterSplitMaxT = 64;
 cudaError_t launch_router_split(const uint16_t* x, int T, int H, int E, int k, const float* W,
                                 const float* b, float* part, float* logits_out, int32_t* idx,
                                 float* w, cudaStream_t st);
+cudaError_t launch_topk_sum(const float* part, int ksplit, const float* b, int T, int E, int k,
+                            float* logits_out, int32_t* idx, float* w, cudaStream_t st);
+int router_mma_ksplit(int H);
+cudaError_t router_split_weights(const float* w, int E, int H, uint16_t* w3, cudaStream_t st);
+bool router_map_weights(CUtensorMap* m, const uint16_t* w3, int E, int H);
+cudaError_t launch_router_mma(const CUtensorMap& w3map, const uint16_t* x, int T, int E, int H,
+                              float* part, int32_t* err, int num_sms, cudaStream_t st);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t st);
 cudaError_t launch_ffn_up_simt(const ExpertBank& bank, int T, int k, int n_shared,

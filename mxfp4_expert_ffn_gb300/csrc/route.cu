@@ -204,6 +204,13 @@ cudaError_t launch_router_split(const uint16_t* x, int T, int H, int E, int k, c
   return cudaGetLastError();
 }
 
+cudaError_t launch_topk_sum(const float* part, int ksplit, const float* b, int T, int E, int k,
+                            float* logits_out, int32_t* idx, float* w, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  topk_sum_kernel<<<T, 256, 0, st>>>(part, ksplit, b, T, E, k, logits_out, idx, w);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const float* W,
                                  const float* b, float* logits, int num_sms, cudaStream_t st) {
   (void)num_sms;

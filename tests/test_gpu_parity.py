@@ -274,3 +274,23 @@ def test_gpu_bank_fill_equals_host_generator():
             assert np.array_equal(W[k][e].cpu().numpy(), ex[k]), (e, k)
     sh = synth.host_expert(wl, 1, wl.n_experts + 1)
     assert np.array_equal(W["s_down_codes"][1].cpu().numpy(), sh["down_codes"])
+
+
+@pytest.mark.parametrize("wl", [
+    Workload("router_t200_e40_h256", 256, 128, 40, 6, 1, 200, seed=31),
+    Workload("router_t130_e384_h512", 512, 128, 384, 6, 1, 130, seed=32, zipf=1.1),
+], ids=lambda w: w.name)
+def test_router_many_tokens_tensor_core(wl):
+    # more than 64 tokens: logits from the tensor-core router (three bf16 parts
+    # of W_r, K split over CTAs), ragged expert and token tiles
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    lg = oracle.router_logits(x, synth.router_weights(wl), synth.router_bias(wl))
+    idx, w, lo = gu.run_route(L, x, wl.tokens, wl.n_experts, wl.top_k)
+    tol = 1e-5 * np.abs(lg).max(axis=1, keepdims=True)
+    assert (np.abs(lo - lg) <= tol).all(), np.abs(lo - lg).max()
+    srt = -np.sort(-lg, axis=1)
+    sure = srt[:, wl.top_k - 1] - srt[:, wl.top_k] > 2 * tol[:, 0]
+    ridx, _ = oracle.topk(lg, wl.top_k)
+    assert np.array_equal(np.sort(idx[sure], 1), np.sort(ridx[sure], 1))
+    L.close()
