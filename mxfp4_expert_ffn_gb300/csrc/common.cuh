@@ -84,6 +84,12 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc)
   return acc;
 }
 
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has finished and flushed its writes (a no-op when the kernel was not
+// launched as a dependent), then let the next kernel start its prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

@@ -47,6 +47,9 @@ struct MmaParams {
   const int32_t* n_active;
   const int32_t* tile_prefix;
   const int4* tile_info;
+  int n_stages;              // ring depth (runtime: fits the shared memory)
+  int merged[2];             // up mode, routed / shared: gate and up load as one 4-D op
+  int swap_gu[2];            // ... whose first matrix is the up bank
   uint8_t* hq;
   uint8_t* hs;
   float* o;
@@ -63,24 +66,34 @@ constexpr int kSmemBudget = 227 * 1024 - 2048;
 
 constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
 
+constexpr int kMaxStages = 6;
+
 template <int MODE, int BN, int CH>
 struct Cfg {
   static constexpr int kNA = MODE == kModeUp ? 2 : 1;     // weight matrices per unit
   static constexpr int kATile = 128 * 128 * CH;           // one matrix, one stage
   static constexpr int kBTile = BN * 128 * CH;
-  static constexpr int kStageBytes = kNA * kATile + kBTile;
-  static constexpr int kStages = (kSmemBudget - 1024) / kStageBytes > 6 ? 6 : (kSmemBudget - 1024) / kStageBytes;
   static constexpr int kAccCols = kNA * BN;               // g then u (up) or o (down)
   static constexpr int kNAcc = (MODE == kModeUp && BN >= 128) ? 1 : 2;
   static constexpr int kSfCols = (kNA + 1) * 4 * CH;      // 4 columns per (matrix, chunk)
-  static constexpr int kTmemCols = kNAcc * kAccCols + kStages * kSfCols;
+  static constexpr int kTmemCols = kNAcc * kAccCols + kMaxStages * kSfCols;
   static constexpr int kTmemAlloc = pow2_cols(kTmemCols);
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes;
-  static constexpr uint32_t kTxBytes = kNA * 128 * 64 * CH + BN * 128 * CH;
-  static_assert(kStages >= 2, "pipeline depth");
   static_assert(kTmemCols <= 512, "TMEM budget");
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
+
+// Pipeline geometry: as many stages as fit the shared memory (at most
+// kMaxStages).  The bytes in flight per SM bound the bandwidth (about ten TMA
+// ops in flight, a few microseconds each), so every byte of shared memory goes
+// to the ring.
+template <int MODE, int BN, int CH>
+void geometry(int K, int* n_stages, int* smem) {
+  using C = Cfg<MODE, BN, CH>;
+  (void)K;
+  const int stage = C::kNA * C::kATile + C::kBTile;
+  const int st = (kSmemBudget - 1024) / stage;
+  *n_stages = st > kMaxStages ? kMaxStages : st;
+  *smem = 1024 + *n_stages * stage;
+}
 
 struct Unit {
   int e, pos0, m_tile, row0;
@@ -92,6 +105,15 @@ __device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_pe
   const int v = u / mt_per_expert;
   const int4 t = __ldg(p.tile_info + v);
   return Unit{t.x, t.y, t.z, (u - v * mt_per_expert) * 128};
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
@@ -109,20 +131,23 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   constexpr int NA = C::kNA;
   constexpr int NC = (BN + 31) / 32;  // 32-token groups of the B scale factors
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* stage_base = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full_bar[C::kStages], sf_bar[C::kStages], empty_bar[C::kStages];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages], sf_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt_per_expert = p.rows / 128;
-  const int total = p.tile_prefix[*p.n_active] * mt_per_expert;
   const int k_stages = p.K / (128 * CH);
+  const int NS = p.n_stages;
+  uint8_t* stage_base = smem;
+  const int stage_bytes = NA * C::kATile + C::kBTile;
+  const uint32_t tx_stage = NA * 128 * 64 * CH + BN * 128 * CH;
   const uint32_t sf_col0 = C::kNAcc * C::kAccCols;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&sf_bar[s], 4);
       mbar_init(&empty_bar[s], 1);
@@ -139,6 +164,10 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_slot;
+  // the prologue above overlaps the previous kernel; its outputs are read below
+  pdl_wait();
+  pdl_trigger();
+  const int total = p.tile_prefix[*p.n_active] * mt_per_expert;
 
   auto give_up = [&]() {
     atomicOr(p.err, kErrTimeout);
@@ -150,32 +179,39 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       uint32_t g = 0;
-      int last_parity[C::kStages];
+      int last_parity[kMaxStages];
 #pragma unroll
-      for (int s = 0; s < C::kStages; ++s) last_parity[s] = -1;
+      for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
       for (int u = blockIdx.x; u < total && !aborted(); u += gridDim.x) {
         const Unit un = decode_unit(p, u, mt_per_expert);
         const bool sh = un.e >= p.E;
         const int erow = (sh ? un.e - p.E : un.e) * p.rows + un.row0;
+        bool ok = true;
         for (int s = 0; s < k_stages; ++s, ++g) {
-          const int slot = g % C::kStages;
-          const uint32_t ph = (g / C::kStages) & 1;
-          if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); break; }
-          uint8_t* sa = stage_base + slot * C::kStageBytes;
-          mbar_expect_tx(&full_bar[slot], C::kTxBytes);
+          const int slot = g % NS;
+          const uint32_t ph = (g / NS) & 1;
+          if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); ok = false; break; }
+          uint8_t* sa = stage_base + slot * stage_bytes;
+          mbar_expect_tx(&full_bar[slot], tx_stage);
+          if (NA == 2 && p.merged[sh]) {
+            // gate and up rows of the stage in one op: {chunk elems, rows, chunks, matrix}
+            tma_load_4d(sa, sh ? &p.a_shared[0] : &p.a_routed[0], 0, erow, s * CH, 0, &full_bar[slot]);
+          } else {
 #pragma unroll
-          for (int m = 0; m < NA; ++m)
-            tma_load_3d(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
-                        &full_bar[slot]);
+            for (int m = 0; m < NA; ++m)
+              tma_load_3d(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
+                          &full_bar[slot]);
+          }
           tma_load_3d(sa + NA * C::kATile, &p.b, 0, un.pos0, s * CH, &full_bar[slot]);
 #pragma unroll
-          for (int i = 0; i < C::kStages; ++i)
+          for (int i = 0; i < kMaxStages; ++i)
             if (i == slot) last_parity[i] = (int)ph;
         }
+        if (!ok) break;
       }
-      // never leave with copies in flight: wait for the last load into each slot
+      // never leave with copies in flight: wait for the last load into each buffer
 #pragma unroll
-      for (int s = 0; s < C::kStages; ++s)
+      for (int s = 0; s < kMaxStages; ++s)
         if (last_parity[s] >= 0) mbar_wait(&full_bar[s], (uint32_t)last_parity[s], kWaitLimit);
     }
   } else if (warp == 1) {
@@ -189,17 +225,23 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         if (!mbar_wait(&acce_bar[buf], ph_acc ^ 1, kWaitLimit)) { give_up(); break; }
         fence_after();
         const uint32_t d_tmem = tmem + buf * C::kAccCols;
+        int swap = 0;
+        if (NA == 2) {
+          const int e = decode_unit(p, u, mt_per_expert).e;
+          const int sh = e >= p.E;
+          swap = p.merged[sh] && p.swap_gu[sh];
+        }
         bool ok = true;
         for (int s = 0; s < k_stages; ++s, ++g) {
-          const int slot = g % C::kStages;
-          const uint32_t ph = (g / C::kStages) & 1;
+          const int slot = g % NS;
+          const uint32_t ph = (g / NS) & 1;
           if (!mbar_wait(&full_bar[slot], ph, kWaitLimit) || !mbar_wait(&sf_bar[slot], ph, kWaitLimit)) {
             give_up();
             ok = false;
             break;
           }
           fence_after();
-          const uint32_t sa = smem_u32(stage_base + slot * C::kStageBytes);
+          const uint32_t sa = smem_u32(stage_base + slot * stage_bytes);
           const uint32_t sb = sa + NA * C::kATile;
           const uint32_t sf = tmem + sf_col0 + slot * C::kSfCols;
 #pragma unroll
@@ -209,9 +251,11 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
               const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
               const uint64_t bdesc = sw128_desc(sb + c * BN * 128 + 32 * k);
 #pragma unroll
-              for (int m = 0; m < NA; ++m)
-                mma_mxf8f6f4(d_tmem + m * BN, sw128_desc(sa + m * C::kATile + c * 16384 + 32 * k), bdesc,
-                             idesc, sf + (m * CH + c) * 4, sf + (NA * CH + c) * 4, (s | c | k) ? 1u : 0u);
+              for (int m = 0; m < NA; ++m) {
+                const int acc = swap ? NA - 1 - m : m;  // gate -> accumulator 0, up -> 1
+                mma_mxf8f6f4(d_tmem + acc * BN, sw128_desc(sa + m * C::kATile + c * 16384 + 32 * k), bdesc,
+                             idesc, sf + (acc * CH + c) * 4, sf + (NA * CH + c) * 4, (s | c | k) ? 1u : 0u);
+              }
             }
           mma_commit(&empty_bar[slot]);
         }
@@ -261,8 +305,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
           if (s0 + i >= k_stages) break;
-          const int slot = g % C::kStages;
-          const uint32_t ph = (g / C::kStages) & 1;
+          const int slot = g % NS;
+          const uint32_t ph = (g / NS) & 1;
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); return false; }
           fence_after();
           const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + sf_col0 + slot * C::kSfCols;
@@ -340,23 +384,25 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
 }
 
 template <int MODE, int BN, int CH>
-cudaError_t launch_one(const MmaParams& p, int num_sms, cudaStream_t st) {
-  using C = Cfg<MODE, BN, CH>;
+cudaError_t launch_one(MmaParams& p, int num_sms, cudaStream_t st) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(ffn_mma_kernel<MODE, BN, CH>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  ffn_mma_kernel<MODE, BN, CH><<<num_sms, kThreadsMma, C::kSmemBytes, st>>>(p);
+  int smem = 0;
+  geometry<MODE, BN, CH>(p.K, &p.n_stages, &smem);
+  if (p.n_stages < 2) return cudaErrorInvalidConfiguration;
+  { cudaError_t le_ = launch_pdl(ffn_mma_kernel<MODE, BN, CH>, dim3(num_sms), dim3(kThreadsMma), smem, st, p); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
 template <int MODE, int CH>
-cudaError_t launch_bn(const MmaParams& p, int bn, int num_sms, cudaStream_t st) {
+cudaError_t launch_bn(MmaParams& p, int bn, int num_sms, cudaStream_t st) {
   if (bn == 16) return launch_one<MODE, 16, CH>(p, num_sms, st);
   if (bn == 64) return launch_one<MODE, 64, CH>(p, num_sms, st);
   return launch_one<MODE, 128, CH>(p, num_sms, st);
@@ -400,15 +446,42 @@ bool map_3d(CUtensorMap* m, bool fp4, const void* base, uint64_t K, uint64_t row
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int chunks_per_stage(int K) { return K % 256 == 0 ? 2 : 1; }
+int chunks_per_stage(int K, bool allow3) {
+  if (allow3 && K % 384 == 0) return 3;
+  return K % 256 == 0 ? 2 : 1;
+}
+
+// gate and up banks as one 4-D tensor {128-element chunk, row, chunk index,
+// matrix}: the matrix stride is the distance between the two banks, so one
+// box {128, 128, ch, 2} loads the same rows of both.  Needs the distance to be
+// a multiple of 32 bytes; *swap tells that the up bank comes first.
+bool map_4d_pair(CUtensorMap* m, const void* gate, const void* up, uint64_t K, uint64_t rows,
+                 uint32_t ch, int* swap) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !gate || !up) return false;
+  const uintptr_t g = (uintptr_t)gate, u = (uintptr_t)up;
+  const uintptr_t lo = g < u ? g : u, dist = g < u ? u - g : g - u;
+  if (dist == 0 || dist % 32 != 0 || dist >= (1ull << 40)) return false;
+  *swap = u < g;
+  cuuint64_t dims[4] = {128, rows, K / 128, 2};
+  cuuint64_t strides[3] = {K / 2, 64, (cuuint64_t)dist};
+  cuuint32_t box[4] = {128, 128, ch, 2};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, reinterpret_cast<void*>(lo), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
 struct MmaMaps {
   CUtensorMap gate, up, down, s_gate, s_up, s_down;
+  CUtensorMap gu_pair, s_gu_pair;  // gate + up as one 4-D tensor (when possible)
+  int merged[2], swap_gu[2];
   CUtensorMap xg[3], hq[3];  // per token tile width: 16, 64, 128
   int ch_up, ch_down;
 };
+
 
 static int bn_index(int bn) { return bn == 16 ? 0 : (bn == 64 ? 1 : 2); }
 
@@ -418,8 +491,8 @@ MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Worksp
   MmaMaps* m = new MmaMaps();
   const uint64_t H = c.hidden, I = c.inter, E = c.n_experts, ns = c.n_shared;
   const uint64_t P = (uint64_t)c.max_tokens * (c.top_k + c.n_shared);
-  m->ch_up = chunks_per_stage((int)H);
-  m->ch_down = chunks_per_stage((int)I);
+  m->ch_up = chunks_per_stage((int)H, false);
+  m->ch_down = chunks_per_stage((int)I, true);
   bool ok = map_3d(&m->gate, true, w.gate.codes, H, E * I, 128, m->ch_up) &&
             map_3d(&m->up, true, w.up.codes, H, E * I, 128, m->ch_up) &&
             map_3d(&m->down, true, w.down.codes, I, E * H, 128, m->ch_down);
@@ -427,6 +500,13 @@ MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Worksp
     ok = map_3d(&m->s_gate, true, w.s_gate.codes, H, ns * I, 128, m->ch_up) &&
          map_3d(&m->s_up, true, w.s_up.codes, H, ns * I, 128, m->ch_up) &&
          map_3d(&m->s_down, true, w.s_down.codes, I, ns * H, 128, m->ch_down);
+  m->merged[0] = m->merged[1] = 0;
+  m->swap_gu[0] = m->swap_gu[1] = 0;
+  if (ok) {
+    m->merged[0] = map_4d_pair(&m->gu_pair, w.gate.codes, w.up.codes, H, E * I, m->ch_up, &m->swap_gu[0]);
+    if (ns > 0)
+      m->merged[1] = map_4d_pair(&m->s_gu_pair, w.s_gate.codes, w.s_up.codes, H, ns * I, m->ch_up, &m->swap_gu[1]);
+  }
   const uint32_t bns[3] = {16, 64, 128};
   for (int i = 0; ok && i < 3; ++i)
     ok = map_3d(&m->xg[i], false, ws.xg, H, P, bns[i], m->ch_up) &&
@@ -447,10 +527,14 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
   const int bi = bn_index(bn);
   int ch;
   if (mode == kModeUp) {
-    p.a_routed[0] = mm.gate;
+    p.a_routed[0] = mm.merged[0] ? mm.gu_pair : mm.gate;
     p.a_routed[1] = mm.up;
-    p.a_shared[0] = mm.s_gate;
+    p.a_shared[0] = mm.merged[1] ? mm.s_gu_pair : mm.s_gate;
     p.a_shared[1] = mm.s_up;
+    for (int i = 0; i < 2; ++i) {
+      p.merged[i] = mm.merged[i];
+      p.swap_gu[i] = mm.swap_gu[i];
+    }
     p.b = mm.xg[bi];
     p.sa_routed[0] = bk.gs;
     p.sa_routed[1] = bk.us;
@@ -483,6 +567,7 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
   p.err = ws.err;
   if (mode == kModeUp)
     return ch == 2 ? launch_bn<kModeUp, 2>(p, bn, num_sms, st) : launch_bn<kModeUp, 1>(p, bn, num_sms, st);
+  if (ch == 3) return launch_bn<kModeDown, 3>(p, bn, num_sms, st);
   return ch == 2 ? launch_bn<kModeDown, 2>(p, bn, num_sms, st) : launch_bn<kModeDown, 1>(p, bn, num_sms, st);
 }
 

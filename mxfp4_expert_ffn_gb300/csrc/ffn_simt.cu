@@ -106,6 +106,8 @@ __device__ __forceinline__ float pow2f(int k) {
 
 template <int MT>
 __global__ void __launch_bounds__(kThreads) ffn_up_simt_kernel(ExpertBank bk, Workspace ws) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem[];
   const int H = bk.H, I = bk.I;
   uint32_t* xh = reinterpret_cast<uint32_t*>(smem);          // [MT][H/2] f16x2
@@ -196,6 +198,8 @@ __global__ void __launch_bounds__(kThreads) ffn_up_simt_kernel(ExpertBank bk, Wo
 
 template <int MT>
 __global__ void __launch_bounds__(kThreads) ffn_down_simt_kernel(ExpertBank bk, Workspace ws) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem[];
   const int H = bk.H, I = bk.I;
   uint32_t* xh = reinterpret_cast<uint32_t*>(smem);          // [MT][I/2] f16x2
@@ -302,9 +306,9 @@ cudaError_t launch_ffn_up_simt(const ExpertBank& bank, int T, int k, int n_share
   if (T == 0) return cudaSuccess;
   const int units_max = (bank.E + n_shared) * (bank.I / 32);
   if (T == 1) {
-    ffn_up_simt_kernel<1><<<simt_grid(units_max, num_sms, 4), kThreads, up_smem<1>(bank.H), st>>>(bank, ws);
+    { cudaError_t le_ = launch_pdl(ffn_up_simt_kernel<1>, dim3(simt_grid(units_max, num_sms, 4)), dim3(kThreads), up_smem<1>(bank.H), st, bank, ws); if (le_ != cudaSuccess) return le_; }
   } else {
-    ffn_up_simt_kernel<4><<<simt_grid(units_max, num_sms, 2), kThreads, up_smem<4>(bank.H), st>>>(bank, ws);
+    { cudaError_t le_ = launch_pdl(ffn_up_simt_kernel<4>, dim3(simt_grid(units_max, num_sms, 2)), dim3(kThreads), up_smem<4>(bank.H), st, bank, ws); if (le_ != cudaSuccess) return le_; }
   }
   (void)k;
   return cudaGetLastError();
@@ -315,9 +319,9 @@ cudaError_t launch_ffn_down_simt(const ExpertBank& bank, int T, int k, int n_sha
   if (T == 0) return cudaSuccess;
   const int units_max = (bank.E + n_shared) * (bank.H / 64);
   if (T == 1) {
-    ffn_down_simt_kernel<1><<<simt_grid(units_max, num_sms, 4), kThreads, down_smem<1>(bank.I), st>>>(bank, ws);
+    { cudaError_t le_ = launch_pdl(ffn_down_simt_kernel<1>, dim3(simt_grid(units_max, num_sms, 4)), dim3(kThreads), down_smem<1>(bank.I), st, bank, ws); if (le_ != cudaSuccess) return le_; }
   } else {
-    ffn_down_simt_kernel<4><<<simt_grid(units_max, num_sms, 2), kThreads, down_smem<4>(bank.I), st>>>(bank, ws);
+    { cudaError_t le_ = launch_pdl(ffn_down_simt_kernel<4>, dim3(simt_grid(units_max, num_sms, 2)), dim3(kThreads), down_smem<4>(bank.I), st, bank, ws); if (le_ != cudaSuccess) return le_; }
   }
   (void)k;
   return cudaGetLastError();

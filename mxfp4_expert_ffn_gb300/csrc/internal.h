@@ -75,6 +75,24 @@ struct moe_layer {
 
 namespace moe {
 
+// Launches a kernel as a programmatic dependent of the previous work in the
+// stream: it may start while that work drains and waits in pdl_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Expert weight pointers for expert id e (routed 0..E-1, shared E..E+ns-1).
 struct ExpertBank {
   const uint8_t *gc, *gs, *uc, *us, *dc, *ds;       // routed banks

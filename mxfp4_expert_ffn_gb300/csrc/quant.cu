@@ -39,6 +39,8 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, unsigned quad, int* e_out
 // One thread per 8 bf16 values; four consecutive threads form one 32-block.
 __global__ void quantize_act_kernel(const uint4* __restrict__ x, int n8, uint2* __restrict__ q,
                                     uint8_t* __restrict__ s) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const unsigned quad = 0xFu << (lane & ~3);
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += gridDim.x * blockDim.x) {
@@ -53,6 +55,8 @@ __global__ void quantize_act_kernel(const uint4* __restrict__ x, int n8, uint2* 
 __global__ void quantize_gather_kernel(const uint16_t* __restrict__ x, int P, int H,
                                        const int32_t* __restrict__ pos_tok, uint2* __restrict__ xg,
                                        uint8_t* __restrict__ xgs) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const unsigned quad = 0xFu << (lane & ~3);
   const int per_row = H / 8;
@@ -74,6 +78,8 @@ __global__ void quantize_gather_kernel(const uint16_t* __restrict__ x, int P, in
 // stable counting sort, identical on every run.
 __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restrict__ idx, int T,
                                                         int k, int E, int ns, int bn, Workspace ws) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int32_t sm[];
   const int NE = E + ns;
   int32_t* wcnt = sm;            // [32][E]  per-warp counts, then running bases
@@ -209,6 +215,8 @@ __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restric
 __global__ void combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_pos,
                                const float* __restrict__ w, int T, int H, int k, int ns,
                                const uint16_t* __restrict__ res, uint16_t* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.y;
   const int h = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (h >= H) return;
@@ -251,6 +259,8 @@ __global__ void combine_kernel(const float* __restrict__ o, const int32_t* __res
 // out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)); fixed-order block reduction.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* __restrict__ x, int H,
                                                       float eps, uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[256];
   const int t = blockIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
@@ -298,8 +308,8 @@ cudaError_t launch_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uin
   if (n8 == 0) return cudaSuccess;
   int blocks = (n8 + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  quantize_act_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), n8,
-                                               reinterpret_cast<uint2*>(q), s);
+  { cudaError_t le_ = launch_pdl(quantize_act_kernel, dim3(blocks), dim3(256), 0, st, reinterpret_cast<const uint4*>(x), n8,
+                                               reinterpret_cast<uint2*>(q), s); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -307,7 +317,7 @@ size_t segments_smem_bytes(int E) { return (size_t)(33 * E) * sizeof(int32_t); }
 
 cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared, int bn,
                             const Workspace& ws, cudaStream_t st) {
-  segments_kernel<<<1, 1024, segments_smem_bytes(E), st>>>(idx, T, k, E, n_shared, bn, ws);
+  { cudaError_t le_ = launch_pdl(segments_kernel, dim3(1), dim3(1024), segments_smem_bytes(E), st, idx, T, k, E, n_shared, bn, ws); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -317,7 +327,7 @@ cudaError_t launch_quantize_gather(const uint16_t* x, int P, int H, const int32_
   if (n8 == 0) return cudaSuccess;
   long long blocks = (n8 + 255) / 256;
   if (blocks > 8192) blocks = 8192;
-  quantize_gather_kernel<<<(int)blocks, 256, 0, st>>>(x, P, H, pos_tok, reinterpret_cast<uint2*>(xg), xgs);
+  { cudaError_t le_ = launch_pdl(quantize_gather_kernel, dim3((int)blocks), dim3(256), 0, st, x, P, H, pos_tok, reinterpret_cast<uint2*>(xg), xgs); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -330,14 +340,14 @@ cudaError_t launch_combine(const Workspace& ws, int T, int H, int k, int n_share
                            const uint16_t* residual, uint16_t* y, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   dim3 grid((H / 4 + 255) / 256, T);
-  combine_kernel<<<grid, 256, 0, st>>>(ws.o, ws.slot_pos, w, T, H, k, n_shared, residual, y);
+  { cudaError_t le_ = launch_pdl(combine_kernel, dim3(grid), dim3(256), 0, st, ws.o, ws.slot_pos, w, T, H, k, n_shared, residual, y); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out,
                            cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_kernel<<<T, 256, 0, st>>>(x, H, eps, out);
+  { cudaError_t le_ = launch_pdl(rmsnorm_kernel, dim3(T), dim3(256), 0, st, x, H, eps, out); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 

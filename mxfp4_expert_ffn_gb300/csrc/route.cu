@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     router_logits_kernel(const uint16_t* __restrict__ x, int T, int H, int E,
                          const float* __restrict__ W, const float* __restrict__ b,
                          float* __restrict__ logits) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRouterWarps + warp;
   if (e >= E) return;
@@ -101,6 +103,8 @@ __device__ __forceinline__ void select_topk(const float (&v)[16], int t, int E, 
 // of a warp arg-max over (value desc, index asc); NaN counts as -infinity.
 __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                             int32_t* __restrict__ idx, float* __restrict__ w) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
@@ -120,6 +124,8 @@ template <int TT>
 __global__ void __launch_bounds__(kRouterWarps * 32)
     router_partial_kernel(const uint16_t* __restrict__ x, int T, int H, int E, int kc,
                           const float* __restrict__ W, float* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRouterWarps + warp;
   if (e >= E) return;
@@ -157,6 +163,8 @@ __global__ void __launch_bounds__(256) topk_sum_kernel(const float* __restrict__
                                                        int k, float* __restrict__ logits_out,
                                                        int32_t* __restrict__ idx,
                                                        float* __restrict__ w) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float lg[512];
   const int t = blockIdx.x;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -195,19 +203,19 @@ cudaError_t launch_router_split(const uint16_t* x, int T, int H, int E, int k, c
   const int ks = router_ksplit(H);
   const int gx = (E + kRouterWarps - 1) / kRouterWarps;
   if (T <= 2)
-    router_partial_kernel<2><<<dim3(gx, (T + 1) / 2, ks), kRouterWarps * 32, 0, st>>>(x, T, H, E, H / ks, W, part);
+    { cudaError_t le_ = launch_pdl(router_partial_kernel<2>, dim3(dim3(gx, (T + 1) / 2, ks)), dim3(kRouterWarps * 32), 0, st, x, T, H, E, H / ks, W, part); if (le_ != cudaSuccess) return le_; }
   else
-    router_partial_kernel<8><<<dim3(gx, (T + 7) / 8, ks), kRouterWarps * 32, 0, st>>>(x, T, H, E, H / ks, W, part);
+    { cudaError_t le_ = launch_pdl(router_partial_kernel<8>, dim3(dim3(gx, (T + 7) / 8, ks)), dim3(kRouterWarps * 32), 0, st, x, T, H, E, H / ks, W, part); if (le_ != cudaSuccess) return le_; }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  topk_sum_kernel<<<T, 256, 0, st>>>(part, ks, b, T, E, k, logits_out, idx, w);
+  { cudaError_t le_ = launch_pdl(topk_sum_kernel, dim3(T), dim3(256), 0, st, part, ks, b, T, E, k, logits_out, idx, w); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk_sum(const float* part, int ksplit, const float* b, int T, int E, int k,
                             float* logits_out, int32_t* idx, float* w, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  topk_sum_kernel<<<T, 256, 0, st>>>(part, ksplit, b, T, E, k, logits_out, idx, w);
+  { cudaError_t le_ = launch_pdl(topk_sum_kernel, dim3(T), dim3(256), 0, st, part, ksplit, b, T, E, k, logits_out, idx, w); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -217,11 +225,11 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const f
   if (T == 0) return cudaSuccess;
   const int gx = (E + kRouterWarps - 1) / kRouterWarps;
   if (T <= 2) {
-    router_logits_kernel<2><<<dim3(gx, (T + 1) / 2), kRouterWarps * 32, 0, st>>>(x, T, H, E, W, b,
-                                                                                logits);
+    { cudaError_t le_ = launch_pdl(router_logits_kernel<2>, dim3(dim3(gx, (T + 1) / 2)), dim3(kRouterWarps * 32), 0, st, x, T, H, E, W, b,
+                                                                                logits); if (le_ != cudaSuccess) return le_; }
   } else {
-    router_logits_kernel<8><<<dim3(gx, (T + 7) / 8), kRouterWarps * 32, 0, st>>>(x, T, H, E, W, b,
-                                                                                logits);
+    { cudaError_t le_ = launch_pdl(router_logits_kernel<8>, dim3(dim3(gx, (T + 7) / 8)), dim3(kRouterWarps * 32), 0, st, x, T, H, E, W, b,
+                                                                                logits); if (le_ != cudaSuccess) return le_; }
   }
   return cudaGetLastError();
 }
@@ -229,7 +237,7 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const f
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, k, idx, w);
+  { cudaError_t le_ = launch_pdl(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, logits, T, E, k, idx, w); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 

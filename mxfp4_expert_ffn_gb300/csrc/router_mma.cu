@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(kRThreads, 1) router_mma_kernel(const __grid_c
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_wait();  // x may come from the previous kernel
+  pdl_trigger();
   auto give_up = [&]() {
     atomicOr(p.err, kErrTimeout);
     *(volatile int*)&abort_flag = 1;
@@ -271,7 +273,7 @@ cudaError_t launch_router_mma(const CUtensorMap& w3map, const uint16_t* x, int T
     if (e != cudaSuccess) return e;
     attr[dev] = true;
   }
-  router_mma_kernel<<<num_sms, kRThreads, kRSmem, st>>>(p);
+  { cudaError_t le_ = launch_pdl(router_mma_kernel, dim3(num_sms), dim3(kRThreads), kRSmem, st, p); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
