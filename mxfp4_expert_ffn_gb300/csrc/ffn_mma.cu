@@ -164,8 +164,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_slot;
-  // the prologue above overlaps the previous kernel; its outputs are read below
-  pdl_wait();
+  // Programmatic dependent launch: the tile table and the weights were ready
+  // before the previous kernel started, so they are read right away; the
+  // activations (and the outputs' readers) wait for it in pdl_wait() below.
   pdl_trigger();
   const int total = p.tile_prefix[*p.n_active] * mt_per_expert;
 
@@ -180,6 +181,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     if (lane == 0) {
       uint32_t g = 0;
       int last_parity[kMaxStages];
+      int deferred_pos[kMaxStages], deferred_s[kMaxStages], n_deferred = 0;
+      bool waited = false;
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
       for (int u = blockIdx.x; u < total && !aborted(); u += gridDim.x) {
@@ -190,6 +193,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         for (int s = 0; s < k_stages; ++s, ++g) {
           const int slot = g % NS;
           const uint32_t ph = (g / NS) & 1;
+          if (!waited && g >= (uint32_t)NS) {
+            // ring full: wait for the previous kernel, then load the deferred activations
+            pdl_wait();
+            waited = true;
+            for (int i = 0; i < n_deferred; ++i)
+              tma_load_3d(stage_base + i * stage_bytes + NA * C::kATile, &p.b, 0, deferred_pos[i],
+                          deferred_s[i] * CH, &full_bar[i]);
+          }
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); ok = false; break; }
           uint8_t* sa = stage_base + slot * stage_bytes;
           mbar_expect_tx(&full_bar[slot], tx_stage);
@@ -202,14 +213,25 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
               tma_load_3d(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
                           &full_bar[slot]);
           }
-          tma_load_3d(sa + NA * C::kATile, &p.b, 0, un.pos0, s * CH, &full_bar[slot]);
+          if (waited) {
+            tma_load_3d(sa + NA * C::kATile, &p.b, 0, un.pos0, s * CH, &full_bar[slot]);
+          } else {
+            deferred_pos[n_deferred] = un.pos0;  // slot == n_deferred while g < NS
+            deferred_s[n_deferred++] = s;
+          }
 #pragma unroll
           for (int i = 0; i < kMaxStages; ++i)
             if (i == slot) last_parity[i] = (int)ph;
         }
         if (!ok) break;
       }
-      // never leave with copies in flight: wait for the last load into each buffer
+      if (!waited) {
+        pdl_wait();
+        for (int i = 0; i < n_deferred; ++i)
+          tma_load_3d(stage_base + i * stage_bytes + NA * C::kATile, &p.b, 0, deferred_pos[i],
+                      deferred_s[i] * CH, &full_bar[i]);
+      }
+      // never leave with copies in flight: wait for the last load into each slot
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s)
         if (last_parity[s] >= 0) mbar_wait(&full_bar[s], (uint32_t)last_parity[s], kWaitLimit);
@@ -242,19 +264,21 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           }
           fence_after();
           const uint32_t sa = smem_u32(stage_base + slot * stage_bytes);
-          const uint32_t sb = sa + NA * C::kATile;
+          // descriptors differ only in the start-address field (bits 0..13, address / 16)
+          const uint64_t a_desc0 = sw128_desc(sa), b_desc0 = sw128_desc(sa + NA * C::kATile);
           const uint32_t sf = tmem + sf_col0 + slot * C::kSfCols;
 #pragma unroll
           for (int c = 0; c < CH; ++c)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
-              const uint64_t bdesc = sw128_desc(sb + c * BN * 128 + 32 * k);
+              const uint64_t bdesc = b_desc0 + (uint64_t)((c * BN * 128 + 32 * k) >> 4);
 #pragma unroll
               for (int m = 0; m < NA; ++m) {
                 const int acc = swap ? NA - 1 - m : m;  // gate -> accumulator 0, up -> 1
-                mma_mxf8f6f4(d_tmem + acc * BN, sw128_desc(sa + m * C::kATile + c * 16384 + 32 * k), bdesc,
-                             idesc, sf + (acc * CH + c) * 4, sf + (NA * CH + c) * 4, (s | c | k) ? 1u : 0u);
+                mma_mxf8f6f4(d_tmem + acc * BN, a_desc0 + (uint64_t)((m * C::kATile + c * 16384 + 32 * k) >> 4),
+                             bdesc, idesc, sf + (acc * CH + c) * 4, sf + (NA * CH + c) * 4,
+                             (s | c | k) ? 1u : 0u);
               }
             }
           mma_commit(&empty_bar[slot]);
@@ -269,6 +293,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // registers), so a global-load latency is paid per NB stages.
     constexpr int NB = 4, NW = NA * CH + NC * CH;  // words per stage
     const int q = warp & 3;
+    pdl_wait();  // the activation scales come from the previous kernel
     uint32_t g = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok && !aborted(); u += gridDim.x) {
@@ -338,6 +363,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant of this warp
+    pdl_wait();
     uint32_t it = 0;
     for (int u = blockIdx.x; u < total && !aborted(); u += gridDim.x, ++it) {
       const Unit un = decode_unit(p, u, mt_per_expert);
