@@ -44,7 +44,7 @@ def parse():
     p.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     p.add_argument("--path", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor cores")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--graph", type=int, default=0, help="1: launch each step as a captured CUDA graph")
+    p.add_argument("--graph", type=int, default=1, help="1: launch each step as a captured CUDA graph, 0: stream launches")
     return p.parse_args()
 
 
@@ -230,19 +230,17 @@ def run_ours(args):
     st = torch.cuda.current_stream()
 
     def step(i, y_out=None):
+        # one call per layer: moe_step = route + forward (for up to 64 tokens the
+        # router, top-k, x codes and segments are a single launch)
         x = xs[i]
         if nl == 1:
-            Ls[0].route(x, T, idx, wt)
-            Ls[0].forward(x, T, idx, wt, bufs[0] if y_out is None else y_out)
+            Ls[0].step(x, T, bufs[0] if y_out is None else y_out)
             return
-        cur = x
+        cur, xn = x, bufs[0]
         for layer in range(nl):
-            xn, nxt = bufs[layer % 2], bufs[2] if layer == nl - 1 else bufs[(layer + 1) % 2]
-            if layer == 0:
-                nxt = bufs[1]
-            m.moe_rmsnorm(cur, T, H, 1e-6, xn)
-            Ls[layer].route(xn, T, idx, wt)
-            Ls[layer].forward(xn, T, idx, wt, nxt, residual=cur)
+            nxt = bufs[1] if cur is not bufs[1] else bufs[2]
+            m.moe_rmsnorm(cur, T, H, 1e-6, xn)          # normalised input of the layer
+            Ls[layer].step(xn, T, nxt, residual=cur)   # x_{l+1} = x_l + layer(norm(x_l))
             cur = nxt
 
     run = step

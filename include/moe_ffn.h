@@ -127,6 +127,19 @@ moe_status moe_route(moe_layer* layer, const void* x, int32_t T, const float* lo
 moe_status moe_forward(moe_layer* layer, const void* x, int32_t T, const int32_t* topk_idx,
                        const float* topk_w, const void* residual, void* y, void* stream);
 
+/* One layer step on device buffers: moe_route followed by moe_forward, with
+ * the same results as those two calls (bit for bit: the logits are the same
+ * fixed-order fp32 sums).  For small batches the router, the top-k, the FP8
+ * codes of x and the expert segments run as one launch.  The cost of a
+ * decode step is the bytes of the experts it selects (FreeToken issue #444,
+ * janit's comment item 1: rate = bandwidth / routed bytes per token).
+ *  topk_idx, topk_w  int32/fp32 [T][k] or NULL: receive the routing;
+ *  logits_out        fp32 [T][E] or NULL: receives the logits.
+ * x, y and residual as for moe_forward (16-byte aligned, y may alias the
+ * residual but not x).  T = 0 is a no-op. */
+moe_status moe_step(moe_layer* layer, const void* x, int32_t T, const void* residual, void* y,
+                    int32_t* topk_idx, float* topk_w, float* logits_out, void* stream);
+
 /* moe_route followed by moe_forward, with x and y in HOST memory: copies x to
  * the device, runs the layer and copies y back, all on `stream`; returns
  * after y_host is written (the call synchronises the stream).  For full copy

@@ -19,7 +19,7 @@ MOE_OPT_PATH, MOE_OPT_TIMING = 1, 2
 PATH_AUTO, PATH_SIMT, PATH_MMA = 0, 1, 2
 
 # every symbol include/moe_ffn.h declares
-EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward",
+EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward", "moe_step",
            "moe_forward_host", "moe_quantize_act", "moe_segments", "moe_rmsnorm", "moe_sync",
            "moe_set_option", "moe_get_kernel_times", "moe_status_string", "moe_abi_version",
            "moe_route_static")
@@ -65,6 +65,7 @@ def lib():
         L.moe_layer_destroy.argtypes = [P]
         L.moe_route.argtypes = [P, P, I32, P, P, P, P, P]
         L.moe_forward.argtypes = [P, P, I32, P, P, P, P, P]
+        L.moe_step.argtypes = [P, P, I32, P, P, P, P, P, P]
         L.moe_forward_host.argtypes = [P, P, I32, P, P]
         L.moe_quantize_act.argtypes = [P, P, I32, P, P, P]
         L.moe_segments.argtypes = [P, P, I32, P, P, P]
@@ -141,6 +142,12 @@ def moe_forward(h, x, T, topk_idx, topk_w, residual, y, stream=None) -> None:
                              stream_handle(stream)), "moe_forward")
 
 
+def moe_step(h, x, T, residual, y, topk_idx=None, topk_w=None, logits_out=None,
+             stream=None) -> None:
+    _check(lib().moe_step(h, ptr(x), T, ptr(residual), ptr(y), ptr(topk_idx), ptr(topk_w),
+                          ptr(logits_out), stream_handle(stream)), "moe_step")
+
+
 def moe_forward_host(h, x_host, T, y_host, stream=None) -> None:
     _check(lib().moe_forward_host(h, ptr(x_host), T, ptr(y_host), stream_handle(stream)),
            "moe_forward_host")
@@ -210,6 +217,9 @@ class Layer:
 
     def forward(self, x, T, idx, w, y, residual=None, stream=None):
         moe_forward(self.handle, x, T, idx, w, residual, y, stream)
+
+    def step(self, x, T, y, residual=None, idx=None, w=None, logits_out=None, stream=None):
+        moe_step(self.handle, x, T, residual, y, idx, w, logits_out, stream)
 
     def forward_host(self, x_host, T, y_host, stream=None):
         moe_forward_host(self.handle, x_host, T, y_host, stream)

@@ -46,7 +46,7 @@ struct Carver {
 };
 
 // Lays out the workspace in one allocation (base = nullptr: sizing pass).
-size_t carve(const moe_config& c, char* base, Workspace& ws) {
+size_t carve(const moe_config& c, int num_sms, char* base, Workspace& ws) {
   const size_t T = (size_t)c.max_tokens, H = (size_t)c.hidden, I = (size_t)c.inter;
   const size_t k = (size_t)c.top_k, E = (size_t)c.n_experts, ns = (size_t)c.n_shared;
   const size_t NE = E + ns, S = T * k, P = S + ns * T;
@@ -76,6 +76,15 @@ size_t carve(const moe_config& c, char* base, Workspace& ws) {
   ws.w = cv.take<float>(T * k);
   ws.x = cv.take<uint16_t>(T * H);
   ws.y = cv.take<uint16_t>(T * H);
+  // split partition of the tensor-core GEMM (few units, e.g. decode): two
+  // partial slots per CTA and one counter per (unit, row quadrant), units < 4 * SMs
+  ws.part_bn = mma_tile_for_tokens(c.max_tokens) < 64 ? mma_tile_for_tokens(c.max_tokens) : 64;
+  ws.part = cv.take<float>((size_t)2 * num_sms * 2 * ws.part_bn * 128);
+  ws.split_cnt_n = 2 * 16 * num_sms;
+  ws.split_cnt = cv.take<int32_t>((size_t)ws.split_cnt_n);
+  ws.prep_cnt = cv.take<int32_t>(16);
+  ws.comb_cnt_n = kPrepMaxTokens * (int)(H / 128) * 4;
+  ws.comb_cnt = cv.take<int32_t>((size_t)ws.comb_cnt_n);
   ws.err = cv.take<int32_t>(1);
   return cv.off;
 }
@@ -216,20 +225,21 @@ moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int dev
     return cuda_fail(cudaErrorInvalidDevice);
   }
   Workspace sizing;
-  const size_t bytes = carve(*cfg, nullptr, sizing);
+  const size_t bytes = carve(*cfg, L->num_sms, nullptr, sizing);
   void* base = nullptr;
   if (cudaMalloc(&base, bytes) != cudaSuccess) {
     cudaGetLastError();
     delete L;
     return MOE_ERR_OOM;
   }
-  carve(*cfg, static_cast<char*>(base), L->ws);
+  carve(*cfg, L->num_sms, static_cast<char*>(base), L->ws);
   L->ws.base = base;
   L->ws.bytes = bytes;
   cudaError_t e = cudaMemset(base, 0, bytes);
   if (e == cudaSuccess) e = cudaMallocHost(&L->ws.err_host, sizeof(int32_t));
   if (e == cudaSuccess) e = prepare_segments_kernel(cfg->n_experts);
   if (e == cudaSuccess) e = prepare_ffn_simt(cfg->hidden, cfg->inter);
+  if (e == cudaSuccess) e = prepare_prep_kernel(cfg->n_experts, cfg->hidden);
   if (e == cudaSuccess) {
     L->maps = mma_maps_create(*cfg, *w, L->ws);  // NULL: tensor-core path unavailable
     cudaGetLastError();
@@ -368,14 +378,45 @@ moe_status route_impl(moe_layer* L, const void* x, int32_t T, const float* logit
   return cuda_fail(e);
 }
 
-// Path choice: the SIMT streaming kernels for a single token (every expert
-// sees at most one row), the tensor-core kernels otherwise; MOE_OPT_PATH
-// forces either.
+// The tensor-core path is faster at every token count measured (decode T = 1
+// included); SIMT is kept for MOE_OPT_PATH = 1 and for shapes without maps.
 bool use_mma(const moe_layer* L, int T) {
+  (void)T;
   if (!L->maps) return false;
-  if (L->path == 1) return false;
-  if (L->path == 2) return true;
-  return T > 1;
+  return L->path != 1;
+}
+
+// gate/up, down and combine on the tensor cores, once the segments and the
+// activation codes are in the workspace.
+moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool gather, const float* w,
+                    const void* residual, void* y, cudaStream_t st) {
+  const moe_config& c = L->cfg;
+  const ExpertBank bank = bank_of(L);
+  cudaError_t e;
+  {
+    TimedScope ts(L, st, "ffn_up_mma");
+    e = launch_ffn_mma(*L->maps, bank, 0, bn, gather, L->ws, L->num_sms, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (gather && c.n_shared > 0) {
+    // small batch: the combine runs inside the down GEMM (every token has a
+    // shared-expert position, so every y row has a last writer)
+    const CombineArgs cmb{T, c.top_k, c.n_shared, w, static_cast<const uint16_t*>(residual),
+                          static_cast<uint16_t*>(y)};
+    TimedScope ts(L, st, "ffn_down_mma");
+    return cuda_fail(launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, &cmb));
+  }
+  {
+    TimedScope ts(L, st, "ffn_down_mma");
+    e = launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    TimedScope ts(L, st, "combine");
+    e = launch_combine(L->ws, T, c.hidden, c.top_k, c.n_shared, w,
+                       static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(y), st);
+  }
+  return cuda_fail(e);
 }
 
 moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* idx,
@@ -385,6 +426,15 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
   const bool mma = use_mma(L, T);
   const int bn = mma ? mma_tile_for_tokens(T) : 0;
   cudaError_t e;
+  if (mma && T <= kPrepMaxTokens) {
+    {
+      TimedScope ts(L, st, "prep");
+      e = launch_prep(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts, c.top_k, c.n_shared,
+                      bn, nullptr, nullptr, nullptr, const_cast<int32_t*>(idx), nullptr, false, L->ws, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ffn_tail(L, T, bn, true, w, residual, y, st);
+  }
   {
     TimedScope ts(L, st, "segments");
     e = launch_segments(idx, T, c.top_k, c.n_experts, c.n_shared, bn, L->ws, st);
@@ -398,16 +448,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
                                  L->ws.xg, L->ws.xgs, st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
-    {
-      TimedScope ts(L, st, "ffn_up_mma");
-      e = launch_ffn_mma(*L->maps, bank, 0, bn, L->ws, L->num_sms, st);
-    }
-    if (e != cudaSuccess) return cuda_fail(e);
-    {
-      TimedScope ts(L, st, "ffn_down_mma");
-      e = launch_ffn_mma(*L->maps, bank, 1, bn, L->ws, L->num_sms, st);
-    }
-    if (e != cudaSuccess) return cuda_fail(e);
+    return ffn_tail(L, T, bn, false, w, residual, y, st);
   } else {
     {
       TimedScope ts(L, st, "quantize_act");
@@ -433,9 +474,46 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
   return cuda_fail(e);
 }
 
+// Route and forward in one pass.  For small batches on the tensor cores the
+// router, top-k, the x codes and the segments are a single launch.
+moe_status step_impl(moe_layer* L, const void* x, int32_t T, const void* residual, void* y,
+                     int32_t* idx, float* w, float* logits_out, cudaStream_t st) {
+  const moe_config& c = L->cfg;
+  if (!idx) idx = L->ws.idx;
+  if (!w) w = L->ws.w;
+  if (use_mma(L, T) && T <= kPrepMaxTokens) {
+    const int bn = mma_tile_for_tokens(T);
+    cudaError_t e;
+    {
+      TimedScope ts(L, st, "prep");
+      e = launch_prep(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts, c.top_k, c.n_shared,
+                      bn, L->w.router_w, L->w.router_b, logits_out, idx, w, true, L->ws, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ffn_tail(L, T, bn, true, w, residual, y, st);
+  }
+  moe_status s = route_impl(L, x, T, nullptr, logits_out, idx, w, st);
+  if (s != MOE_OK) return s;
+  return forward_impl(L, x, T, idx, w, residual, y, st);
+}
+
 }  // namespace
 
 extern "C" {
+
+moe_status moe_step(moe_layer* L, const void* x, int32_t T, const void* residual, void* y,
+                    int32_t* topk_idx, float* topk_w, float* logits_out, void* stream) {
+  moe_status s = check_tokens(L, T);
+  if (s != MOE_OK || T == 0) return s;
+  if (!x || !y || x == y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || (residual && !aligned(residual, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if (fault("launch")) return MOE_ERR_CUDA;
+  DeviceGuard g(L->device);
+  if (g.status != cudaSuccess) return cuda_fail(g.status);
+  return step_impl(L, x, T, residual, y, topk_idx, topk_w, logits_out,
+                   static_cast<cudaStream_t>(stream));
+}
 
 moe_status moe_route(moe_layer* L, const void* x, int32_t T, const float* logits_in,
                      float* logits_out, int32_t* topk_idx, float* topk_w, void* stream) {
@@ -475,8 +553,7 @@ moe_status moe_forward_host(moe_layer* L, const void* x_host, int32_t T, void* y
   const size_t bytes = (size_t)T * L->cfg.hidden * sizeof(uint16_t);
   cudaError_t e = cudaMemcpyAsync(L->ws.x, x_host, bytes, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e);
-  if ((s = route_impl(L, L->ws.x, T, nullptr, nullptr, L->ws.idx, L->ws.w, st)) != MOE_OK) return s;
-  if ((s = forward_impl(L, L->ws.x, T, L->ws.idx, L->ws.w, nullptr, L->ws.y, st)) != MOE_OK) return s;
+  if ((s = step_impl(L, L->ws.x, T, nullptr, L->ws.y, nullptr, nullptr, nullptr, st)) != MOE_OK) return s;
   e = cudaMemcpyAsync(y_host, L->ws.y, bytes, cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e);
   return moe_sync(L, stream);

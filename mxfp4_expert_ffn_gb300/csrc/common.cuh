@@ -84,6 +84,30 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc)
   return acc;
 }
 
+// Quantises 8 consecutive bf16 values; the four lanes of a quad (one 32-block)
+// agree on the block exponent.  Returns the 8 codes; *e gets the exponent.
+__device__ __forceinline__ uint2 quant8(const uint4 v, unsigned quad, int* e_out) {
+  float f[8];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 2));
+  const int e = fp8_block_exponent(amax);
+  uint32_t c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    c[j] = e4m3x2(scale_pow2_neg(f[2 * j], e), scale_pow2_neg(f[2 * j + 1], e));
+  *e_out = e;
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
 // Programmatic dependent launch: wait until the preceding kernel in the
 // stream has finished and flushed its writes (a no-op when the kernel was not
 // launched as a dependent), then let the next kernel start its prologue.

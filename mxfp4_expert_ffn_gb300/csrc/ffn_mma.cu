@@ -53,6 +53,19 @@ struct MmaParams {
   uint8_t* hq;
   uint8_t* hs;
   float* o;
+  float* part;               // split partition: fp32 partial tiles, 2 slots per CTA
+  int32_t* cnt;              // split partition: pieces finished per (unit, row quadrant)
+  int split_ok;              // part/cnt are large enough for this launch
+  int gather;                // up mode, BN 16: activation rows gathered by token from xq
+  int fuse_combine;          // down mode, BN <= 64: the last writer of a token's rows combines them
+  int T, k, ns;              // fuse_combine: tokens, top-k, shared experts
+  const int32_t* slot_pos;   // fuse_combine: position of slot t*k + j (-1: invalid id)
+  const float* w;            // fuse_combine: combine weights [T][k]
+  const uint16_t* res;       // fuse_combine: bf16 residual [T][H] or null
+  uint16_t* y;               // fuse_combine: bf16 output [T][H]
+  int32_t* comb_cnt;         // fuse_combine: writers finished per (token, 128-row tile, quadrant)
+  const uint8_t* xq;         // gather: E4M3 codes of x by token, [T][K]
+  const int32_t* pos_tok;    // gather: token of each position
   int32_t* err;
 };
 
@@ -107,6 +120,73 @@ __device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_pe
   return Unit{t.x, t.y, t.z, (u - v * mt_per_expert) * 128};
 }
 
+// Work partition.  Plain: whole units strided over the CTAs.  Split: when
+// there are few units (a decode step), the units' K stages form one sequence
+// that is cut into gridDim.x nearly equal contiguous ranges, so that every SM
+// streams the same number of weight bytes.  A unit cut between CTAs is
+// finished by the last of them to arrive, which adds the fp32 partial tiles in
+// piece order (fixed, so results do not depend on arrival order).
+struct Piece {
+  int u, s0, s1;  // unit, stage range [s0, s1)
+};
+
+constexpr int kMaxPieces = 16;  // pieces per unit in the split partition
+constexpr int kMaxTopK = 8, kMaxShared = 4;  // layer limits (moe_config)
+
+// All arithmetic in 32 bits: split mode needs total < 4 * gridDim.x, so the
+// stage iterations stay below 2^20.
+struct Sched {
+  int ti, g, end;  // split: stage iterations in all, cursor, end of this CTA's range
+  int total, ks, u;
+  bool split;
+  __device__ Sched(int total_, int ks_, int split_ok) : total(total_), ks(ks_) {
+    const int G = gridDim.x;
+    split = false;
+    if (split_ok && total < 4 * G) {
+      ti = total * ks;
+      const int split_max = (ti + G - 1) / G;
+      const int plain_max = ((total + G - 1) / G) * ks;
+      // worth it when the busiest CTA gets at least 5 % fewer stages, and
+      // no unit is cut into more than kMaxPieces pieces
+      split = ti >= G && split_max * 20 < plain_max * 19 && ks <= (kMaxPieces - 2) * (ti / G);
+    }
+    g = split ? begin(blockIdx.x) : 0;
+    end = split ? begin(blockIdx.x + 1) : 0;
+    u = blockIdx.x;
+  }
+  __device__ int begin(int c) const { return (int)(((unsigned)c * (unsigned)ti) / gridDim.x); }
+  // the CTA whose range holds stage iteration it
+  __device__ int owner(int it) const { return (int)(((unsigned)(it + 1) * gridDim.x + ti - 1) / ti) - 1; }
+  __device__ Piece next() {
+    Piece pc{-1, 0, 0};
+    if (!split) {
+      if (u < total) pc = Piece{u, 0, ks};
+      u += gridDim.x;
+      return pc;
+    }
+    if (g >= end) return pc;
+    pc.u = g / ks;
+    pc.s0 = g - pc.u * ks;
+    pc.s1 = min(ks, pc.s0 + (end - g));
+    g += pc.s1 - pc.s0;
+    return pc;
+  }
+  // Unit uu is computed by CTAs first .. first + n - 1 (piece j by CTA first + j).
+  __device__ void pieces(int uu, int& first, int& n) const {
+    if (!split) {
+      first = blockIdx.x;
+      n = 1;
+      return;
+    }
+    first = owner(uu * ks);
+    n = owner((uu + 1) * ks - 1) - first + 1;
+  }
+  // Partial slot of piece j: 2c for the first piece of CTA c's range, 2c + 1 for its last.
+  __device__ int slot(int uu, int first, int j) const {
+    return (j == 0 && begin(first) != uu * ks) ? 2 * first + 1 : 2 * (first + j);
+  }
+};
+
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
                                             int32_t c2, int32_t c3, uint64_t* bar) {
   asm volatile(
@@ -143,7 +223,12 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   const int NS = p.n_stages;
   uint8_t* stage_base = smem;
   const int stage_bytes = NA * C::kATile + C::kBTile;
-  const uint32_t tx_stage = NA * 128 * 64 * CH + BN * 128 * CH;
+  // Gather mode (gate/up at 16-token tiles, i.e. decode): the scale-factor
+  // warps copy each position's activation row from the per-token codes into
+  // the stage (swizzled like a TMA tile), so no slot-ordered copy of x exists.
+  constexpr bool kGatherCapable = MODE == kModeUp && BN == 16;
+  const bool gather = kGatherCapable && p.gather;
+  const uint32_t tx_stage = NA * 128 * 64 * CH + (gather ? 0 : BN * 128 * CH);
   const uint32_t sf_col0 = C::kNAcc * C::kAccCols;
 
   if (threadIdx.x == 0) {
@@ -169,6 +254,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   // activations (and the outputs' readers) wait for it in pdl_wait() below.
   pdl_trigger();
   const int total = p.tile_prefix[*p.n_active] * mt_per_expert;
+  const Sched sc0(total, k_stages, BN <= 64 && p.split_ok);
 
   auto give_up = [&]() {
     atomicOr(p.err, kErrTimeout);
@@ -182,15 +268,17 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       uint32_t g = 0;
       int last_parity[kMaxStages];
       int deferred_pos[kMaxStages], deferred_s[kMaxStages], n_deferred = 0;
-      bool waited = false;
+      bool waited = gather;  // gather mode: the TMA warp loads weights only
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
-      for (int u = blockIdx.x; u < total && !aborted(); u += gridDim.x) {
-        const Unit un = decode_unit(p, u, mt_per_expert);
+      Sched sc = sc0;
+      for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next()) {
+        const Unit un = decode_unit(p, pc.u, mt_per_expert);
         const bool sh = un.e >= p.E;
         const int erow = (sh ? un.e - p.E : un.e) * p.rows + un.row0;
         bool ok = true;
-        for (int s = 0; s < k_stages; ++s, ++g) {
+        const int s_end = pc.s1;
+        for (int s = pc.s0; s < s_end; ++s, ++g) {
           const int slot = g % NS;
           const uint32_t ph = (g / NS) & 1;
           if (!waited && g >= (uint32_t)NS) {
@@ -213,7 +301,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
               tma_load_3d(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
                           &full_bar[slot]);
           }
-          if (waited) {
+          if (gather) {
+            // activations come from the scale-factor warps
+          } else if (waited) {
             tma_load_3d(sa + NA * C::kATile, &p.b, 0, un.pos0, s * CH, &full_bar[slot]);
           } else {
             deferred_pos[n_deferred] = un.pos0;  // slot == n_deferred while g < NS
@@ -241,7 +331,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     if (lane == 0) {
       uint32_t g = 0, it = 0;
       const uint32_t idesc_base = idesc_e2m1_e4m3(128, BN, 0);
-      for (int u = blockIdx.x; u < total && !aborted(); u += gridDim.x, ++it) {
+      Sched sc = sc0;
+      for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
         const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
         const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
         if (!mbar_wait(&acce_bar[buf], ph_acc ^ 1, kWaitLimit)) { give_up(); break; }
@@ -249,12 +340,13 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         const uint32_t d_tmem = tmem + buf * C::kAccCols;
         int swap = 0;
         if (NA == 2) {
-          const int e = decode_unit(p, u, mt_per_expert).e;
+          const int e = decode_unit(p, pc.u, mt_per_expert).e;
           const int sh = e >= p.E;
           swap = p.merged[sh] && p.swap_gu[sh];
         }
         bool ok = true;
-        for (int s = 0; s < k_stages; ++s, ++g) {
+        const int s_beg = pc.s0, s_end = pc.s1;
+        for (int s = s_beg; s < s_end; ++s, ++g) {
           const int slot = g % NS;
           const uint32_t ph = (g / NS) & 1;
           if (!mbar_wait(&full_bar[slot], ph, kWaitLimit) || !mbar_wait(&sf_bar[slot], ph, kWaitLimit)) {
@@ -278,7 +370,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
                 const int acc = swap ? NA - 1 - m : m;  // gate -> accumulator 0, up -> 1
                 mma_mxf8f6f4(d_tmem + acc * BN, a_desc0 + (uint64_t)((m * C::kATile + c * 16384 + 32 * k) >> 4),
                              bdesc, idesc, sf + (acc * CH + c) * 4, sf + (NA * CH + c) * 4,
-                             (s | c | k) ? 1u : 0u);
+                             (s != s_beg || c || k) ? 1u : 0u);
               }
             }
           mma_commit(&empty_bar[slot]);
@@ -292,12 +384,15 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // The scale words of NB stages are fetched at once (double-buffered in
     // registers), so a global-load latency is paid per NB stages.
     constexpr int NB = 4, NW = NA * CH + NC * CH;  // words per stage
+    constexpr int BCH = kGatherCapable ? CH : 1;   // gathered 16-byte granules per stage
     const int q = warp & 3;
     pdl_wait();  // the activation scales come from the previous kernel
     uint32_t g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok && !aborted(); u += gridDim.x) {
-      const Unit un = decode_unit(p, u, mt_per_expert);
+    Sched sc = sc0;
+    for (Piece pc = sc.next(); ok && pc.u >= 0 && !aborted(); pc = sc.next()) {
+      const Unit un = decode_unit(p, pc.u, mt_per_expert);
+      const int s_end = pc.s1;
       const bool sh = un.e >= p.E;
       const size_t erow = (size_t)(sh ? un.e - p.E : un.e) * p.rows + un.row0 + 32 * q + lane;
       const uint8_t* sa_row[NA];
@@ -307,12 +402,33 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
 #pragma unroll
       for (int cb = 0; cb < NC; ++cb) {
         const int n = lane + 32 * cb;
-        sb_row[cb] = n < un.m_tile ? p.sb + (size_t)(un.pos0 + n) * (p.K / 32) : nullptr;
+        sb_row[cb] = nullptr;
+        if (n < un.m_tile) {
+          const size_t row = gather ? (size_t)p.pos_tok[un.pos0 + n] : (size_t)(un.pos0 + n);
+          sb_row[cb] = p.sb + row * (p.K / 32);
+        }
       }
+      // gather: this thread copies 16-byte granule bg of activation row br of
+      // every chunk (128 threads x 2 chunks = the 16 x 256-byte B stage)
+      const int br = (32 * q + lane) >> 3, bg = lane & 7;
+      const uint8_t* xrow = nullptr;
+      if (gather && br < un.m_tile) xrow = p.xq + (size_t)p.pos_tok[un.pos0 + br] * p.K + bg * 16;
+      const int b_off = NA * C::kATile + br * 128 + ((bg ^ (br & 7)) << 4);  // 128-byte swizzle
+      auto load_b = [&](uint4 (&bw)[NB][BCH], int s0) {
+        if constexpr (kGatherCapable) {
+#pragma unroll
+          for (int i = 0; i < NB; ++i)
+#pragma unroll
+            for (int c = 0; c < BCH; ++c)
+              bw[i][c] = (xrow && s0 + i < s_end)
+                             ? __ldg(reinterpret_cast<const uint4*>(xrow + ((s0 + i) * CH + c) * 128))
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+      };
       auto load = [&](uint32_t (&w)[NB][NW], int s0) {
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
-          if (s0 + i < k_stages) {
+          if (s0 + i < s_end) {
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
               const int kb = 4 * ((s0 + i) * CH + c);  // first k-block of the chunk
@@ -326,14 +442,22 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           }
         }
       };
-      auto store = [&](const uint32_t (&w)[NB][NW], int s0) -> bool {
+      auto store = [&](const uint32_t (&w)[NB][NW], const uint4 (&bw)[NB][BCH], int s0) -> bool {
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
-          if (s0 + i >= k_stages) break;
+          if (s0 + i >= s_end) break;
           const int slot = g % NS;
           const uint32_t ph = (g / NS) & 1;
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); return false; }
           fence_after();
+          if constexpr (kGatherCapable) {
+            if (gather) {
+              uint8_t* dst = stage_base + slot * stage_bytes + b_off;
+#pragma unroll
+              for (int c = 0; c < BCH; ++c) *reinterpret_cast<uint4*>(dst + c * BN * 128) = bw[i][c];
+              fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
+            }
+          }
           const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + sf_col0 + slot * C::kSfCols;
 #pragma unroll
           for (int c = 0; c < CH; ++c) {
@@ -351,52 +475,190 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         return true;
       };
       uint32_t w0[NB][NW], w1[NB][NW];
-      load(w0, 0);
-      for (int s0 = 0; s0 < k_stages; s0 += 2 * NB) {
-        if (s0 + NB < k_stages) load(w1, s0 + NB);
-        if (!(ok = store(w0, s0))) break;
-        if (s0 + NB >= k_stages) break;
-        if (s0 + 2 * NB < k_stages) load(w0, s0 + 2 * NB);
-        if (!(ok = store(w1, s0 + NB))) break;
+      uint4 b0[NB][BCH], b1[NB][BCH];
+      load(w0, pc.s0);
+      load_b(b0, pc.s0);
+      for (int s0 = pc.s0; s0 < s_end; s0 += 2 * NB) {
+        if (s0 + NB < s_end) {
+          load(w1, s0 + NB);
+          load_b(b1, s0 + NB);
+        }
+        if (!(ok = store(w0, b0, s0))) break;
+        if (s0 + NB >= s_end) break;
+        if (s0 + 2 * NB < s_end) {
+          load(w0, s0 + 2 * NB);
+          load_b(b0, s0 + 2 * NB);
+        }
+        if (!(ok = store(w1, b1, s0 + NB))) break;
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int q = warp & 3;        // TMEM lane quadrant of this warp
+    const int rl = 32 * q + lane;  // row within the 128-row tile
     pdl_wait();
+    // One output column (a token position) of the tile: all 32 lanes of the
+    // warp take part (the h block scale is a max over the warp's 32 rows).
+    auto emit = [&](const Unit& un, int col, float a, float b) {
+      const size_t pos = (size_t)(un.pos0 + col);
+      const int row = un.row0 + rl;  // weight row (I row for up, H row for down)
+      if (MODE == kModeDown) {
+        p.o[pos * p.out_cols + row] = a;
+      } else {
+        const float h = a / (1.0f + expf(-a)) * b;
+        const int ex = fp8_block_exponent(warp_max(fabsf(h)));
+        p.hq[pos * p.out_cols + row] = (uint8_t)(e4m3x2(scale_pow2_neg(h, ex), 0.f) & 0xFFu);
+        if (lane == 0) p.hs[pos * (p.out_cols / 32) + (un.row0 + 32 * q) / 32] = (uint8_t)(ex + 127);
+      }
+    };
+    // Down mode with the combine fused (small batches): after a warp has
+    // written the o rows of its unit, each of the unit's positions counts one
+    // arrival for its token; the warp that brings a token's count to the
+    // number of its positions (valid routed slots + shared experts) adds that
+    // token's o rows for these 32 output rows in the fixed order of the
+    // combine (shared experts, then slots j = 0..k-1) and writes y.
+    auto combine_tail = [&](const Unit& un) {
+      if constexpr (MODE == kModeDown && BN <= 64) {
+        if (!p.fuse_combine) return;
+        __threadfence();
+        __syncwarp();
+        const int n_rt = p.out_cols / 128, rt = un.row0 / 128;
+        int done = -1;
+        if (lane < un.m_tile) {
+          const int t = p.pos_tok[un.pos0 + lane];
+          int sp[kMaxTopK];
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j) sp[j] = j < p.k ? p.slot_pos[t * p.k + j] : -1;
+          int need = p.ns;
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j) need += sp[j] >= 0;
+          if (atomicAdd(&p.comb_cnt[(t * n_rt + rt) * 4 + q], 1) == need - 1) done = t;
+        }
+        unsigned todo = __ballot_sync(0xFFFFFFFFu, done >= 0);
+        if (todo) __threadfence();
+        const int row = un.row0 + rl;
+        const size_t S = (size_t)p.T * p.k, H = (size_t)p.out_cols;
+        while (todo) {
+          const int t = __shfl_sync(0xFFFFFFFFu, done, __ffs(todo) - 1);
+          todo &= todo - 1;
+          // lane j < k holds slot j's position and weight; then every o load is in flight at once
+          const int my_pp = lane < p.k ? p.slot_pos[t * p.k + lane] : -1;
+          const float my_w = lane < p.k ? p.w[t * p.k + lane] : 0.f;
+          float osh[kMaxShared], ov[kMaxTopK];
+#pragma unroll
+          for (int j = 0; j < kMaxShared; ++j)
+            osh[j] = j < p.ns ? __ldcg(p.o + (S + (size_t)j * p.T + t) * H + row) : 0.f;
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j) {
+            const int pp = __shfl_sync(0xFFFFFFFFu, my_pp, j);
+            ov[j] = pp >= 0 ? __ldcg(p.o + (size_t)pp * H + row) : 0.f;
+          }
+          // the combine's fixed order: shared experts, then slots j = 0..k-1
+          float acc = 0.f;
+#pragma unroll
+          for (int j = 0; j < kMaxShared; ++j)
+            if (j < p.ns) acc += osh[j];
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j) {
+            const float wj = __shfl_sync(0xFFFFFFFFu, my_w, j);
+            if (__shfl_sync(0xFFFFFFFFu, my_pp, j) >= 0) acc = fmaf(wj, ov[j], acc);
+          }
+          uint16_t yb = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+          if (p.res)
+            yb = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits_to_float(p.res[(size_t)t * H + row]) +
+                                                          bf16_bits_to_float(yb)));
+          p.y[(size_t)t * H + row] = yb;
+        }
+      }
+    };
+    constexpr int kSlot = NA * BN * 128;  // floats per partial slot: [matrix][column][row]
     uint32_t it = 0;
-    for (int u = blockIdx.x; u < total && !aborted(); u += gridDim.x, ++it) {
-      const Unit un = decode_unit(p, u, mt_per_expert);
+    Sched sc = sc0;
+    for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
+      const Unit un = decode_unit(p, pc.u, mt_per_expert);
       const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
       const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
       if (!mbar_wait(&accf_bar[buf], ph_acc, kWaitLimit)) { give_up(); break; }
       fence_after();
       const uint32_t t_base = tmem + ((uint32_t)(32 * q) << 16) + buf * C::kAccCols;
-      const int row = un.row0 + 32 * q + lane;  // weight row (I row for up, H row for down)
+      int first, n;
+      sc.pieces(pc.u, first, n);
+      if (n == 1) {
+        // the whole unit: straight from TMEM to the outputs
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 16) {
-        uint32_t v[16], vu[16];
-        tmem_ld16(t_base + c, v);
-        if (MODE == kModeUp) tmem_ld16(t_base + BN + c, vu);
-        tmem_ld_wait();
-        if (c + 16 >= BN) {
-          fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acce_bar[buf]);
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (c + j >= un.m_tile) break;  // warp-uniform
-          const size_t pos = (size_t)(un.pos0 + c + j);
-          if (MODE == kModeDown) {
-            p.o[pos * p.out_cols + row] = __uint_as_float(v[j]);
-          } else {
-            const float gg = __uint_as_float(v[j]);
-            const float h = gg / (1.0f + expf(-gg)) * __uint_as_float(vu[j]);
-            const int ex = fp8_block_exponent(warp_max(fabsf(h)));
-            p.hq[pos * p.out_cols + row] = (uint8_t)(e4m3x2(scale_pow2_neg(h, ex), 0.f) & 0xFFu);
-            if (lane == 0) p.hs[pos * (p.out_cols / 32) + (un.row0 + 32 * q) / 32] = (uint8_t)(ex + 127);
+        for (int c = 0; c < BN; c += 16) {
+          uint32_t v[16], vu[16];
+          tmem_ld16(t_base + c, v);
+          if (MODE == kModeUp) tmem_ld16(t_base + BN + c, vu);
+          tmem_ld_wait();
+          if (c + 16 >= BN) {
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce_bar[buf]);
           }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c + j >= un.m_tile) break;  // warp-uniform
+            emit(un, c + j, __uint_as_float(v[j]), MODE == kModeUp ? __uint_as_float(vu[j]) : 0.f);
+          }
+        }
+        combine_tail(un);
+        continue;
+      }
+      if constexpr (BN <= 64) {
+        // A piece of a unit cut between CTAs: publish the fp32 partial tile;
+        // the last piece to arrive adds all of them in piece order.  Each warp
+        // owns its 32 rows, so the hand-off is per warp (one counter per unit
+        // and quadrant) and no warp ever waits for another.
+        float* mine = p.part + (size_t)sc.slot(pc.u, first, blockIdx.x - first) * kSlot;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          uint32_t v[16], vu[16];
+          tmem_ld16(t_base + c, v);
+          if (MODE == kModeUp) tmem_ld16(t_base + BN + c, vu);
+          tmem_ld_wait();
+          if (c + 16 >= BN) {
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce_bar[buf]);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c + j >= un.m_tile) break;  // warp-uniform
+            mine[(c + j) * 128 + rl] = __uint_as_float(v[j]);
+            if (MODE == kModeUp) mine[(BN + c + j) * 128 + rl] = __uint_as_float(vu[j]);
+          }
+        }
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&p.cnt[pc.u * 4 + q], 1) == n - 1;
+        if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+          __threadfence();
+          const float* src[kMaxPieces];
+#pragma unroll
+          for (int j = 0; j < kMaxPieces; ++j)
+            src[j] = p.part + (size_t)sc.slot(pc.u, first, j < n ? j : 0) * kSlot + rl;
+#pragma unroll 1
+          for (int col = 0; col < un.m_tile; ++col) {
+            float pa[kMaxPieces], pb[kMaxPieces];
+#pragma unroll
+            for (int j = 0; j < kMaxPieces; ++j) {  // all loads in flight, then the fixed-order sum
+              pa[j] = j < n ? __ldcg(src[j] + col * 128) : 0.f;
+              pb[j] = (MODE == kModeUp && j < n) ? __ldcg(src[j] + (BN + col) * 128) : 0.f;
+            }
+            float a = 0.f, b = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxPieces; ++j) {
+              if (j < n) {
+                a += pa[j];
+                b += pb[j];
+              }
+            }
+            emit(un, col, a, b);
+          }
+          if (lane == 0) p.cnt[pc.u * 4 + q] = 0;
+          combine_tail(un);
         }
       }
     }
@@ -546,8 +808,8 @@ MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Worksp
 
 void mma_maps_destroy(MmaMaps* m) { delete m; }
 
-cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn,
-                           const Workspace& ws, int num_sms, cudaStream_t st) {
+cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn, bool gather,
+                           const Workspace& ws, int num_sms, cudaStream_t st, const CombineArgs* cmb) {
   MmaParams p;
   memset(&p, 0, sizeof(p));
   const int bi = bn_index(bn);
@@ -567,6 +829,12 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
     p.sa_shared[0] = bk.sgs;
     p.sa_shared[1] = bk.sus;
     p.sb = ws.xgs;
+    if (gather && bn == 16) {  // activations by token: codes xq, scales xs
+      p.gather = 1;
+      p.xq = ws.xq;
+      p.pos_tok = ws.pos_tok;
+      p.sb = ws.xs;
+    }
     p.K = bk.H;
     p.rows = bk.I;
     p.out_cols = bk.I;
@@ -590,7 +858,22 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
   p.hq = ws.hq;
   p.hs = ws.hs;
   p.o = ws.o;
+  p.part = ws.part;
+  p.cnt = ws.split_cnt + (mode == kModeUp ? 0 : ws.split_cnt_n / 2);
+  p.split_ok = bn <= ws.part_bn && ws.split_cnt_n >= 2 * 16 * num_sms;
   p.err = ws.err;
+  if (mode == kModeDown && cmb && bn <= 64) {
+    p.fuse_combine = 1;
+    p.T = cmb->T;
+    p.k = cmb->k;
+    p.ns = cmb->ns;
+    p.slot_pos = ws.slot_pos;
+    p.pos_tok = ws.pos_tok;
+    p.w = cmb->w;
+    p.res = cmb->residual;
+    p.y = cmb->y;
+    p.comb_cnt = ws.comb_cnt;
+  }
   if (mode == kModeUp)
     return ch == 2 ? launch_bn<kModeUp, 2>(p, bn, num_sms, st) : launch_bn<kModeUp, 1>(p, bn, num_sms, st);
   if (ch == 3) return launch_bn<kModeDown, 3>(p, bn, num_sms, st);

@@ -39,6 +39,13 @@ struct Workspace {
   float* w = nullptr;         // [T][k]
   uint16_t* x = nullptr;      // [T][H]     bf16 staging (host entry point)
   uint16_t* y = nullptr;      // [T][H]
+  float* part = nullptr;      // [2*SMs][2][part_bn][128] split-partition partial tiles
+  int32_t* split_cnt = nullptr; // [2][16*SMs] split-partition counters (up, down)
+  int split_cnt_n = 0;        // entries of split_cnt (zeroed by the segments kernel)
+  int part_bn = 0;            // token-tile width the partial slots are sized for
+  int32_t* prep_cnt = nullptr;// [16]       small-batch preparation counters (zero between launches)
+  int32_t* comb_cnt = nullptr;// [64][H/128][4] fused-combine counters (zeroed by the segments)
+  int comb_cnt_n = 0;
   int32_t* err = nullptr;     // [1]        device error word
   int32_t* err_host = nullptr;// pinned copy of err
   void* base = nullptr;       // single allocation holding all of the above
@@ -133,8 +140,26 @@ cudaError_t launch_combine(const Workspace& ws, int T, int H, int k, int n_share
 MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Workspace& ws);
 void mma_maps_destroy(MmaMaps* m);
 int mma_tile_for_tokens(int T);
-cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn,
-                           const Workspace& ws, int num_sms, cudaStream_t st);
+// The combine fused into the down GEMM (small batches).
+struct CombineArgs {
+  int T, k, ns;
+  const float* w;           // [T][k]
+  const uint16_t* residual; // [T][H] or null
+  uint16_t* y;              // [T][H]
+};
+// gather (gate/up at bn 16 only): activation rows are read by token from xq/xs
+// through pos_tok instead of from the slot-ordered copy xg/xgs.  cmb (down,
+// bn <= 64): the combine runs inside the down GEMM (needs T <= kPrepMaxTokens).
+cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn, bool gather,
+                           const Workspace& ws, int num_sms, cudaStream_t st,
+                           const CombineArgs* cmb = nullptr);
+// Small batches (T <= kPrepMaxTokens): router + top-k (route) or the given
+// routing, FP8 codes of x by token (xq/xs) and the segments, in one launch.
+constexpr int kPrepMaxTokens = 64;
+cudaError_t prepare_prep_kernel(int E, int H);
+cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, int bn,
+                        const float* W, const float* b, float* logits_out, int32_t* idx, float* w,
+                        bool route, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out,
                            cudaStream_t st);
 

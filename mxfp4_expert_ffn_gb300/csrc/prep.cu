@@ -1,0 +1,193 @@
+// One launch that prepares a small batch (T <= 64 tokens) for the tensor-core
+// expert GEMM: router logits and top-k (or the caller's routing), the FP8
+// codes of x by token and the expert segments.
+//
+// Router: l = W_r x + b in fp32 with ties to the lower expert index and a
+// softmax over the selected logits (the gate as a discrete top-6 switch:
+// ai.rs, "What remains is the reference rounding itself"; llama.cpp
+// discussion #28766, "Correctness").  Activations: the checkpoint's dynamic
+// per-32 FP8 scheme with UE8M0 scales (FreeToken issue #444, "Is the
+// quantization already supported").
+//
+// Phases, with no CTA ever waiting for another:
+//   1. every CTA: router partial sums of (32 experts, 8 tokens, one K chunk)
+//      and a share of the x quantisation;
+//   2. the last CTA of each 8-token block to finish adds the K chunks of its
+//      tokens' logits in a fixed order, selects top-k and writes the weights;
+//   3. the last token block to finish builds the expert segments.
+// "Last" is decided by an atomic counter after a device-scope fence; the
+// finisher resets the counter, so the next launch starts from zero.  The sums
+// are the same fixed-order sums as the split-K router kernels, so the logits
+// are bit-identical to theirs.
+#include "common.cuh"
+#include "internal.h"
+#include "segments.cuh"
+#include "router.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kPrepWarps = 32;  // experts per CTA (one warp each)
+constexpr int kPrepTT = 8;      // tokens per block
+
+struct PrepParams {
+  const uint16_t* x;
+  int T, H, E, k, ns, bn;
+  int route;             // 1: compute logits and top-k; 0: idx and w are given
+  const float* W;        // [E][H] router weights (route)
+  const float* b;        // [E] bias or null
+  int ks;                // K chunks of the router
+  float* part;           // [ks][T][E] partial sums
+  float* logits_out;     // [T][E] or null
+  int32_t* idx;          // [T][k] written (route) or read
+  float* w;              // [T][k] written (route)
+  int32_t* counters;     // [token blocks + 1], zero between launches
+  Workspace ws;
+};
+
+__global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ PrepParams p) {
+  pdl_wait();  // x may come from the previous kernel
+  extern __shared__ int32_t sm[];
+  __shared__ int last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- 1a. router partial sums: warp = expert, CTA = (expert group, token block, K chunk);
+  // the CTA's x chunk (8 tokens x H/ks) is staged in shared memory once
+  if (p.route) {
+    const int e = blockIdx.x * kPrepWarps + warp;
+    const int t0 = blockIdx.y * kPrepTT, nt = min(kPrepTT, p.T - t0);
+    const int kc = p.H / p.ks, k0 = blockIdx.z * kc;
+    uint32_t* xsm = reinterpret_cast<uint32_t*>(sm);  // [nt][kc / 2] bf16 pairs
+    for (int i = threadIdx.x; i < nt * (kc / 8); i += blockDim.x) {
+      const int t = i / (kc / 8), c = i - t * (kc / 8);
+      reinterpret_cast<uint4*>(xsm)[i] = *reinterpret_cast<const uint4*>(p.x + (size_t)(t0 + t) * p.H + k0 + 8 * c);
+    }
+    __syncthreads();
+    if (e < p.E) {
+      float acc[kPrepTT];
+#pragma unroll
+      for (int i = 0; i < kPrepTT; ++i) acc[i] = 0.f;
+      router_dot<kPrepTT>(p.W + (size_t)e * p.H + k0, kc, nt, lane,
+                          [&](int i, int h) { return xsm[i * (kc / 2) + h / 2]; }, acc);
+#pragma unroll
+      for (int i = 0; i < kPrepTT; ++i) {
+        const float s = warp_sum(acc[i]);
+        if (lane == 0 && i < nt) p.part[((size_t)blockIdx.z * p.T + t0 + i) * p.E + e] = s;
+      }
+    }
+  }
+
+  // ---- 1b. FP8 codes of x by token, 8 values per thread, spread over all CTAs
+  {
+    const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    const int stride = gridDim.x * gridDim.y * gridDim.z * blockDim.x;
+    const int n8 = p.T * (p.H / 8);  // a multiple of 4: whole quads stay in or out
+    const unsigned quad = 0xFu << (lane & ~3);
+    const uint4* x8 = reinterpret_cast<const uint4*>(p.x);
+    uint2* q8 = reinterpret_cast<uint2*>(p.ws.xq);
+    for (int i = cta * blockDim.x + threadIdx.x; i < n8; i += stride) {
+      int ex;
+      q8[i] = quant8(x8[i], quad, &ex);
+      if ((lane & 3) == 0) p.ws.xs[i >> 2] = (uint8_t)(ex + 127);
+    }
+  }
+
+  // ---- 2. the last CTA of this token block selects its tokens' experts
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(&p.counters[blockIdx.y], 1) == (int)(gridDim.x * gridDim.z) - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (threadIdx.x == 0) p.counters[blockIdx.y] = 0;
+  if (p.route) {
+    float* lg = reinterpret_cast<float*>(sm);  // [nt][E]
+    const int t0 = blockIdx.y * kPrepTT, nt = min(kPrepTT, p.T - t0);
+    for (int i = threadIdx.x; i < nt * p.E; i += blockDim.x) {
+      const int t = i / p.E, e = i - t * p.E;
+      const float f = router_sum_partials(p.part, p.ks, p.T, p.E, t0 + t, e, p.b);
+      lg[i] = f;
+      if (p.logits_out) p.logits_out[(size_t)(t0 + t) * p.E + e] = f;
+    }
+    __syncthreads();
+    if (warp < nt) {
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int e = lane + 32 * i;
+        const float f = e < p.E ? lg[warp * p.E + e] : -INFINITY;
+        v[i] = isnan(f) ? -INFINITY : f;
+      }
+      select_topk(v, t0 + warp, p.E, p.k, lane, p.idx, p.w);
+    }
+  }
+
+  // ---- 3. the last token block builds the expert segments
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(&p.counters[gridDim.y], 1) == (int)gridDim.y - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (threadIdx.x == 0) p.counters[gridDim.y] = 0;
+  if (p.T * p.k <= (int)blockDim.x)
+    segments_small_cta(p.idx, p.T, p.k, p.E, p.ns, p.bn, p.ws, sm);
+  else
+    segments_cta(p.idx, p.T, p.k, p.E, p.ns, p.bn, p.ws, sm);
+}
+
+size_t prep_smem_bytes(int E, int H) {
+  const size_t seg = (size_t)33 * E * sizeof(int32_t), lg = (size_t)kPrepTT * E * sizeof(float);
+  const size_t xs = (size_t)kPrepTT * H * sizeof(uint16_t);  // bound for one K chunk of x
+  const size_t small = (size_t)(4 * E + 2 * 4 + 1024 + 1) * sizeof(int32_t);  // segments_small_cta
+  size_t m = seg > lg ? seg : lg;
+  m = m > xs ? m : xs;
+  return m > small ? m : small;
+}
+
+}  // namespace
+
+cudaError_t prepare_prep_kernel(int E, int H) {
+  return cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)prep_smem_bytes(E, H));
+}
+
+cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, int bn,
+                        const float* W, const float* b, float* logits_out, int32_t* idx, float* w,
+                        bool route, const Workspace& ws, cudaStream_t st) {
+  if (T <= 0 || T > kPrepMaxTokens) return cudaErrorInvalidValue;
+  PrepParams p;
+  p.x = x;
+  p.T = T;
+  p.H = H;
+  p.E = E;
+  p.k = k;
+  p.ns = ns;
+  p.bn = bn;
+  p.route = route ? 1 : 0;
+  p.W = W;
+  p.b = b;
+  p.ks = router_ksplit(H);
+  p.part = ws.rpart;
+  p.logits_out = logits_out;
+  p.idx = idx;
+  p.w = w;
+  p.counters = ws.prep_cnt;
+  p.ws = ws;
+  dim3 grid;
+  if (route) {
+    grid = dim3((E + kPrepWarps - 1) / kPrepWarps, (T + kPrepTT - 1) / kPrepTT, p.ks);
+  } else {
+    const int n8 = T * (H / 8);
+    int g = (n8 + 1023) / 1024;
+    grid = dim3(g < 1 ? 1 : (g > 64 ? 64 : g), 1, 1);
+  }
+  { cudaError_t le_ = launch_pdl(prep_kernel, grid, dim3(1024), prep_smem_bytes(E, H), st, p); if (le_ != cudaSuccess) return le_; }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

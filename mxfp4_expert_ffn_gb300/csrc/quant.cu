@@ -8,33 +8,10 @@
 // SIMT pipes with 128-bit accesses.
 #include "common.cuh"
 #include "internal.h"
+#include "segments.cuh"
 
 namespace moe {
 namespace {
-
-// Quantises 8 consecutive bf16 values; the four lanes of a quad (one 32-block)
-// agree on the block exponent.  Returns the 8 codes; *e gets the exponent.
-__device__ __forceinline__ uint2 quant8(const uint4 v, unsigned quad, int* e_out) {
-  float f[8];
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    f[2 * j] = __uint_as_float(w[j] << 16);
-    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-  }
-  float amax = 0.f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 2));
-  const int e = fp8_block_exponent(amax);
-  uint32_t c[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    c[j] = e4m3x2(scale_pow2_neg(f[2 * j], e), scale_pow2_neg(f[2 * j + 1], e));
-  *e_out = e;
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
 
 // One thread per 8 bf16 values; four consecutive threads form one 32-block.
 __global__ void quantize_act_kernel(const uint4* __restrict__ x, int n8, uint2* __restrict__ q,
@@ -71,142 +48,13 @@ __global__ void quantize_gather_kernel(const uint16_t* __restrict__ x, int P, in
   }
 }
 
-// Builds the expert segments in one CTA of 1024 threads.  Each warp owns a
-// contiguous range of slots; pass 1 counts its slots per expert, pass 2 turns
-// the counts into per-warp bases (warps in slot order), pass 3 places each
-// slot at base + rank among the warp's equal-expert lanes.  The result is a
-// stable counting sort, identical on every run.
+// Expert segments in one CTA of 1024 threads (segments.cuh).
 __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restrict__ idx, int T,
                                                         int k, int E, int ns, int bn, Workspace ws) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ int32_t sm[];
-  const int NE = E + ns;
-  int32_t* wcnt = sm;            // [32][E]  per-warp counts, then running bases
-  int32_t* stot = sm + 32 * E;   // [E]      totals, then exclusive offsets
-  __shared__ int routed_total;
-  const int S = T * k;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
-  __syncthreads();
-  const int per = (S + 31) / 32;
-  const int lo = min(S, warp * per), hi = min(S, lo + per);
-  for (int b = lo; b < hi; b += 32) {
-    const int s = b + lane;
-    int e = -1;
-    if (s < hi) {
-      e = idx[s];
-      if (e < 0 || e >= E) {
-        raise_error(ws.err, kErrExpertRange);
-        e = -1;
-      }
-    }
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
-    __syncwarp();
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int w = 0; w < 32; ++w) {
-      const int c = wcnt[w * E + e];
-      wcnt[w * E + e] = run;
-      run += c;
-    }
-    stot[e] = run;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // exclusive scan of the E totals and of the "has tokens" flags
-    const int chunk = (E + 31) / 32;
-    const int c0 = min(E, lane * chunk), c1 = min(E, c0 + chunk);
-    // (and of the token tiles of width bn, for the tensor-core path)
-    const int tb = bn > 0 ? bn : 1;
-    int sum = 0, nf = 0, nt = 0;
-    for (int e = c0; e < c1; ++e) {
-      sum += stot[e];
-      nf += stot[e] > 0;
-      nt += (stot[e] + tb - 1) / tb;
-    }
-    int isum = sum, inf = nf, intl = nt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xFFFFFFFFu, isum, o);
-      const int f = __shfl_up_sync(0xFFFFFFFFu, inf, o);
-      const int t = __shfl_up_sync(0xFFFFFFFFu, intl, o);
-      if (lane >= o) {
-        isum += a;
-        inf += f;
-        intl += t;
-      }
-    }
-    int run = isum - sum, fr = inf - nf, tr = intl - nt;
-    for (int e = c0; e < c1; ++e) {
-      const int c = stot[e];
-      ws.cnt[e] = c;
-      ws.off[e] = run;
-      stot[e] = run;
-      if (c > 0) {
-        ws.tile_prefix[fr] = tr;
-        ws.active[fr++] = e;
-        tr += (c + tb - 1) / tb;
-      }
-      run += c;
-    }
-    const int n_routed_active = __shfl_sync(0xFFFFFFFFu, inf, 31);
-    const int routed_tiles = __shfl_sync(0xFFFFFFFFu, intl, 31);
-    const int valid = __shfl_sync(0xFFFFFFFFu, isum, 31);
-    if (lane == 0) {
-      routed_total = valid;
-      int tiles = routed_tiles;
-      for (int sh = 0; sh < ns; ++sh) {
-        ws.cnt[E + sh] = T;
-        ws.off[E + sh] = S + sh * T;
-        if (T > 0) {
-          ws.active[n_routed_active + sh] = E + sh;
-          ws.tile_prefix[n_routed_active + sh] = tiles;
-          tiles += (T + tb - 1) / tb;
-        }
-      }
-      ws.off[NE] = S + ns * T;
-      *ws.n_active = n_routed_active + (T > 0 ? ns : 0);
-      ws.tile_prefix[n_routed_active + (T > 0 ? ns : 0)] = tiles;
-    }
-  }
-  __syncthreads();
-  for (int b = lo; b < hi; b += 32) {
-    const int s = b + lane;
-    int e = -1;
-    if (s < hi) {
-      e = idx[s];
-      if (e < 0 || e >= E) e = -1;
-    }
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-    if (e >= 0) {
-      const int p = stot[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
-      ws.perm[p] = s;
-      ws.slot_pos[s] = p;
-      ws.pos_tok[p] = s / k;
-    } else if (s < hi) {
-      ws.slot_pos[s] = -1;
-    }
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
-    __syncwarp();
-  }
-  for (int i = threadIdx.x; i < ns * T; i += blockDim.x) ws.pos_tok[S + i] = i % T;
-  // token tiles of width bn for the tensor-core path: (expert, first position, tokens)
-  if (bn > 0) {
-    const int na = *ws.n_active;
-    for (int a = threadIdx.x; a < na; a += blockDim.x) {
-      const int e = ws.active[a], c = ws.cnt[e], p0 = ws.off[e], t0 = ws.tile_prefix[a];
-      for (int j = 0; j * bn < c; ++j)
-        ws.tile_info[t0 + j] = make_int4(e, p0 + j * bn, min(bn, c - j * bn), 0);
-    }
-  }
-  // positions left free by invalid expert ids still name a real token, so
-  // that every position's row can be read safely
-  for (int p = routed_total + threadIdx.x; p < S; p += blockDim.x) ws.pos_tok[p] = 0;
+  segments_cta(idx, T, k, E, ns, bn, ws, sm);
 }
 
 // y[t] = bf16( sum_s o[S + s*T + t] + sum_j w[t][j] * o[slot_pos[t*k + j]] ),

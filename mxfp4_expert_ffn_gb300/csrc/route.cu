@@ -8,6 +8,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "router.cuh"
 
 namespace moe {
 namespace {
@@ -31,71 +32,14 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   float acc[TT];
 #pragma unroll
   for (int i = 0; i < TT; ++i) acc[i] = 0.f;
-  const float4* wr = reinterpret_cast<const float4*>(W + (size_t)e * H);
-  for (int h4 = lane; h4 < H / 4; h4 += 32) {
-    const float4 wv = __ldg(wr + h4);
-#pragma unroll
-    for (int i = 0; i < TT; ++i) {
-      if (i < nt) {
-        const uint2 xv = *reinterpret_cast<const uint2*>(x + (size_t)(t0 + i) * H + 4 * h4);
-        acc[i] = fmaf(wv.x, __uint_as_float(xv.x << 16), acc[i]);
-        acc[i] = fmaf(wv.y, __uint_as_float(xv.x & 0xFFFF0000u), acc[i]);
-        acc[i] = fmaf(wv.z, __uint_as_float(xv.y << 16), acc[i]);
-        acc[i] = fmaf(wv.w, __uint_as_float(xv.y & 0xFFFF0000u), acc[i]);
-      }
-    }
-  }
+  const uint32_t* x32 = reinterpret_cast<const uint32_t*>(x);
+  router_dot<TT>(W + (size_t)e * H, H, nt, lane,
+                 [&](int i, int h) { return x32[((size_t)(t0 + i) * H + h) / 2]; }, acc);
   const float bias = b ? b[e] : 0.f;
 #pragma unroll
   for (int i = 0; i < TT; ++i) {
     const float s = warp_sum(acc[i]);
     if (lane == 0 && i < nt) logits[(size_t)(t0 + i) * E + e] = s + bias;
-  }
-}
-
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-// k rounds of a warp arg-max over (value desc, index asc) on the 16 values
-// per lane (v[i] is expert lane + 32 i), then the softmax over the k chosen.
-__device__ __forceinline__ void select_topk(const float (&v)[16], int t, int E, int k, int lane,
-                                            int32_t* __restrict__ idx, float* __restrict__ w) {
-  uint32_t taken = 0;
-  float sv[8];
-  int si[8];
-  for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && ranks_before(v[i], e, bv, bi)) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      if (ranks_before(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    sv[r] = bv;
-    si[r] = bi;
-  }
-  if (lane == 0) {
-    const float m = sv[0];
-    float den = 0.f;
-    for (int r = 0; r < k; ++r) den += expf(sv[r] - m);
-    for (int r = 0; r < k; ++r) {
-      idx[(size_t)t * k + r] = si[r];
-      w[(size_t)t * k + r] = expf(sv[r] - m) / den;
-    }
   }
 }
 
@@ -135,20 +79,9 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 #pragma unroll
   for (int i = 0; i < TT; ++i) acc[i] = 0.f;
   const int k0 = ks * kc;
-  const float4* wr = reinterpret_cast<const float4*>(W + (size_t)e * H + k0);
-  for (int h4 = lane; h4 < kc / 4; h4 += 32) {
-    const float4 wv = __ldg(wr + h4);
-#pragma unroll
-    for (int i = 0; i < TT; ++i) {
-      if (i < nt) {
-        const uint2 xv = *reinterpret_cast<const uint2*>(x + (size_t)(t0 + i) * H + k0 + 4 * h4);
-        acc[i] = fmaf(wv.x, __uint_as_float(xv.x << 16), acc[i]);
-        acc[i] = fmaf(wv.y, __uint_as_float(xv.x & 0xFFFF0000u), acc[i]);
-        acc[i] = fmaf(wv.z, __uint_as_float(xv.y << 16), acc[i]);
-        acc[i] = fmaf(wv.w, __uint_as_float(xv.y & 0xFFFF0000u), acc[i]);
-      }
-    }
-  }
+  const uint32_t* x32 = reinterpret_cast<const uint32_t*>(x);
+  router_dot<TT>(W + (size_t)e * H + k0, kc, nt, lane,
+                 [&](int i, int h) { return x32[((size_t)(t0 + i) * H + k0 + h) / 2]; }, acc);
 #pragma unroll
   for (int i = 0; i < TT; ++i) {
     const float sum = warp_sum(acc[i]);
@@ -168,9 +101,7 @@ __global__ void __launch_bounds__(256) topk_sum_kernel(const float* __restrict__
   __shared__ float lg[512];
   const int t = blockIdx.x;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float f = 0.f;
-    for (int s = 0; s < ksplit; ++s) f += part[((size_t)s * T + t) * E + e];
-    f += b ? b[e] : 0.f;
+    const float f = router_sum_partials(part, ksplit, T, E, t, e, b);
     lg[e] = f;
     if (logits_out) logits_out[(size_t)t * E + e] = f;
   }

@@ -140,6 +140,30 @@ def test_layer_matches_oracle(wl, path):
     L.close()
 
 
+# Few work units with many K stages: the tensor-core GEMM cuts the units' K
+# range across CTAs and the last CTA of each unit adds the partial tiles.
+# gate/up split (K = 5120, 20 stages, ~10 pieces per unit); down split (K = 2304,
+# 6 stages in 3-chunk steps, 2-3 pieces per unit); ragged token tiles.
+SPLIT = [
+    Workload("split_up_h5120_i256_e8_k2_t3", 5120, 256, 8, 2, 1, 3, seed=21, scale_lo=-8, scale_hi=-4),
+    Workload("split_down_h1024_i2304_e8_k2_t3", 1024, 2304, 8, 2, 1, 3, seed=22, scale_lo=-8, scale_hi=-4),
+    Workload("split_both_h5120_i2304_e6_k1_t2", 5120, 2304, 6, 1, 1, 2, seed=23, scale_lo=-8, scale_hi=-4),
+]
+
+
+@pytest.mark.parametrize("wl", SPLIT, ids=lambda w: w.name)
+def test_split_partition_matches_oracle_and_is_deterministic(wl):
+    L, _ = gu.make_layer(wl)
+    L.set_option(m.MOE_OPT_PATH, m.PATH_MMA)
+    x = _x(wl)
+    idx, w = _oracle_routing(wl, x)
+    y = gu.run_forward(L, x, idx, w)
+    gu.assert_y_close(y, gu.oracle_layer(wl, 0, x, idx, w))
+    for _ in range(3):  # partial tiles are added in piece order, whoever arrives last
+        assert np.array_equal(gu.run_forward(L, x, idx, w), y)
+    L.close()
+
+
 def test_layer_with_residual_matches_oracle():
     wl = SMALL[1]
     L, _ = gu.make_layer(wl)
@@ -250,6 +274,47 @@ def test_forward_host_matches_device_path():
     idx, w, _ = gu.run_route(L, x, wl.tokens, wl.n_experts, wl.top_k)
     yd = gu.run_forward(L, x, idx, w)
     assert np.array_equal(yh.numpy().view(np.uint16), yd)
+    L.close()
+
+
+STEP = SMALL + [
+    Workload("step_h1024_i256_e64_k6_t64", 1024, 256, 64, 6, 1, 64, seed=24, scale_lo=-8, scale_hi=-4),
+    Workload("step_h512_i256_e32_k4_t80", 512, 256, 32, 4, 1, 80, seed=25, scale_lo=-8, scale_hi=-4),
+]
+
+
+@pytest.mark.parametrize("wl", STEP, ids=lambda w: w.name)
+@pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_SIMT])
+def test_step_equals_route_then_forward_and_matches_oracle(wl, path):
+    """moe_step (one launch for router + top-k + x codes + segments at up to
+    64 tokens) gives bit for bit what moe_route then moe_forward give; its
+    routing is the oracle's given its own logits; y is within tolerance."""
+    L, _ = gu.make_layer(wl)
+    L.set_option(m.MOE_OPT_PATH, path)
+    x = _x(wl)
+    T, E, k = wl.tokens, wl.n_experts, wl.top_k
+    xt = sg.bf16_tensor(x)
+    y = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=gu.DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=gu.DEV)
+    lo = torch.empty((T, E), dtype=torch.float32, device=gu.DEV)
+    L.step(xt, T, y, idx=idx, w=w, logits_out=lo)
+    assert L.sync() == m.MOE_OK
+    y, idx, w, lo = (y.cpu().numpy().view(np.uint16), idx.cpu().numpy(), w.cpu().numpy(),
+                     lo.cpu().numpy())
+    idx2, w2, lo2 = gu.run_route(L, x, T, E, k)
+    assert np.array_equal(lo, lo2) and np.array_equal(idx, idx2) and np.array_equal(w, w2)
+    assert np.array_equal(gu.run_forward(L, x, idx2, w2), y)
+    ridx, rw = oracle.topk(lo.astype(np.float32), k)
+    assert np.array_equal(idx, ridx)
+    assert np.allclose(w, rw, rtol=2e-6, atol=1e-7)
+    gu.assert_y_close(y, gu.oracle_layer(wl, 0, x, idx, rw))
+    # with a residual and without the optional outputs
+    r = _x(wl, stream=5)
+    y3 = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    L.step(xt, T, y3, residual=sg.bf16_tensor(r))
+    assert L.sync() == m.MOE_OK
+    assert np.array_equal(y3.cpu().numpy().view(np.uint16), gu.run_forward(L, x, idx2, w2, residual_bits=r))
     L.close()
 
 
