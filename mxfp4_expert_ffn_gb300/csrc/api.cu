@@ -59,7 +59,7 @@ size_t carve(const moe_config& c, int num_sms, char* base, Workspace& ws) {
   ws.slot_pos = cv.take<int32_t>(S);
   ws.pos_tok = cv.take<int32_t>(P);
   ws.active = cv.take<int32_t>(NE);
-  ws.n_active = cv.take<int32_t>(1);
+  ws.n_active = cv.take<int32_t>(2);
   ws.tile_prefix = cv.take<int32_t>(NE + 1);
   // sum over experts of ceil(tokens / 16) <= slots / 16 + experts
   ws.tile_info = cv.take<int4>(P / 16 + NE + 16);

@@ -108,6 +108,16 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, unsigned quad, int* e_out
   return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
+// *p += v at device scope with acquire-release order; returns the old value.
+// Used by one thread after a CTA barrier: it publishes the writes the barrier
+// ordered before it and, for the thread that sees the final count, acquires
+// the writes every other CTA published the same way.
+__device__ __forceinline__ int atomic_add_acq_rel(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Programmatic dependent launch: wait until the preceding kernel in the
 // stream has finished and flushed its writes (a no-op when the kernel was not
 // launched as a dependent), then let the next kernel start its prologue.

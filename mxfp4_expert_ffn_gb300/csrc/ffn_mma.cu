@@ -44,8 +44,9 @@ struct MmaParams {
   const uint8_t* sb;         // activation scales by position, [P][K/32]
   int E, K, rows;            // rows per expert of the weight matrices (I up, H down)
   int out_cols;              // I (h row length) in up mode, H in down mode
-  const int32_t* n_active;
+  const int32_t* n_active;   // [0] active experts, [1] token tiles in all
   const int32_t* tile_prefix;
+  int wait_tiles;            // the tile table comes from the previous kernel itself
   const int4* tile_info;
   int n_stages;              // ring depth (runtime: fits the shared memory)
   int merged[2];             // up mode, routed / shared: gate and up load as one 4-D op
@@ -73,7 +74,8 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreadsMma = 320;
+constexpr int kThreadsMma = 352;  // 11 warps: TMA, MMA, 4 epilogue, 4 scale-factor, 2nd MMA
+constexpr int kIssuer2Warp = 10;
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kSmemBudget = 227 * 1024 - 2048;
 
@@ -86,9 +88,22 @@ struct Cfg {
   static constexpr int kNA = MODE == kModeUp ? 2 : 1;     // weight matrices per unit
   static constexpr int kATile = 128 * 128 * CH;           // one matrix, one stage
   static constexpr int kBTile = BN * 128 * CH;
-  static constexpr int kAccCols = kNA * BN;               // g then u (up) or o (down)
+  // MMA issue is split over two threads (see the kernel): gate/up one matrix
+  // each; down one half of the token columns each (BN >= 64) or one half of
+  // each stage's K steps, into a second accumulator (BN = 16).
+  static constexpr bool kSplitN = MODE == kModeDown && BN >= 64;
+  static constexpr bool kSplitK = MODE == kModeDown && BN < 64;
+  static constexpr int kAccCols = (MODE == kModeUp || kSplitK ? 2 : 1) * BN;  // g, u (up); o (down)
   static constexpr int kNAcc = (MODE == kModeUp && BN >= 128) ? 1 : 2;
-  static constexpr int kSfCols = (kNA + 1) * 4 * CH;      // 4 columns per (matrix, chunk)
+  // Scale factors in TMEM, per stage: 4 columns per (weight matrix, chunk),
+  // then per chunk the token scales (group of 32 tokens g at column g); with
+  // the column split each half starts a 4-column group of its own (the MMA
+  // is handed a 4-column-aligned scale address).
+  static constexpr int kBCols = kSplitN ? 8 : 4;
+  static constexpr int kSfCols = kNA * 4 * CH + kBCols * CH;
+  __host__ __device__ static constexpr int sfb_col(int c, int g) {
+    return kNA * 4 * CH + c * kBCols + (kSplitN ? (g / (BN / 64)) * 4 + g % (BN / 64) : g);
+  }
   static constexpr int kTmemCols = kNAcc * kAccCols + kMaxStages * kSfCols;
   static constexpr int kTmemAlloc = pow2_cols(kTmemCols);
   static_assert(kTmemCols <= 512, "TMEM budget");
@@ -235,10 +250,10 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&sf_bar[s], 4);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], 2);  // one commit per MMA-issuing thread
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&accf_bar[b], 1);
+      mbar_init(&accf_bar[b], 2);
       mbar_init(&acce_bar[b], 4);
     }
     abort_flag = 0;
@@ -249,11 +264,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_slot;
-  // Programmatic dependent launch: the tile table and the weights were ready
-  // before the previous kernel started, so they are read right away; the
-  // activations (and the outputs' readers) wait for it in pdl_wait() below.
+  // Programmatic dependent launch.  Usually the tile table and the weights
+  // were final before the previous kernel started, so they are read right
+  // away and only the activations (and the outputs' readers) wait for the
+  // previous kernel in pdl_wait() below; after the small-batch preparation
+  // kernel the tile table is that kernel's own output, so everything waits.
+  if (p.wait_tiles) pdl_wait();
   pdl_trigger();
-  const int total = p.tile_prefix[*p.n_active] * mt_per_expert;
+  const int total = p.n_active[1] * mt_per_expert;
   const Sched sc0(total, k_stages, BN <= 64 && p.split_ok);
 
   auto give_up = [&]() {
@@ -326,11 +344,18 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       for (int s = 0; s < kMaxStages; ++s)
         if (last_parity[s] >= 0) mbar_wait(&full_bar[s], (uint32_t)last_parity[s], kWaitLimit);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kIssuer2Warp) {
     // ---------------------------------------------------------------- MMA
+    // Two issuing threads.  A thread that also commits (tcgen05.commit in the
+    // same loop) issues tcgen05.mma at ~105 cycles per instruction for N <=
+    // 128; two such threads keep the tensor pipe at its throughput (measured:
+    // ~39 cycles at N = 16, ~64 at N = 128).  Each thread commits its own
+    // MMAs, so the empty and accumulator-full barriers count two arrivals.
     if (lane == 0) {
+      const int j = warp == 1 ? 0 : 1;
+      constexpr int NI = C::kSplitN ? BN / 2 : BN;  // N of each MMA
       uint32_t g = 0, it = 0;
-      const uint32_t idesc_base = idesc_e2m1_e4m3(128, BN, 0);
+      const uint32_t idesc_base = idesc_e2m1_e4m3(128, NI, 0);
       Sched sc = sc0;
       for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
         const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
@@ -365,12 +390,22 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             for (int k = 0; k < 4; ++k) {
               const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
               const uint64_t bdesc = b_desc0 + (uint64_t)((c * BN * 128 + 32 * k) >> 4);
-#pragma unroll
-              for (int m = 0; m < NA; ++m) {
-                const int acc = swap ? NA - 1 - m : m;  // gate -> accumulator 0, up -> 1
+              const uint32_t sfb = sf + C::sfb_col(c, 0);
+              if constexpr (MODE == kModeUp) {
+                const int m = j, acc = swap ? 1 - m : m;  // gate -> accumulator 0, up -> 1
                 mma_mxf8f6f4(d_tmem + acc * BN, a_desc0 + (uint64_t)((m * C::kATile + c * 16384 + 32 * k) >> 4),
-                             bdesc, idesc, sf + (acc * CH + c) * 4, sf + (NA * CH + c) * 4,
+                             bdesc, idesc, sf + (acc * CH + c) * 4, sfb, (s != s_beg || c || k) ? 1u : 0u);
+              } else if constexpr (C::kSplitN) {
+                // token columns [j * NI, (j + 1) * NI): B rows and their scale lanes
+                mma_mxf8f6f4(d_tmem + j * NI, a_desc0 + (uint64_t)((c * 16384 + 32 * k) >> 4),
+                             bdesc + (uint64_t)((j * NI * 128) >> 4), idesc, sf + c * 4, sf + C::sfb_col(c, j * NI / 32),
                              (s != s_beg || c || k) ? 1u : 0u);
+              } else {
+                // K steps i = 4c + k of the stage: the first half to accumulator 0
+                const int i = c * 4 + k, first = j * CH * 2;
+                if ((i < CH * 2) == (j == 0))
+                  mma_mxf8f6f4(d_tmem + j * BN, a_desc0 + (uint64_t)((c * 16384 + 32 * k) >> 4), bdesc, idesc,
+                               sf + c * 4, sfb, (s != s_beg || i != first) ? 1u : 0u);
               }
             }
           mma_commit(&empty_bar[slot]);
@@ -464,7 +499,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
 #pragma unroll
             for (int m = 0; m < NA; ++m) tmem_st_x1(col + (m * CH + c) * 4 + q, w[i][m * CH + c]);
 #pragma unroll
-            for (int cb = 0; cb < NC; ++cb) tmem_st_x1(col + (NA * CH + c) * 4 + cb, w[i][NA * CH + c * NC + cb]);
+            for (int cb = 0; cb < NC; ++cb) tmem_st_x1(col + C::sfb_col(c, cb), w[i][NA * CH + c * NC + cb]);
           }
           tmem_st_wait();
           fence_before();
@@ -589,7 +624,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         for (int c = 0; c < BN; c += 16) {
           uint32_t v[16], vu[16];
           tmem_ld16(t_base + c, v);
-          if (MODE == kModeUp) tmem_ld16(t_base + BN + c, vu);
+          if (MODE == kModeUp || C::kSplitK) tmem_ld16(t_base + BN + c, vu);
           tmem_ld_wait();
           if (c + 16 >= BN) {
             fence_before();
@@ -599,7 +634,10 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c + j >= un.m_tile) break;  // warp-uniform
-            emit(un, c + j, __uint_as_float(v[j]), MODE == kModeUp ? __uint_as_float(vu[j]) : 0.f);
+            if constexpr (C::kSplitK)  // the two K halves, in fixed order
+              emit(un, c + j, __uint_as_float(v[j]) + __uint_as_float(vu[j]), 0.f);
+            else
+              emit(un, c + j, __uint_as_float(v[j]), MODE == kModeUp ? __uint_as_float(vu[j]) : 0.f);
           }
         }
         combine_tail(un);
@@ -615,7 +653,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         for (int c = 0; c < BN; c += 16) {
           uint32_t v[16], vu[16];
           tmem_ld16(t_base + c, v);
-          if (MODE == kModeUp) tmem_ld16(t_base + BN + c, vu);
+          if (MODE == kModeUp || C::kSplitK) tmem_ld16(t_base + BN + c, vu);
           tmem_ld_wait();
           if (c + 16 >= BN) {
             fence_before();
@@ -625,7 +663,10 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c + j >= un.m_tile) break;  // warp-uniform
-            mine[(c + j) * 128 + rl] = __uint_as_float(v[j]);
+            if constexpr (C::kSplitK)
+              mine[(c + j) * 128 + rl] = __uint_as_float(v[j]) + __uint_as_float(vu[j]);
+            else
+              mine[(c + j) * 128 + rl] = __uint_as_float(v[j]);
             if (MODE == kModeUp) mine[(BN + c + j) * 128 + rl] = __uint_as_float(vu[j]);
           }
         }
@@ -831,6 +872,7 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
     p.sb = ws.xgs;
     if (gather && bn == 16) {  // activations by token: codes xq, scales xs
       p.gather = 1;
+      p.wait_tiles = 1;  // launched right after the preparation kernel
       p.xq = ws.xq;
       p.pos_tok = ws.pos_tok;
       p.sb = ws.xs;

@@ -24,7 +24,7 @@ struct Workspace {
   int32_t* slot_pos = nullptr;// [T*k]      position of each slot (-1: invalid id)
   int32_t* pos_tok = nullptr; // [P]        token of each position
   int32_t* active = nullptr;  // [NE]       experts with tokens, routed then shared
-  int32_t* n_active = nullptr;// [1]
+  int32_t* n_active = nullptr;// [2]        active experts, token tiles in all
   int32_t* tile_prefix = nullptr; // [NE+1] token tiles before each active expert
   int4* tile_info = nullptr;  // [tiles]    (expert, first position, tokens, 0) per token tile
   uint8_t* xg = nullptr;      // [P][H]     E4M3 codes of x, gathered by position

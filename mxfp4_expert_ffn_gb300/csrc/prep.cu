@@ -15,8 +15,8 @@
 //   2. the last CTA of each 8-token block to finish adds the K chunks of its
 //      tokens' logits in a fixed order, selects top-k and writes the weights;
 //   3. the last token block to finish builds the expert segments.
-// "Last" is decided by an atomic counter after a device-scope fence; the
-// finisher resets the counter, so the next launch starts from zero.  The sums
+// "Last" is decided by an acquire-release atomic counter; the finisher resets
+// the counter, so the next launch starts from zero.  The sums
 // are the same fixed-order sums as the split-K router kernels, so the logits
 // are bit-identical to theirs.
 #include "common.cuh"
@@ -46,7 +46,8 @@ struct PrepParams {
 };
 
 __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ PrepParams p) {
-  pdl_wait();  // x may come from the previous kernel
+  pdl_wait();     // x may come from the previous kernel
+  pdl_trigger();  // the expert GEMM may start its prologue; it waits for all of this
   extern __shared__ int32_t sm[];
   __shared__ int last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -93,15 +94,15 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
   }
 
   // ---- 2. the last CTA of this token block selects its tokens' experts
+  // (one acquire-release atomic per CTA: it publishes the CTA's writes, which
+  // the barrier made its own, and the last arriver acquires everyone's)
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    last = atomicAdd(&p.counters[blockIdx.y], 1) == (int)(gridDim.x * gridDim.z) - 1;
+    last = atomic_add_acq_rel(&p.counters[blockIdx.y], 1) == (int)(gridDim.x * gridDim.z) - 1;
+    if (last) p.counters[blockIdx.y] = 0;
   }
   __syncthreads();
   if (!last) return;
-  __threadfence();
-  if (threadIdx.x == 0) p.counters[blockIdx.y] = 0;
   if (p.route) {
     float* lg = reinterpret_cast<float*>(sm);  // [nt][E]
     const int t0 = blockIdx.y * kPrepTT, nt = min(kPrepTT, p.T - t0);
@@ -126,14 +127,14 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
 
   // ---- 3. the last token block builds the expert segments
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    last = atomicAdd(&p.counters[gridDim.y], 1) == (int)gridDim.y - 1;
+  if (gridDim.y > 1) {
+    if (threadIdx.x == 0) {
+      last = atomic_add_acq_rel(&p.counters[gridDim.y], 1) == (int)gridDim.y - 1;
+      if (last) p.counters[gridDim.y] = 0;
+    }
+    __syncthreads();
+    if (!last) return;
   }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  if (threadIdx.x == 0) p.counters[gridDim.y] = 0;
   if (p.T * p.k <= (int)blockDim.x)
     segments_small_cta(p.idx, p.T, p.k, p.E, p.ns, p.bn, p.ws, sm);
   else

@@ -111,6 +111,7 @@ __device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx, in
       }
       ws.off[NE] = S + ns * T;
       *ws.n_active = n_routed_active + (T > 0 ? ns : 0);
+      ws.n_active[1] = tiles;
       ws.tile_prefix[n_routed_active + (T > 0 ? ns : 0)] = tiles;
     }
   }
@@ -236,6 +237,7 @@ __device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ i
       const int na = n_routed_active + (T > 0 ? ns : 0);
       n_act_s = na;
       *ws.n_active = na;
+      ws.n_active[1] = tiles;
       tp_s[na] = tiles;
     }
   }
