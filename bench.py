@@ -125,6 +125,26 @@ def layer_bytes(wl, n_experts_touched: int, T: int) -> dict:
             "ffn_up_mma": up, "ffn_down_mma": down}
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu capture
+# summarised in profiles/ffn_mma_decode_e24_t1_full.md; valid only for the kernel source it was
+# taken on and for a decode token (7 experts streamed per launch, as in that capture).
+_TRAFFIC_SRC = "mxfp4_expert_ffn_gb300/csrc/ffn_mma.cu"
+_TRAFFIC_SHA256 = "61d8ccfb1a5b688dc3c0b2574e1d72be49e3955e6987f6d8f2681087d700cbec"
+_TRAFFIC = {("v41_layer_decode_t1", "ffn_up_mma"): (88.534272 + 2.638336) * 1e6,
+            ("v41_layer_decode_t1", "ffn_down_mma"): (43.983872 + 0.027136) * 1e6}
+
+
+def measured_traffic(workload: str, kernel: str):
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, _TRAFFIC_SRC), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != _TRAFFIC_SHA256:
+                return None  # the kernel changed since the counters were taken
+    except OSError:
+        return None
+    return _TRAFFIC.get((workload, kernel))
+
+
 def layer_flops(wl, T: int) -> int:
     return (T * wl.top_k + wl.n_shared * T) * 3 * 2 * wl.hidden * wl.inter
 
@@ -320,7 +340,8 @@ def run_ours(args):
         if dom in b:
             ach = b[dom] / (dom_ms / 1e3) / 1e9
             roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": pk["hbm_gbs"],
-                        "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None,
+                        "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                        "traffic": measured_traffic(wl.name, dom),
                         "algorithmic_bytes_per_launch": b[dom], "avg_launch_ms": dom_ms,
                         "peak_src": pk["src"]}
         layer_gbs = b["layer"] / (ms_step / 1e3) / 1e9
