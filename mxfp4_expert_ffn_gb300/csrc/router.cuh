@@ -65,6 +65,19 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
+// The k selected (value, expert) pairs in rank order -> idx[t][r] and
+// w[t][r] = exp(v_r - v_0) / sum_r' exp(v_r' - v_0), summed in rank order.
+__device__ __forceinline__ void topk_softmax_write(const float* sv, const int* si, int t, int k,
+                                                   int32_t* __restrict__ idx, float* __restrict__ w) {
+  const float m = sv[0];
+  float den = 0.f;
+  for (int r = 0; r < k; ++r) den += expf(sv[r] - m);
+  for (int r = 0; r < k; ++r) {
+    idx[(size_t)t * k + r] = si[r];
+    w[(size_t)t * k + r] = expf(sv[r] - m) / den;
+  }
+}
+
 // k rounds of a warp arg-max over (value desc, index asc) on the 16 values
 // per lane (v[i] is expert lane + 32 i), then the softmax over the k chosen.
 __device__ __forceinline__ void select_topk(const float (&v)[16], int t, int E, int k, int lane,
@@ -96,15 +109,7 @@ __device__ __forceinline__ void select_topk(const float (&v)[16], int t, int E, 
     sv[r] = bv;
     si[r] = bi;
   }
-  if (lane == 0) {
-    const float m = sv[0];
-    float den = 0.f;
-    for (int r = 0; r < k; ++r) den += expf(sv[r] - m);
-    for (int r = 0; r < k; ++r) {
-      idx[(size_t)t * k + r] = si[r];
-      w[(size_t)t * k + r] = expf(sv[r] - m) / den;
-    }
-  }
+  if (lane == 0) topk_softmax_write(sv, si, t, k, idx, w);
 }
 
 }  // namespace moe

@@ -152,7 +152,7 @@ __device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx, in
 }
 
 
-// The same segments for a small batch (T * k <= blockDim.x == 1024, E <= 512),
+// The same segments for a small batch (T * k <= blockDim.x == 1024, E <= 1024),
 // with every intermediate in shared memory: one thread per slot, counts by
 // shared atomics, the rank of a slot among its expert's slots by counting
 // the earlier equal slots (so the order is the stable one above, bit for bit).
@@ -182,48 +182,65 @@ __device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ i
     if (e >= 0) atomicAdd(&cnt_s[e], 1);
   }
   __syncthreads();
-  if (warp == 0) {
-    // exclusive scans of the counts, of the "has slots" flags and of the token tiles
-    const int chunk = (E + 31) / 32;
-    const int c0 = min(E, lane * chunk), c1 = min(E, c0 + chunk);
+  {
+    // block-wide exclusive scans over the experts (one thread each) of the counts,
+    // of the "has slots" flags and of the token tiles
+    __shared__ int wsum[32][3];
     const int tb = bn > 0 ? bn : 1;
-    int sum = 0, nf = 0, nt = 0;
-    for (int x = c0; x < c1; ++x) {
-      const int c = cnt_s[x];
-      sum += c;
-      nf += c > 0;
-      nt += (c + tb - 1) / tb;
-    }
-    int isum = sum, inf = nf, intl = nt;
+    const int c = tid < E ? cnt_s[tid] : 0;
+    const int f = c > 0, ntl = (c + tb - 1) / tb;
+    int a = c, b = f, d = ntl;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xFFFFFFFFu, isum, o);
-      const int f = __shfl_up_sync(0xFFFFFFFFu, inf, o);
-      const int t = __shfl_up_sync(0xFFFFFFFFu, intl, o);
+      const int a2 = __shfl_up_sync(0xFFFFFFFFu, a, o);
+      const int b2 = __shfl_up_sync(0xFFFFFFFFu, b, o);
+      const int d2 = __shfl_up_sync(0xFFFFFFFFu, d, o);
       if (lane >= o) {
-        isum += a;
-        inf += f;
-        intl += t;
+        a += a2;
+        b += b2;
+        d += d2;
       }
     }
-    int run = isum - sum, fr = inf - nf, tr = intl - nt;
-    for (int x = c0; x < c1; ++x) {
-      const int c = cnt_s[x];
-      ws.cnt[x] = c;
-      ws.off[x] = run;
-      off_s[x] = run;
+    if (lane == 31) {
+      wsum[warp][0] = a;
+      wsum[warp][1] = b;
+      wsum[warp][2] = d;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int x = wsum[lane][0], y = wsum[lane][1], z = wsum[lane][2];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x2 = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        const int y2 = __shfl_up_sync(0xFFFFFFFFu, y, o);
+        const int z2 = __shfl_up_sync(0xFFFFFFFFu, z, o);
+        if (lane >= o) {
+          x += x2;
+          y += y2;
+          z += z2;
+        }
+      }
+      wsum[lane][0] = x;  // inclusive prefix over warps
+      wsum[lane][1] = y;
+      wsum[lane][2] = z;
+    }
+    __syncthreads();
+    const int pa = warp ? wsum[warp - 1][0] : 0, pb = warp ? wsum[warp - 1][1] : 0,
+              pd = warp ? wsum[warp - 1][2] : 0;
+    if (tid < E) {
+      const int off = pa + a - c, fr = pb + b - f, tr = pd + d - ntl;
+      ws.cnt[tid] = c;
+      ws.off[tid] = off;
+      off_s[tid] = off;
       if (c > 0) {
+        act_s[fr] = tid;
         tp_s[fr] = tr;
-        act_s[fr++] = x;
-        tr += (c + tb - 1) / tb;
       }
-      run += c;
     }
-    const int n_routed_active = __shfl_sync(0xFFFFFFFFu, inf, 31);
-    int tiles = __shfl_sync(0xFFFFFFFFu, intl, 31);
-    const int valid = __shfl_sync(0xFFFFFFFFu, isum, 31);
-    if (lane == 0) {
-      routed_total_s = valid;
+    if (tid == 0) {
+      const int n_routed_active = wsum[31][1];
+      int tiles = wsum[31][2];
+      routed_total_s = wsum[31][0];
       for (int sh = 0; sh < ns; ++sh) {
         ws.cnt[E + sh] = T;
         ws.off[E + sh] = S + sh * T;
