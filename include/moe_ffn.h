@@ -196,12 +196,31 @@ moe_status moe_route_static(const void* x, int32_t T, int32_t H, int32_t E, int3
 moe_status moe_sync(moe_layer* layer, void* stream);
 
 /* Options (moe_set_option):
- *  MOE_OPT_PATH    0 = automatic by per-expert load, 1 = always the SIMT
- *                  streaming kernels, 2 = always the tensor-core kernels
- *                  (MOE_ERR_UNSUPPORTED if the build has none).
+ *  MOE_OPT_PATH    0 = automatic (the tensor-core kernels when the build
+ *                  has them), 1 = always the SIMT streaming kernels, 2 =
+ *                  always the tensor-core kernels (MOE_ERR_UNSUPPORTED if
+ *                  the build has none).
  *  MOE_OPT_TIMING  1 = record CUDA events around each kernel the layer
- *                  launches (read with moe_get_kernel_times), 0 = off.   */
-enum { MOE_OPT_PATH = 1, MOE_OPT_TIMING = 2 };
+ *                  launches (read with moe_get_kernel_times), 0 = off.
+ *  MOE_OPT_SCORING how the routed weights follow from the logits:
+ *                  MOE_SCORING_SOFTMAX (default): logits include router_b,
+ *                  selection on them, weights = softmax over the k selected;
+ *                  MOE_SCORING_SIGMOID: logits l = router_w x without the
+ *                  bias, s = sigmoid(l), selection on s + router_b (ties to
+ *                  the lower index), weights = s / (sum of the k selected s).
+ *                  The pages call the gate a switch over the top 6 (ai.rs,
+ *                  "What remains is the reference rounding itself") without
+ *                  naming the score; softmax is this library's reading, sigmoid
+ *                  with a selection-only bias is the DeepSeek-V3-style variant.
+ *                  sigmoid is computed by a fixed sequence of fp32 operations
+ *                  (no library exp) so that selection is reproducible bit for
+ *                  bit; logits_in / logits_out of moe_route are then unbiased.
+ *  MOE_OPT_ROUTED_SCALE  routed weights are multiplied by this factor (the
+ *                  shared experts keep weight 1): value = the IEEE-754 bits
+ *                  of a positive finite float in the low 32 bits; default 1.
+ * moe_route_static always uses softmax scoring with scale 1.             */
+enum { MOE_OPT_PATH = 1, MOE_OPT_TIMING = 2, MOE_OPT_SCORING = 3, MOE_OPT_ROUTED_SCALE = 4 };
+enum { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 };
 moe_status moe_set_option(moe_layer* layer, int32_t option, int64_t value);
 
 /* Per-kernel timing gathered while MOE_OPT_TIMING is on (synchronises the

@@ -15,7 +15,8 @@ LIB_PATH = os.path.join(_HERE, "libmoe_ffn.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_INTERNAL = 4, 5, 6
-MOE_OPT_PATH, MOE_OPT_TIMING = 1, 2
+MOE_OPT_PATH, MOE_OPT_TIMING, MOE_OPT_SCORING, MOE_OPT_ROUTED_SCALE = 1, 2, 3, 4
+MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_MMA = 0, 1, 2
 
 # every symbol include/moe_ffn.h declares
@@ -235,6 +236,13 @@ class Layer:
 
     def set_option(self, option, value):
         moe_set_option(self.handle, option, value)
+
+    def set_scoring(self, scoring: int, routed_scale: float = 1.0):
+        """Scoring mode (MOE_SCORING_*) and routed scaling factor."""
+        import struct
+        moe_set_option(self.handle, MOE_OPT_SCORING, scoring)
+        moe_set_option(self.handle, MOE_OPT_ROUTED_SCALE,
+                       struct.unpack("<I", struct.pack("<f", routed_scale))[0])
 
     def kernel_times(self):
         return moe_get_kernel_times(self.handle)

@@ -279,6 +279,20 @@ moe_status moe_set_option(moe_layer* L, int32_t option, int64_t value) {
     L->path = (int)value;
     return MOE_OK;
   }
+  if (option == MOE_OPT_SCORING) {
+    if (value != MOE_SCORING_SOFTMAX && value != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+    L->scoring = (int)value;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_ROUTED_SCALE) {
+    if (value < 0 || value > 0xFFFFFFFFll) return MOE_ERR_INVALID_ARG;
+    const uint32_t bits = (uint32_t)value;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    if (!(f > 0.f) || f > 3.0e38f) return MOE_ERR_INVALID_ARG;  // positive, finite (NaN fails too)
+    L->routed_scale = f;
+    return MOE_OK;
+  }
   if (option == MOE_OPT_TIMING) {
     DeviceGuard g(L->device);
     if (value && !L->ev_pool[0]) {
@@ -338,6 +352,10 @@ moe_status check_tokens(const moe_layer* L, int32_t T) {
   return MOE_OK;
 }
 
+Scoring scoring_of(const moe_layer* L) {
+  return Scoring{L->scoring, L->routed_scale, L->w.router_b};
+}
+
 moe_status route_impl(moe_layer* L, const void* x, int32_t T, const float* logits_in,
                       float* logits_out, int32_t* idx, float* w, cudaStream_t st) {
   const moe_config& c = L->cfg;
@@ -347,8 +365,8 @@ moe_status route_impl(moe_layer* L, const void* x, int32_t T, const float* logit
     // small T: split-K logits (W_r streamed by ~E/8 x 8 CTAs), summed in the top-k pass
     TimedScope ts(L, st, "router_split");
     return cuda_fail(launch_router_split(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts,
-                                         c.top_k, L->w.router_w, L->w.router_b, L->ws.rpart,
-                                         logits_out, idx, w, st));
+                                         c.top_k, L->w.router_w, L->w.router_b, scoring_of(L),
+                                         L->ws.rpart, logits_out, idx, w, st));
   }
   if (!lg && L->router_mma && L->path != 1) {
     // many tokens: tensor-core logits (three bf16 parts of W_r), K split over CTAs
@@ -357,14 +375,14 @@ moe_status route_impl(moe_layer* L, const void* x, int32_t T, const float* logit
                           L->ws.rpart, L->ws.err, L->num_sms, st);
     if (e == cudaSuccess)
       e = launch_topk_sum(L->ws.rpart, router_mma_ksplit(c.hidden), L->w.router_b, T, c.n_experts,
-                          c.top_k, logits_out, idx, w, st);
+                          c.top_k, scoring_of(L), logits_out, idx, w, st);
     return cuda_fail(e);
   }
   if (!lg) {
     float* dst = logits_out ? logits_out : L->ws.logits;
     TimedScope ts(L, st, "router_logits");
-    e = launch_router_logits(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts,
-                             L->w.router_w, L->w.router_b, dst, L->num_sms, st);
+    e = launch_router_logits(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts, L->w.router_w,
+                             L->scoring ? nullptr : L->w.router_b, dst, L->num_sms, st);
     lg = dst;
   } else if (logits_out && logits_out != logits_in) {
     e = cudaMemcpyAsync(logits_out, logits_in, sizeof(float) * (size_t)T * c.n_experts,
@@ -373,7 +391,7 @@ moe_status route_impl(moe_layer* L, const void* x, int32_t T, const float* logit
   if (e != cudaSuccess) return cuda_fail(e);
   {
     TimedScope ts(L, st, "topk");
-    e = launch_topk(lg, T, c.n_experts, c.top_k, idx, w, st);
+    e = launch_topk(lg, T, c.n_experts, c.top_k, scoring_of(L), idx, w, st);
   }
   return cuda_fail(e);
 }
@@ -430,7 +448,8 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
     {
       TimedScope ts(L, st, "prep");
       e = launch_prep(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts, c.top_k, c.n_shared,
-                      bn, nullptr, nullptr, nullptr, const_cast<int32_t*>(idx), nullptr, false, L->ws, st);
+                      bn, nullptr, nullptr, scoring_of(L), nullptr, const_cast<int32_t*>(idx), nullptr, false,
+                      L->ws, st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return ffn_tail(L, T, bn, true, w, residual, y, st);
@@ -487,7 +506,7 @@ moe_status step_impl(moe_layer* L, const void* x, int32_t T, const void* residua
     {
       TimedScope ts(L, st, "prep");
       e = launch_prep(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts, c.top_k, c.n_shared,
-                      bn, L->w.router_w, L->w.router_b, logits_out, idx, w, true, L->ws, st);
+                      bn, L->w.router_w, L->w.router_b, scoring_of(L), logits_out, idx, w, true, L->ws, st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return ffn_tail(L, T, bn, true, w, residual, y, st);

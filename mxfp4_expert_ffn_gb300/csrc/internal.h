@@ -11,6 +11,19 @@ namespace moe {
 
 constexpr int kMaxTimed = 16;
 
+// How routed weights are formed from the fp32 router logits l.
+//  softmax (0): the bias is part of l; selection on l; w = softmax over the k
+//               selected l.
+//  sigmoid (1): s = sigmoid(l) with l unbiased; selection on s + bias; w = s /
+//               (sum of the k selected s).  The DeepSeek-V3 style gate.
+// In both, w is then multiplied by scale (the routed scaling factor).
+struct Scoring {
+  int sigmoid;
+  float scale;
+  const float* sel_bias;  // sigmoid: per-expert selection bias, or null
+};
+
+
 // Device workspace, sized at create time for cfg.max_tokens.
 // Positions: the T*k routed slots grouped expert by expert (stable in slot
 // order), then n_shared blocks of T positions for the shared experts
@@ -68,6 +81,8 @@ struct moe_layer {
   int device = 0;
   int num_sms = 0;
   int path = 0;
+  int scoring = 0;            // MOE_SCORING_SOFTMAX / MOE_SCORING_SIGMOID
+  float routed_scale = 1.0f;  // routed weights are multiplied by it
   bool timing = false;
   moe::Workspace ws;
   moe::MmaMaps* maps = nullptr;  // TMA descriptors of the tensor-core path
@@ -119,17 +134,18 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const f
 int router_ksplit(int H);
 constexpr int kRouterSplitMaxT = 64;
 cudaError_t launch_router_split(const uint16_t* x, int T, int H, int E, int k, const float* W,
-                                const float* b, float* part, float* logits_out, int32_t* idx,
-                                float* w, cudaStream_t st);
+                                const float* b, const Scoring& sg, float* part, float* logits_out,
+                                int32_t* idx, float* w, cudaStream_t st);
 cudaError_t launch_topk_sum(const float* part, int ksplit, const float* b, int T, int E, int k,
-                            float* logits_out, int32_t* idx, float* w, cudaStream_t st);
+                            const Scoring& sg, float* logits_out, int32_t* idx, float* w,
+                            cudaStream_t st);
 int router_mma_ksplit(int H);
 cudaError_t router_split_weights(const float* w, int E, int H, uint16_t* w3, cudaStream_t st);
 bool router_map_weights(CUtensorMap* m, const uint16_t* w3, int E, int H);
 cudaError_t launch_router_mma(const CUtensorMap& w3map, const uint16_t* x, int T, int E, int H,
                               float* part, int32_t* err, int num_sms, cudaStream_t st);
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
-                        cudaStream_t st);
+cudaError_t launch_topk(const float* logits, int T, int E, int k, const Scoring& sg, int32_t* idx,
+                        float* w, cudaStream_t st);
 cudaError_t launch_ffn_up_simt(const ExpertBank& bank, int T, int k, int n_shared,
                                const Workspace& ws, int num_sms, cudaStream_t st);
 cudaError_t launch_ffn_down_simt(const ExpertBank& bank, int T, int k, int n_shared,
@@ -158,8 +174,8 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
 constexpr int kPrepMaxTokens = 64;
 cudaError_t prepare_prep_kernel(int E, int H);
 cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, int bn,
-                        const float* W, const float* b, float* logits_out, int32_t* idx, float* w,
-                        bool route, const Workspace& ws, cudaStream_t st);
+                        const float* W, const float* b, const Scoring& sg, float* logits_out,
+                        int32_t* idx, float* w, bool route, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out,
                            cudaStream_t st);
 

@@ -42,6 +42,7 @@ struct PrepParams {
   int32_t* idx;          // [T][k] written (route) or read
   float* w;              // [T][k] written (route)
   int32_t* counters;     // [token blocks + 1], zero between launches
+  Scoring sg;            // how the weights follow from the logits
   Workspace ws;
 };
 
@@ -108,20 +109,21 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
     const int t0 = blockIdx.y * kPrepTT, nt = min(kPrepTT, p.T - t0);
     for (int i = threadIdx.x; i < nt * p.E; i += blockDim.x) {
       const int t = i / p.E, e = i - t * p.E;
-      const float f = router_sum_partials(p.part, p.ks, p.T, p.E, t0 + t, e, p.b);
+      // the bias is part of the logit for softmax scoring, of the selection key for sigmoid
+      const float f = router_sum_partials(p.part, p.ks, p.T, p.E, t0 + t, e, p.sg.sigmoid ? nullptr : p.b);
       lg[i] = f;
       if (p.logits_out) p.logits_out[(size_t)(t0 + t) * p.E + e] = f;
     }
     __syncthreads();
     if (warp < nt) {
-      float v[16];
+      float l[16], key[16], sc[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int e = lane + 32 * i;
-        const float f = e < p.E ? lg[warp * p.E + e] : -INFINITY;
-        v[i] = isnan(f) ? -INFINITY : f;
+        l[i] = e < p.E ? lg[warp * p.E + e] : -INFINITY;
       }
-      select_topk(v, t0 + warp, p.E, p.k, lane, p.idx, p.w);
+      topk_keys(l, p.E, lane, p.sg, key, sc);
+      select_topk(key, sc, t0 + warp, p.E, p.k, lane, p.sg, p.idx, p.w);
     }
   }
 
@@ -158,8 +160,8 @@ cudaError_t prepare_prep_kernel(int E, int H) {
 }
 
 cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, int bn,
-                        const float* W, const float* b, float* logits_out, int32_t* idx, float* w,
-                        bool route, const Workspace& ws, cudaStream_t st) {
+                        const float* W, const float* b, const Scoring& sg, float* logits_out,
+                        int32_t* idx, float* w, bool route, const Workspace& ws, cudaStream_t st) {
   if (T <= 0 || T > kPrepMaxTokens) return cudaErrorInvalidValue;
   PrepParams p;
   p.x = x;
@@ -178,6 +180,7 @@ cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, i
   p.idx = idx;
   p.w = w;
   p.counters = ws.prep_cnt;
+  p.sg = sg;
   p.ws = ws;
   dim3 grid;
   if (route) {

@@ -45,21 +45,21 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 
 // One warp per token; lane l holds logits l, l+32, ... (E <= 512).  k rounds
 // of a warp arg-max over (value desc, index asc); NaN counts as -infinity.
-__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k, Scoring sg,
                             int32_t* __restrict__ idx, float* __restrict__ w) {
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
-  float v[16];
+  float l[16], key[16], sc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int e = lane + 32 * i;
-    float f = e < E ? logits[(size_t)t * E + e] : -INFINITY;
-    v[i] = isnan(f) ? -INFINITY : f;
+    l[i] = e < E ? logits[(size_t)t * E + e] : -INFINITY;
   }
-  select_topk(v, t, E, k, lane, idx, w);
+  topk_keys(l, E, lane, sg, key, sc);
+  select_topk(key, sc, t, E, k, lane, sg, idx, w);
 }
 
 // Split-K variant for small T: warp = (expert, K chunk); partial sums go to
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 // logits (fixed ks order, plus bias) in parallel, then one warp selects.
 __global__ void __launch_bounds__(256) topk_sum_kernel(const float* __restrict__ part, int ksplit,
                                                        const float* __restrict__ b, int T, int E,
-                                                       int k, float* __restrict__ logits_out,
+                                                       int k, Scoring sg, float* __restrict__ logits_out,
                                                        int32_t* __restrict__ idx,
                                                        float* __restrict__ w) {
   pdl_wait();
@@ -101,21 +101,22 @@ __global__ void __launch_bounds__(256) topk_sum_kernel(const float* __restrict__
   __shared__ float lg[512];
   const int t = blockIdx.x;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const float f = router_sum_partials(part, ksplit, T, E, t, e, b);
+    // the bias is part of the logit for softmax scoring, of the selection key for sigmoid
+    const float f = router_sum_partials(part, ksplit, T, E, t, e, sg.sigmoid ? nullptr : b);
     lg[e] = f;
     if (logits_out) logits_out[(size_t)t * E + e] = f;
   }
   __syncthreads();
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
-  float v[16];
+  float l[16], key[16], sc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int e = lane + 32 * i;
-    const float f = e < E ? lg[e] : -INFINITY;
-    v[i] = isnan(f) ? -INFINITY : f;
+    l[i] = e < E ? lg[e] : -INFINITY;
   }
-  select_topk(v, t, E, k, lane, idx, w);
+  topk_keys(l, E, lane, sg, key, sc);
+  select_topk(key, sc, t, E, k, lane, sg, idx, w);
 }
 
 }  // namespace
@@ -128,8 +129,8 @@ int router_ksplit(int H) {
 }
 
 cudaError_t launch_router_split(const uint16_t* x, int T, int H, int E, int k, const float* W,
-                                const float* b, float* part, float* logits_out, int32_t* idx,
-                                float* w, cudaStream_t st) {
+                                const float* b, const Scoring& sg, float* part, float* logits_out,
+                                int32_t* idx, float* w, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const int ks = router_ksplit(H);
   const int gx = (E + kRouterWarps - 1) / kRouterWarps;
@@ -139,14 +140,15 @@ cudaError_t launch_router_split(const uint16_t* x, int T, int H, int E, int k, c
     { cudaError_t le_ = launch_pdl(router_partial_kernel<8>, dim3(dim3(gx, (T + 7) / 8, ks)), dim3(kRouterWarps * 32), 0, st, x, T, H, E, H / ks, W, part); if (le_ != cudaSuccess) return le_; }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  { cudaError_t le_ = launch_pdl(topk_sum_kernel, dim3(T), dim3(256), 0, st, part, ks, b, T, E, k, logits_out, idx, w); if (le_ != cudaSuccess) return le_; }
+  { cudaError_t le_ = launch_pdl(topk_sum_kernel, dim3(T), dim3(256), 0, st, part, ks, b, T, E, k, sg, logits_out, idx, w); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk_sum(const float* part, int ksplit, const float* b, int T, int E, int k,
-                            float* logits_out, int32_t* idx, float* w, cudaStream_t st) {
+                            const Scoring& sg, float* logits_out, int32_t* idx, float* w,
+                            cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  { cudaError_t le_ = launch_pdl(topk_sum_kernel, dim3(T), dim3(256), 0, st, part, ksplit, b, T, E, k, logits_out, idx, w); if (le_ != cudaSuccess) return le_; }
+  { cudaError_t le_ = launch_pdl(topk_sum_kernel, dim3(T), dim3(256), 0, st, part, ksplit, b, T, E, k, sg, logits_out, idx, w); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -165,10 +167,10 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const f
   return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
-                        cudaStream_t st) {
+cudaError_t launch_topk(const float* logits, int T, int E, int k, const Scoring& sg, int32_t* idx,
+                        float* w, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  { cudaError_t le_ = launch_pdl(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, logits, T, E, k, idx, w); if (le_ != cudaSuccess) return le_; }
+  { cudaError_t le_ = launch_pdl(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, logits, T, E, k, sg, idx, w); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 

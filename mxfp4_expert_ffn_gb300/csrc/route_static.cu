@@ -66,7 +66,7 @@ extern "C" moe_status moe_route_static(const void* x, int32_t T, int32_t H, int3
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   e = moe::launch_router_logits(static_cast<const uint16_t*>(x), T, H, E, router_w, router_b,
                                 scratch, 0, st);
-  if (e == cudaSuccess) e = moe::launch_topk(scratch, T, E, k, topk_idx, topk_w, st);
+  if (e == cudaSuccess) e = moe::launch_topk(scratch, T, E, k, moe::Scoring{0, 1.0f, nullptr}, topk_idx, topk_w, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;

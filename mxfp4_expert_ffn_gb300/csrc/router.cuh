@@ -10,8 +10,34 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "internal.h"
 
 namespace moe {
+
+// e^x in fp32 from IEEE operations only (Cody-Waite reduction by ln 2, a
+// degree-7 Taylor polynomial on |r| <= ln2/2, exact scaling by 2^n), so that any
+// implementation doing the same operations gets the same bits.  x is clamped
+// to [-87, 88]; error a few ulp.
+__device__ __forceinline__ float exp_poly_f32(float x) {
+  x = fminf(fmaxf(x, -87.0f), 88.0f);
+  const float n = rintf(__fmul_rn(x, 1.44269504f));
+  float r = __fmaf_rn(n, -0.693145752f, x);
+  r = __fmaf_rn(n, -1.42860677e-06f, r);
+  float q = 1.98412698e-04f;
+  q = __fmaf_rn(q, r, 1.38888889e-03f);
+  q = __fmaf_rn(q, r, 8.33333333e-03f);
+  q = __fmaf_rn(q, r, 4.16666667e-02f);
+  q = __fmaf_rn(q, r, 1.66666667e-01f);
+  q = __fmaf_rn(q, r, 0.5f);
+  q = __fmaf_rn(q, r, 1.0f);
+  q = __fmaf_rn(q, r, 1.0f);
+  return __fmul_rn(q, __int_as_float(((int)n + 127) << 23));
+}
+
+// sigmoid(l) = 1 / (1 + e^-l), correctly rounded add and divide.
+__device__ __forceinline__ float sigmoid_f32(float l) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_poly_f32(-l)));
+}
 
 // acc[i] += sum over h in [k0, k0 + kc) of W[h] * x_i[h] for one W_r row (fp32)
 // and nt <= TT bf16 tokens; lane l takes the float4 groups l, l + 32, ... in
@@ -65,25 +91,61 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
-// The k selected (value, expert) pairs in rank order -> idx[t][r] and
-// w[t][r] = exp(v_r - v_0) / sum_r' exp(v_r' - v_0), summed in rank order.
-__device__ __forceinline__ void topk_softmax_write(const float* sv, const int* si, int t, int k,
-                                                   int32_t* __restrict__ idx, float* __restrict__ w) {
+// The k selected experts in rank order -> idx[t][r] and their weights:
+// softmax: w_r = exp(v_r - v_0) / sum_r' exp(v_r' - v_0) with v the logits;
+// sigmoid: w_r = s_r / sum_r' s_r' with s the sigmoid scores; sums in rank
+// order; then times the routed scale.
+__device__ __forceinline__ void topk_weights_write(const float* sv, const float* ss, const int* si, int t,
+                                                   int k, const Scoring& sg, int32_t* __restrict__ idx,
+                                                   float* __restrict__ w) {
+  if (sg.sigmoid) {
+    float den = 0.f;
+    for (int r = 0; r < k; ++r) den = __fadd_rn(den, ss[r]);
+    for (int r = 0; r < k; ++r) {
+      idx[(size_t)t * k + r] = si[r];
+      w[(size_t)t * k + r] = __fmul_rn(__fdiv_rn(ss[r], den), sg.scale);
+    }
+    return;
+  }
   const float m = sv[0];
   float den = 0.f;
   for (int r = 0; r < k; ++r) den += expf(sv[r] - m);
   for (int r = 0; r < k; ++r) {
     idx[(size_t)t * k + r] = si[r];
-    w[(size_t)t * k + r] = expf(sv[r] - m) / den;
+    w[(size_t)t * k + r] = (expf(sv[r] - m) / den) * sg.scale;
+  }
+}
+
+// Per-lane selection keys and scores from the logits l[e] of one token held by
+// lane e % 32 (e = lane + 32 i): softmax keys are l (NaN as -infinity);
+// sigmoid keys are sigmoid(l) + bias (NaN as -infinity), scores sigmoid(l).
+__device__ __forceinline__ void topk_keys(const float (&l)[16], int E, int lane, const Scoring& sg,
+                                          float (&key)[16], float (&sc)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int e = lane + 32 * i;
+    float kv = -INFINITY, sv = 0.f;
+    if (e < E && !isnan(l[i])) {  // a NaN logit: key -infinity, score 0
+      if (sg.sigmoid) {
+        sv = sigmoid_f32(l[i]);
+        kv = __fadd_rn(sv, sg.sel_bias ? sg.sel_bias[e] : 0.f);
+        if (isnan(kv)) kv = -INFINITY;
+      } else {
+        kv = sv = l[i];
+      }
+    }
+    key[i] = kv;
+    sc[i] = sv;
   }
 }
 
 // k rounds of a warp arg-max over (value desc, index asc) on the 16 values
 // per lane (v[i] is expert lane + 32 i), then the softmax over the k chosen.
-__device__ __forceinline__ void select_topk(const float (&v)[16], int t, int E, int k, int lane,
-                                            int32_t* __restrict__ idx, float* __restrict__ w) {
+__device__ __forceinline__ void select_topk(const float (&v)[16], const float (&sc)[16], int t, int E, int k,
+                                            int lane, const Scoring& sg, int32_t* __restrict__ idx,
+                                            float* __restrict__ w) {
   uint32_t taken = 0;
-  float sv[8];
+  float sv[8], ss[8];
   int si[8];
   for (int r = 0; r < k; ++r) {
     float bv = -INFINITY;
@@ -106,10 +168,15 @@ __device__ __forceinline__ void select_topk(const float (&v)[16], int t, int E, 
       }
     }
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    float mine = 0.f;  // the winner's score, from the lane that holds it
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (i == (bi >> 5)) mine = sc[i];
     sv[r] = bv;
+    ss[r] = __shfl_sync(0xFFFFFFFFu, mine, bi & 31);
     si[r] = bi;
   }
-  if (lane == 0) topk_softmax_write(sv, si, t, k, idx, w);
+  if (lane == 0) topk_weights_write(sv, ss, si, t, k, sg, idx, w);
 }
 
 }  // namespace moe

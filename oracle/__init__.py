@@ -23,7 +23,7 @@ def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so with gcc (OpenMP, no -march flags)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
@@ -59,6 +59,11 @@ def _declare(L):
     L.orc_quantize_act.argtypes = [P, C.c_int, C.c_int, P, P]
     L.orc_router_logits.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P, P, C.c_int]
     L.orc_topk.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
+    L.orc_exp_f32.restype = C.c_float
+    L.orc_exp_f32.argtypes = [C.c_float]
+    L.orc_sigmoid_f32.restype = C.c_float
+    L.orc_sigmoid_f32.argtypes = [C.c_float]
+    L.orc_topk_sigmoid.argtypes = [P, P, C.c_int, C.c_int, C.c_int, C.c_double, P, P]
     L.orc_segments.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
     L.orc_expert_ffn.restype = C.c_int
     L.orc_expert_ffn.argtypes = [P, C.c_int, C.c_int, P, P, P, P, P, P]
@@ -145,6 +150,23 @@ def topk(logits, k: int) -> tuple[np.ndarray, np.ndarray]:
     idx = np.zeros((T, k), np.int32)
     w = np.zeros((T, k), np.float64)
     lib().orc_topk(_p(lg), T, E, k, _p(idx), _p(w))
+    return idx, w
+
+
+def sigmoid_f32(logits) -> np.ndarray:
+    """The oracle's fp32 sigmoid (fixed sequence of fp32 operations)."""
+    lg = _c(logits, np.float32).ravel()
+    return np.array([lib().orc_sigmoid_f32(float(v)) for v in lg], np.float32).reshape(np.shape(logits))
+
+
+def topk_sigmoid(logits, bias, k: int, scale: float = 1.0) -> tuple[np.ndarray, np.ndarray]:
+    """Sigmoid scoring: selection on fp32 sigmoid(l) + bias, weights s / sum(s) * scale."""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    bb = None if bias is None else _c(bias, np.float32)
+    idx = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    lib().orc_topk_sigmoid(_p(lg), None if bb is None else _p(bb), T, E, k, C.c_double(scale), _p(idx), _p(w))
     return idx, w
 
 

@@ -209,6 +209,72 @@ void orc_topk(const float* logits, int T, int E, int k, int32_t* idx, double* w)
   free(a);
 }
 
+/* --------------------------------------------------------- sigmoid scoring */
+
+/* A second router scoring (DeepSeek-V3 style; the pages never name the score
+ * function, see the readings): s = sigmoid(l) of the unbiased logit, the bias
+ * added to s for the selection only, weights s / (sum of the k selected s),
+ * times a routed scaling factor.  Which experts are selected is decided in
+ * fp32, the precision the layer computes it in, so sigmoid here is a fixed
+ * sequence of correctly rounded fp32 operations: e^x by Cody and Waite's
+ * reduction x = n ln2 + r (n = round-half-even(x log2 e), ln 2 split into
+ * 0.693145752 + 1.42860677e-6 so that n * 0.693145752 is exact), e^r by its
+ * degree-7 Taylor polynomial in Horner form with fused multiply-adds
+ * (truncation below 6e-9 relative on |r| <= ln2/2), then times 2^n; x is first
+ * clamped to [-87, 88].  Compiled without floating-point contraction. */
+float orc_exp_f32(float x) {
+  x = fminf(fmaxf(x, -87.0f), 88.0f);
+  const float n = rintf(x * 1.44269504f);
+  float r = fmaf(n, -0.693145752f, x);
+  r = fmaf(n, -1.42860677e-06f, r);
+  float q = 1.98412698e-04f;  /* 1/7! */
+  q = fmaf(q, r, 1.38888889e-03f);  /* 1/6! */
+  q = fmaf(q, r, 8.33333333e-03f);  /* 1/5! */
+  q = fmaf(q, r, 4.16666667e-02f);  /* 1/4! */
+  q = fmaf(q, r, 1.66666667e-01f);  /* 1/3! */
+  q = fmaf(q, r, 0.5f);
+  q = fmaf(q, r, 1.0f);
+  q = fmaf(q, r, 1.0f);
+  const uint32_t bits = (uint32_t)((int)n + 127) << 23;
+  float p2;
+  memcpy(&p2, &bits, sizeof p2);
+  return q * p2;
+}
+
+float orc_sigmoid_f32(float l) { return 1.0f / (1.0f + orc_exp_f32(-l)); }
+
+/* Sigmoid top-k: key_e = fp32(s_e + bias_e) (NaN logits: key -infinity,
+ * s = 0), selection by (key desc, index asc) with a full sort, weights in
+ * fp64: w_j = s_j / sum_j' s_j' * scale, j in rank order. */
+void orc_topk_sigmoid(const float* logits, const float* bias, int T, int E, int k, double scale,
+                      int32_t* idx, double* w) {
+  orc_scored* a = (orc_scored*)malloc(sizeof(orc_scored) * (size_t)E);
+  float* sc = (float*)malloc(sizeof(float) * (size_t)E);
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      const float l = logits[(size_t)t * E + e];
+      if (isnan(l)) {
+        sc[e] = 0.0f;
+        a[e].key = -INFINITY;
+      } else {
+        sc[e] = orc_sigmoid_f32(l);
+        const float key = sc[e] + (bias ? bias[e] : 0.0f);
+        a[e].key = isnan(key) ? -INFINITY : (double)key;
+      }
+      a[e].index = e;
+    }
+    qsort(a, (size_t)E, sizeof(orc_scored), orc_rank_cmp);
+    double den = 0.0;
+    for (int j = 0; j < k; ++j) den += (double)sc[a[j].index];
+    for (int j = 0; j < k; ++j) {
+      idx[(size_t)t * k + j] = a[j].index;
+      w[(size_t)t * k + j] = (double)sc[a[j].index] / den * scale;
+    }
+  }
+  free(sc);
+  free(a);
+}
+
 /* Expert segments of the T*k slots (slot s = t*k + j): off[e] = number of
  * slots routed to experts below e (off[E] = T*k); perm lists the slots
  * expert by expert, each expert's slots in increasing slot order. */

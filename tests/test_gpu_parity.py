@@ -318,6 +318,69 @@ def test_step_equals_route_then_forward_and_matches_oracle(wl, path):
     L.close()
 
 
+# ---- sigmoid scoring with a selection-only bias and a routed scaling factor
+
+SIG_ZIPF = Workload("sig_h512_i256_e64_k6_t20_zipf", 512, 256, 64, 6, 1, 20, seed=26, zipf=1.1,
+                    scale_lo=-8, scale_hi=-4)
+
+@pytest.mark.parametrize("wl", [SMALL[2], SIG_ZIPF, STEP[-1]], ids=lambda w: w.name)
+def test_sigmoid_scoring_bit_exact_given_logits(wl):
+    L, _ = gu.make_layer(wl)
+    L.set_scoring(m.MOE_SCORING_SIGMOID, 2.5)
+    x = _x(wl)
+    lg = oracle.router_logits(x, synth.router_weights(wl), None)   # unbiased logits
+    lg[0, 3] = np.nan
+    lg[1, :] = lg[1, 0]                                            # ties before the bias
+    b = synth.router_bias(wl)
+    b = np.zeros(wl.n_experts, np.float32) if b is None else b
+    ridx, rw = oracle.topk_sigmoid(lg, b, wl.top_k, 2.5)
+    idx, w, lo = gu.run_route(L, x, wl.tokens, wl.n_experts, wl.top_k, logits_in=lg)
+    assert np.array_equal(idx, ridx)
+    assert np.allclose(w, rw, rtol=1e-6, atol=0)
+    L.close()
+
+
+@pytest.mark.parametrize("wl", [SMALL[1], SIG_ZIPF, STEP[-1]], ids=lambda w: w.name)
+@pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_SIMT])
+def test_sigmoid_scoring_layer_matches_oracle(wl, path):
+    """The GPU's own (unbiased) logits, sigmoid selection reproduced by the oracle
+    bit for bit, the layer within tolerance; moe_step equals route + forward."""
+    L, _ = gu.make_layer(wl)
+    L.set_option(m.MOE_OPT_PATH, path)
+    L.set_scoring(m.MOE_SCORING_SIGMOID, 2.5)
+    x = _x(wl)
+    T, E, k = wl.tokens, wl.n_experts, wl.top_k
+    xt = sg.bf16_tensor(x)
+    y = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=gu.DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=gu.DEV)
+    lo = torch.empty((T, E), dtype=torch.float32, device=gu.DEV)
+    L.step(xt, T, y, idx=idx, w=w, logits_out=lo)
+    assert L.sync() == m.MOE_OK
+    y, idx, w, lo = (y.cpu().numpy().view(np.uint16), idx.cpu().numpy(), w.cpu().numpy(), lo.cpu().numpy())
+    ref_lo = oracle.router_logits(x, synth.router_weights(wl), None)
+    assert (np.abs(lo - ref_lo) <= 1e-5 * (1 + np.abs(ref_lo))).all()
+    b = synth.router_bias(wl)
+    ridx, rw = oracle.topk_sigmoid(lo, b, k, 2.5)
+    assert np.array_equal(idx, ridx)
+    assert np.allclose(w, rw, rtol=1e-6, atol=0)
+    idx2, w2, lo2 = gu.run_route(L, x, T, E, k)
+    assert np.array_equal(lo2, lo) and np.array_equal(idx2, idx) and np.array_equal(w2, w)
+    assert np.array_equal(gu.run_forward(L, x, idx2, w2), y)
+    gu.assert_y_close(y, gu.oracle_layer(wl, 0, x, ridx, rw))
+    L.close()
+
+
+def test_scoring_options_are_validated():
+    L, _ = gu.make_layer(TINY)
+    for opt, val in ((m.MOE_OPT_SCORING, 2), (m.MOE_OPT_ROUTED_SCALE, 0x7FC00000),
+                     (m.MOE_OPT_ROUTED_SCALE, 0xBF800000), (m.MOE_OPT_ROUTED_SCALE, 0)):
+        with pytest.raises(m.MoeError) as e:
+            L.set_option(opt, val)
+        assert e.value.status == m.MOE_ERR_INVALID_ARG
+    L.close()
+
+
 def test_rmsnorm_matches_oracle():
     rng = np.random.default_rng(8)
     x = synth.f32_to_bf16_bits((rng.standard_normal((33, 5120)) * 200).astype(np.float32))

@@ -187,6 +187,72 @@ def test_combine_weights_renormalised_softmax():
     assert np.allclose(w, sel / sel.sum(axis=1, keepdims=True), rtol=1e-13, atol=0)
 
 
+# ---- sigmoid scoring (selection on fp32 sigmoid(l) + bias, weights s / sum s * scale)
+
+def test_sigmoid_f32_within_3_ulp_of_fp64_and_monotonic():
+    l = np.linspace(-80, 80, 200001).astype(np.float32)
+    s = oracle.sigmoid_f32(l).astype(np.float64)
+    ref = 1.0 / (1.0 + np.exp(-l.astype(np.float64)))
+    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert (np.abs(s - ref) / ulp).max() <= 3.0
+    assert np.all(np.diff(s) >= 0)
+    assert oracle.sigmoid_f32(np.float32([0.0]))[0] == 0.5
+    assert oracle.sigmoid_f32(np.float32([30.0]))[0] == 1.0
+
+
+def _brute_sigmoid(l, b, k, scale):
+    s = oracle.sigmoid_f32(l)
+    key = (s + b).astype(np.float32)
+    order = sorted(range(len(l)), key=lambda e: (-(-math.inf if math.isnan(l[e]) or math.isnan(key[e])
+                                                   else float(key[e])), e))
+    sel = order[:k]
+    sv = np.array([0.0 if math.isnan(l[e]) else float(s[e]) for e in sel])
+    return sel, sv / sv.sum() * scale
+
+
+@pytest.mark.parametrize("E,k", [(16, 2), (384, 6)])
+def test_topk_sigmoid_matches_brute_force(E, k):
+    rng = np.random.default_rng(100 + E)
+    T = 32
+    lg = (rng.standard_normal((T, E)) * 1.4).astype(np.float32)
+    b = (rng.standard_normal(E) * 0.05).astype(np.float32)
+    lg[1, :] = 0.25                                   # all tied before the bias
+    lg[2, : E // 2] = np.nan                          # NaN logits rank last
+    lg[3, :] = np.round(lg[3, :] * 2) / 2
+    idx, w = oracle.topk_sigmoid(lg, b, k, 2.5)
+    for t in range(T):
+        sel, ww = _brute_sigmoid(lg[t], b, k, 2.5)
+        assert idx[t].tolist() == sel, t
+        assert np.allclose(w[t], ww, rtol=1e-12, atol=0), t
+    assert np.allclose(w.sum(axis=1), 2.5, rtol=1e-12)
+
+
+def test_topk_sigmoid_without_bias_selects_like_the_logits():
+    # sigmoid is increasing: with no bias and no saturation ties the selection
+    # is the logits' top-k (the softmax scoring's selection)
+    rng = np.random.default_rng(7)
+    lg = (rng.standard_normal((64, 384)) * 1.4).astype(np.float32)
+    idx_s, _ = oracle.topk_sigmoid(lg, None, 6, 1.0)
+    idx_l, _ = oracle.topk(lg, 6)
+    s = oracle.sigmoid_f32(lg)
+    for t in range(64):
+        if len(np.unique(s[t])) == len(np.unique(lg[t])):
+            assert idx_s[t].tolist() == idx_l[t].tolist(), t
+
+
+def test_topk_sigmoid_bias_selects_but_does_not_weight():
+    rng = np.random.default_rng(8)
+    lg = (rng.standard_normal((4, 64)) * 1.4).astype(np.float32)
+    b = np.zeros(64, np.float32)
+    b[37] = 10.0                                      # forces expert 37 into first place
+    idx, w = oracle.topk_sigmoid(lg, b, 4, 1.0)
+    s = oracle.sigmoid_f32(lg).astype(np.float64)
+    for t in range(4):
+        assert idx[t, 0] == 37
+        sel = s[t, idx[t]]
+        assert np.allclose(w[t], sel / sel.sum(), rtol=1e-12)   # the bias is not in the weights
+
+
 def test_router_logits_match_numpy_matmul():
     wl = TINY
     x = synth.activations(wl, tokens=16)
