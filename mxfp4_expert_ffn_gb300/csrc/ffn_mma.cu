@@ -211,6 +211,13 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// h = silu(g) * u = g / (1 + e^-g) * u with the SFU exponential and the fast
+// divide: a few ulp from the correctly rounded form, far inside the FP8
+// rounding of h that follows (one E4M3 step is 2^-3 relative).
+__device__ __forceinline__ float swiglu(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
                                             int32_t c2, uint64_t* bar) {
   asm volatile(
@@ -540,10 +547,45 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       if (MODE == kModeDown) {
         p.o[pos * p.out_cols + row] = a;
       } else {
-        const float h = a / (1.0f + expf(-a)) * b;
+        const float h = swiglu(a, b);
         const int ex = fp8_block_exponent(warp_max(fabsf(h)));
         p.hq[pos * p.out_cols + row] = (uint8_t)(e4m3x2(scale_pow2_neg(h, ex), 0.f) & 0xFFu);
         if (lane == 0) p.hs[pos * (p.out_cols / 32) + (un.row0 + 32 * q) / 32] = (uint8_t)(ex + 127);
+      }
+    };
+    // Sixteen columns at once (the main path): the SwiGLU values of all of them
+    // first, then the sixteen 32-row maxima as interleaved shuffle trees, so
+    // the shuffle latency is paid once per group rather than once per column.
+    // Same operations per column as emit(), so the same bits.
+    auto emit16 = [&](const Unit& un, int c, const uint32_t (&v)[16], const uint32_t (&vu)[16]) {
+      const int row = un.row0 + rl;
+      if constexpr (MODE == kModeDown) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (c + j >= un.m_tile) break;  // warp-uniform
+          const float a = C::kSplitK ? __uint_as_float(v[j]) + __uint_as_float(vu[j]) : __uint_as_float(v[j]);
+          p.o[(size_t)(un.pos0 + c + j) * p.out_cols + row] = a;
+        }
+      } else {
+        float h[16], am[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float g = __uint_as_float(v[j]);
+          h[j] = swiglu(g, __uint_as_float(vu[j]));
+          am[j] = fabsf(h[j]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) am[j] = fmaxf(am[j], __shfl_xor_sync(0xFFFFFFFFu, am[j], o));
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (c + j >= un.m_tile) break;  // warp-uniform
+          const size_t pos = (size_t)(un.pos0 + c + j);
+          const int ex = fp8_block_exponent(am[j]);
+          p.hq[pos * p.out_cols + row] = (uint8_t)(e4m3x2(scale_pow2_neg(h[j], ex), 0.f) & 0xFFu);
+          if (lane == 0) p.hs[pos * (p.out_cols / 32) + (un.row0 + 32 * q) / 32] = (uint8_t)(ex + 127);
+        }
       }
     };
     // Down mode with the combine fused (small batches): after a warp has
@@ -631,14 +673,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce_bar[buf]);
           }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c + j >= un.m_tile) break;  // warp-uniform
-            if constexpr (C::kSplitK)  // the two K halves, in fixed order
-              emit(un, c + j, __uint_as_float(v[j]) + __uint_as_float(vu[j]), 0.f);
-            else
-              emit(un, c + j, __uint_as_float(v[j]), MODE == kModeUp ? __uint_as_float(vu[j]) : 0.f);
-          }
+          if (c < un.m_tile) emit16(un, c, v, vu);  // down split-K: the two K halves, in fixed order
         }
         combine_tail(un);
         continue;

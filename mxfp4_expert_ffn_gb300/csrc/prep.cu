@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
 }
 
 size_t prep_smem_bytes(int E, int H) {
-  const size_t seg = (size_t)33 * E * sizeof(int32_t), lg = (size_t)kPrepTT * E * sizeof(float);
+  const size_t seg = (size_t)(36 * E + 2 * 4 + 1) * sizeof(int32_t), lg = (size_t)kPrepTT * E * sizeof(float);
   const size_t xs = (size_t)kPrepTT * H * sizeof(uint16_t);  // bound for one K chunk of x
   const size_t small = (size_t)(4 * E + 2 * 4 + 1024 + 1) * sizeof(int32_t);  // segments_small_cta
   size_t m = seg > lg ? seg : lg;

@@ -28,7 +28,8 @@ __global__ void quantize_act_kernel(const uint4* __restrict__ x, int n8, uint2* 
 }
 
 // Same quantisation, written once per position (row p of xg is token
-// pos_tok[p]), so that each expert's activation rows are contiguous.
+// pos_tok[p]), so that each expert's activation rows are contiguous.  One CTA
+// per position row (grid-strided), threads over the row's 8-value groups.
 __global__ void quantize_gather_kernel(const uint16_t* __restrict__ x, int P, int H,
                                        const int32_t* __restrict__ pos_tok, uint2* __restrict__ xg,
                                        uint8_t* __restrict__ xgs) {
@@ -36,25 +37,27 @@ __global__ void quantize_gather_kernel(const uint16_t* __restrict__ x, int P, in
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   const unsigned quad = 0xFu << (lane & ~3);
-  const int per_row = H / 8;
-  const long long n8 = (long long)P * per_row;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int p = (int)(i / per_row), j = (int)(i - (long long)p * per_row);
-    const uint4 v = reinterpret_cast<const uint4*>(x + (size_t)pos_tok[p] * H)[j];
-    int e;
-    xg[i] = quant8(v, quad, &e);
-    if ((lane & 3) == 0) xgs[i >> 2] = (uint8_t)(e + 127);
+  const int per_row = H / 8;  // a multiple of 16: whole quads stay in or out
+  for (int p = blockIdx.x; p < P; p += gridDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)pos_tok[p] * H);
+    uint2* dst = xg + (size_t)p * per_row;
+    uint8_t* dsts = xgs + (size_t)p * (H / 32);
+    for (int j = threadIdx.x; j < per_row; j += blockDim.x) {
+      int e;
+      dst[j] = quant8(src[j], quad, &e);
+      if ((lane & 3) == 0) dsts[j >> 2] = (uint8_t)(e + 127);
+    }
   }
 }
 
 // Expert segments in one CTA of 1024 threads (segments.cuh).
 __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restrict__ idx, int T,
-                                                        int k, int E, int ns, int bn, Workspace ws) {
+                                                        int k, int E, int ns, int bn, Workspace ws,
+                                                        int stage_idx) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ int32_t sm[];
-  segments_cta(idx, T, k, E, ns, bn, ws, sm);
+  segments_cta(idx, T, k, E, ns, bn, ws, sm, stage_idx != 0);
 }
 
 // y[t] = bf16( sum_s o[S + s*T + t] + sum_j w[t][j] * o[slot_pos[t*k + j]] ),
@@ -161,27 +164,29 @@ cudaError_t launch_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uin
   return cudaGetLastError();
 }
 
-size_t segments_smem_bytes(int E) { return (size_t)(33 * E) * sizeof(int32_t); }
+size_t segments_smem_bytes(int E) { return (size_t)(36 * E + 2 * 4 + 1) * sizeof(int32_t); }
+constexpr size_t kSegmentsSmemMax = 200 * 1024;  // room for the staged ids of up to ~30k slots
 
 cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared, int bn,
                             const Workspace& ws, cudaStream_t st) {
-  { cudaError_t le_ = launch_pdl(segments_kernel, dim3(1), dim3(1024), segments_smem_bytes(E), st, idx, T, k, E, n_shared, bn, ws); if (le_ != cudaSuccess) return le_; }
+  const size_t base = segments_smem_bytes(E), staged = base + (size_t)T * k * sizeof(int32_t);
+  const bool stage = staged <= kSegmentsSmemMax;
+  { cudaError_t le_ = launch_pdl(segments_kernel, dim3(1), dim3(1024), stage ? staged : base, st, idx, T, k, E, n_shared, bn, ws, stage ? 1 : 0); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_gather(const uint16_t* x, int P, int H, const int32_t* pos_tok,
                                    uint8_t* xg, uint8_t* xgs, cudaStream_t st) {
-  const long long n8 = (long long)P * (H / 8);
-  if (n8 == 0) return cudaSuccess;
-  long long blocks = (n8 + 255) / 256;
-  if (blocks > 8192) blocks = 8192;
-  { cudaError_t le_ = launch_pdl(quantize_gather_kernel, dim3((int)blocks), dim3(256), 0, st, x, P, H, pos_tok, reinterpret_cast<uint2*>(xg), xgs); if (le_ != cudaSuccess) return le_; }
+  if (P == 0) return cudaSuccess;
+  const int blocks = P < 65536 ? P : 65536;
+  { cudaError_t le_ = launch_pdl(quantize_gather_kernel, dim3(blocks), dim3(256), 0, st, x, P, H, pos_tok, reinterpret_cast<uint2*>(xg), xgs); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
 cudaError_t prepare_segments_kernel(int E) {
+  const size_t b = segments_smem_bytes(E);
   return cudaFuncSetAttribute(segments_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)segments_smem_bytes(E));
+                              (int)(b > kSegmentsSmemMax ? b : kSegmentsSmemMax));
 }
 
 cudaError_t launch_combine(const Workspace& ws, int T, int H, int k, int n_shared, const float* w,

@@ -168,13 +168,15 @@ __device__ __forceinline__ void select_topk(const float (&v)[16], const float (&
       }
     }
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    float mine = 0.f;  // the winner's score, from the lane that holds it
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i == (bi >> 5)) mine = sc[i];
     sv[r] = bv;
-    ss[r] = __shfl_sync(0xFFFFFFFFu, mine, bi & 31);
     si[r] = bi;
+    if (sg.sigmoid) {  // the winner's score, from the lane that holds it
+      float mine = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (i == (bi >> 5)) mine = sc[i];
+      ss[r] = __shfl_sync(0xFFFFFFFFu, mine, bi & 31);
+    }
   }
   if (lane == 0) topk_weights_write(sv, ss, si, t, k, sg, idx, w);
 }

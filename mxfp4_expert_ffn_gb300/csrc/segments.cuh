@@ -9,179 +9,16 @@
 
 namespace moe {
 
-// Builds the expert segments in one CTA of 1024 threads.  Each warp owns a
-// contiguous range of slots; pass 1 counts its slots per expert, pass 2 turns
-// the counts into per-warp bases (warps in slot order), pass 3 places each
-// slot at base + rank among the warp's equal-expert lanes.  The result is a
-// stable counting sort, identical on every run.
-// Needs blockDim.x == 1024 and sm = 33 * E ints of shared memory; every
-// thread of the CTA must call it.
-__device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx, int T, int k, int E,
-                                             int ns, int bn, const Workspace& ws, int32_t* sm) {
-  const int NE = E + ns;
-  int32_t* wcnt = sm;            // [32][E]  per-warp counts, then running bases
-  int32_t* stot = sm + 32 * E;   // [E]      totals, then exclusive offsets
-  __shared__ int routed_total;
-  const int S = T * k;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
-  // the tensor-core GEMM's split-partition counters start every forward at zero
-  for (int i = threadIdx.x; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
-  // and so do the fused-combine counters
-  for (int i = threadIdx.x; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
-  __syncthreads();
-  const int per = (S + 31) / 32;
-  const int lo = min(S, warp * per), hi = min(S, lo + per);
-  for (int b = lo; b < hi; b += 32) {
-    const int s = b + lane;
-    int e = -1;
-    if (s < hi) {
-      e = idx[s];
-      if (e < 0 || e >= E) {
-        raise_error(ws.err, kErrExpertRange);
-        e = -1;
-      }
-    }
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
-    __syncwarp();
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int w = 0; w < 32; ++w) {
-      const int c = wcnt[w * E + e];
-      wcnt[w * E + e] = run;
-      run += c;
-    }
-    stot[e] = run;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // exclusive scan of the E totals and of the "has tokens" flags
-    const int chunk = (E + 31) / 32;
-    const int c0 = min(E, lane * chunk), c1 = min(E, c0 + chunk);
-    // (and of the token tiles of width bn, for the tensor-core path)
-    const int tb = bn > 0 ? bn : 1;
-    int sum = 0, nf = 0, nt = 0;
-    for (int e = c0; e < c1; ++e) {
-      sum += stot[e];
-      nf += stot[e] > 0;
-      nt += (stot[e] + tb - 1) / tb;
-    }
-    int isum = sum, inf = nf, intl = nt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xFFFFFFFFu, isum, o);
-      const int f = __shfl_up_sync(0xFFFFFFFFu, inf, o);
-      const int t = __shfl_up_sync(0xFFFFFFFFu, intl, o);
-      if (lane >= o) {
-        isum += a;
-        inf += f;
-        intl += t;
-      }
-    }
-    int run = isum - sum, fr = inf - nf, tr = intl - nt;
-    for (int e = c0; e < c1; ++e) {
-      const int c = stot[e];
-      ws.cnt[e] = c;
-      ws.off[e] = run;
-      stot[e] = run;
-      if (c > 0) {
-        ws.tile_prefix[fr] = tr;
-        ws.active[fr++] = e;
-        tr += (c + tb - 1) / tb;
-      }
-      run += c;
-    }
-    const int n_routed_active = __shfl_sync(0xFFFFFFFFu, inf, 31);
-    const int routed_tiles = __shfl_sync(0xFFFFFFFFu, intl, 31);
-    const int valid = __shfl_sync(0xFFFFFFFFu, isum, 31);
-    if (lane == 0) {
-      routed_total = valid;
-      int tiles = routed_tiles;
-      for (int sh = 0; sh < ns; ++sh) {
-        ws.cnt[E + sh] = T;
-        ws.off[E + sh] = S + sh * T;
-        if (T > 0) {
-          ws.active[n_routed_active + sh] = E + sh;
-          ws.tile_prefix[n_routed_active + sh] = tiles;
-          tiles += (T + tb - 1) / tb;
-        }
-      }
-      ws.off[NE] = S + ns * T;
-      *ws.n_active = n_routed_active + (T > 0 ? ns : 0);
-      ws.n_active[1] = tiles;
-      ws.tile_prefix[n_routed_active + (T > 0 ? ns : 0)] = tiles;
-    }
-  }
-  __syncthreads();
-  for (int b = lo; b < hi; b += 32) {
-    const int s = b + lane;
-    int e = -1;
-    if (s < hi) {
-      e = idx[s];
-      if (e < 0 || e >= E) e = -1;
-    }
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-    if (e >= 0) {
-      const int p = stot[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
-      ws.perm[p] = s;
-      ws.slot_pos[s] = p;
-      ws.pos_tok[p] = s / k;
-    } else if (s < hi) {
-      ws.slot_pos[s] = -1;
-    }
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
-    __syncwarp();
-  }
-  for (int i = threadIdx.x; i < ns * T; i += blockDim.x) ws.pos_tok[S + i] = i % T;
-  // token tiles of width bn for the tensor-core path: (expert, first position, tokens)
-  if (bn > 0) {
-    const int na = *ws.n_active;
-    for (int a = threadIdx.x; a < na; a += blockDim.x) {
-      const int e = ws.active[a], c = ws.cnt[e], p0 = ws.off[e], t0 = ws.tile_prefix[a];
-      for (int j = 0; j * bn < c; ++j)
-        ws.tile_info[t0 + j] = make_int4(e, p0 + j * bn, min(bn, c - j * bn), 0);
-    }
-  }
-  // positions left free by invalid expert ids still name a real token, so
-  // that every position's row can be read safely
-  for (int p = routed_total + threadIdx.x; p < S; p += blockDim.x) ws.pos_tok[p] = 0;
-}
-
-
-// The same segments for a small batch (T * k <= blockDim.x == 1024, E <= 1024),
-// with every intermediate in shared memory: one thread per slot, counts by
-// shared atomics, the rank of a slot among its expert's slots by counting
-// the earlier equal slots (so the order is the stable one above, bit for bit).
-// sm needs 4 * E + 2 * ns + T * k + 1 ints.
-__device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ idx, int T, int k, int E,
-                                                   int ns, int bn, const Workspace& ws, int32_t* sm) {
-  const int NE = E + ns, S = T * k, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  int32_t* cnt_s = sm;             // [E]     slots per expert
-  int32_t* off_s = sm + E;         // [E]     first position per expert
-  int32_t* act_s = sm + 2 * E;     // [NE]    active experts, routed then shared
-  int32_t* tp_s = sm + 2 * E + NE; // [NE+1]  token tiles before each active expert
-  int32_t* sid = tp_s + NE + 1;    // [S]     expert of each slot (-1: invalid)
-  __shared__ int n_act_s, routed_total_s;
-  for (int i = tid; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
-  for (int i = tid; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
-  for (int e = tid; e < E; e += blockDim.x) cnt_s[e] = 0;
-  __syncthreads();
-  int e = -1;
-  if (tid < S) {
-    e = idx[tid];
-    if (e < 0 || e >= E) {
-      raise_error(ws.err, kErrExpertRange);
-      e = -1;
-    }
-    sid[tid] = e;
-    if (e >= 0) atomicAdd(&cnt_s[e], 1);
-  }
-  __syncthreads();
+// Block-wide exclusive scans over the experts (thread e for expert e; needs
+// blockDim.x == 1024 >= E) of the per-expert slot counts cnt_s[e], of the
+// "has slots" flags and of the token tiles of width bn: writes ws.cnt/off, the
+// first position off_s[e], the active list act_s (routed experts in order,
+// then the shared ones) with tile prefixes tp_s[0..na], n_active and the
+// routed slot total.  Ends with a barrier.
+__device__ __forceinline__ void scan_experts(const int32_t* cnt_s, int E, int T, int S, int ns, int bn,
+                                             const Workspace& ws, int32_t* off_s, int32_t* act_s,
+                                             int32_t* tp_s, int* n_act_s, int* routed_total_s) {
+  const int NE = E + ns, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   {
     // block-wide exclusive scans over the experts (one thread each) of the counts,
     // of the "has slots" flags and of the token tiles
@@ -240,7 +77,7 @@ __device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ i
     if (tid == 0) {
       const int n_routed_active = wsum[31][1];
       int tiles = wsum[31][2];
-      routed_total_s = wsum[31][0];
+      *routed_total_s = wsum[31][0];
       for (int sh = 0; sh < ns; ++sh) {
         ws.cnt[E + sh] = T;
         ws.off[E + sh] = S + sh * T;
@@ -252,13 +89,147 @@ __device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ i
       }
       ws.off[NE] = S + ns * T;
       const int na = n_routed_active + (T > 0 ? ns : 0);
-      n_act_s = na;
+      *n_act_s = na;
       *ws.n_active = na;
       ws.n_active[1] = tiles;
       tp_s[na] = tiles;
     }
   }
   __syncthreads();
+}
+
+// Builds the expert segments in one CTA of 1024 threads.  Each warp owns a
+// contiguous range of slots; pass 1 counts its slots per expert, pass 2 turns
+// the counts into per-warp bases (warps in slot order), pass 3 places each
+// slot at base + rank among the warp's equal-expert lanes.  The result is a
+// stable counting sort, identical on every run.
+// Needs blockDim.x == 1024 and sm = 36 * E + 2 * ns + 1 ints of shared memory; every
+// thread of the CTA must call it.
+__device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx_g, int T, int k, int E,
+                                             int ns, int bn, const Workspace& ws, int32_t* sm,
+                                             bool stage_idx = false) {
+  const int NE = E + ns;
+  int32_t* wcnt = sm;                  // [32][E] per-warp counts, then running bases
+  int32_t* stot = sm + 32 * E;         // [E]     slots per expert
+  int32_t* off_s = stot + E;           // [E]     first position per expert
+  int32_t* act_s = off_s + E;          // [NE]    active experts
+  int32_t* tp_s = act_s + NE;          // [NE+1]  token tiles before each active expert
+  __shared__ int n_act_s, routed_total_s;
+  const int S = T * k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+  // the tensor-core GEMM's split-partition counters start every forward at zero
+  for (int i = threadIdx.x; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
+  // and so do the fused-combine counters
+  for (int i = threadIdx.x; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
+  // with room, the slots' expert ids are staged in shared memory by one
+  // coalesced pass, so the two per-warp passes below never wait on global loads
+  const int32_t* idx = idx_g;
+  if (stage_idx) {
+    int32_t* sidx = tp_s + NE + 1;  // [S]
+    for (int i = threadIdx.x; i < S; i += blockDim.x) sidx[i] = idx_g[i];
+    idx = sidx;
+  }
+  __syncthreads();
+  const int per = (S + 31) / 32;
+  const int lo = min(S, warp * per), hi = min(S, lo + per);
+  for (int b = lo; b < hi; b += 32) {
+    const int s = b + lane;
+    int e = -1;
+    if (s < hi) {
+      e = idx[s];
+      if (e < 0 || e >= E) {
+        raise_error(ws.err, kErrExpertRange);
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+    stot[e] = run;
+  }
+  __syncthreads();
+  scan_experts(stot, E, T, S, ns, bn, ws, off_s, act_s, tp_s, &n_act_s, &routed_total_s);
+  const int na = n_act_s;
+  for (int a = threadIdx.x; a <= na; a += blockDim.x) {
+    ws.tile_prefix[a] = tp_s[a];
+    if (a < na) ws.active[a] = act_s[a];
+  }
+  for (int b = lo; b < hi; b += 32) {
+    const int s = b + lane;
+    int e = -1;
+    if (s < hi) {
+      e = idx[s];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (e >= 0) {
+      const int p = off_s[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
+      ws.perm[p] = s;
+      ws.slot_pos[s] = p;
+      ws.pos_tok[p] = s / k;
+    } else if (s < hi) {
+      ws.slot_pos[s] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  for (int i = threadIdx.x; i < ns * T; i += blockDim.x) ws.pos_tok[S + i] = i % T;
+  // token tiles of width bn for the tensor-core path: (expert, first position, tokens)
+  if (bn > 0) {
+    for (int a = threadIdx.x; a < na; a += blockDim.x) {
+      const int x = act_s[a];
+      const int c = x < E ? stot[x] : T, p0 = x < E ? off_s[x] : S + (x - E) * T, t0 = tp_s[a];
+      for (int j = 0; j * bn < c; ++j) ws.tile_info[t0 + j] = make_int4(x, p0 + j * bn, min(bn, c - j * bn), 0);
+    }
+  }
+  // positions left free by invalid expert ids still name a real token, so
+  // that every position's row can be read safely
+  for (int p = routed_total_s + threadIdx.x; p < S; p += blockDim.x) ws.pos_tok[p] = 0;
+}
+
+
+// The same segments for a small batch (T * k <= blockDim.x == 1024, E <= 1024),
+// with every intermediate in shared memory: one thread per slot, counts by
+// shared atomics, the rank of a slot among its expert's slots by counting
+// the earlier equal slots (so the order is the stable one above, bit for bit).
+// sm needs 4 * E + 2 * ns + T * k + 1 ints.
+__device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ idx, int T, int k, int E,
+                                                   int ns, int bn, const Workspace& ws, int32_t* sm) {
+  const int NE = E + ns, S = T * k, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  int32_t* cnt_s = sm;             // [E]     slots per expert
+  int32_t* off_s = sm + E;         // [E]     first position per expert
+  int32_t* act_s = sm + 2 * E;     // [NE]    active experts, routed then shared
+  int32_t* tp_s = sm + 2 * E + NE; // [NE+1]  token tiles before each active expert
+  int32_t* sid = tp_s + NE + 1;    // [S]     expert of each slot (-1: invalid)
+  __shared__ int n_act_s, routed_total_s;
+  for (int i = tid; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
+  for (int i = tid; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
+  for (int e = tid; e < E; e += blockDim.x) cnt_s[e] = 0;
+  __syncthreads();
+  int e = -1;
+  if (tid < S) {
+    e = idx[tid];
+    if (e < 0 || e >= E) {
+      raise_error(ws.err, kErrExpertRange);
+      e = -1;
+    }
+    sid[tid] = e;
+    if (e >= 0) atomicAdd(&cnt_s[e], 1);
+  }
+  __syncthreads();
+  scan_experts(cnt_s, E, T, S, ns, bn, ws, off_s, act_s, tp_s, &n_act_s, &routed_total_s);
   const int na = n_act_s;
   for (int a = tid; a <= na; a += blockDim.x) {
     ws.tile_prefix[a] = tp_s[a];
