@@ -89,12 +89,18 @@ struct Cfg {
   static constexpr int kATile = 128 * 128 * CH;           // one matrix, one stage
   static constexpr int kBTile = BN * 128 * CH;
   // MMA issue is split over two threads (see the kernel): gate/up one matrix
-  // each; down one half of the token columns each (BN >= 64) or one half of
-  // each stage's K steps, into a second accumulator (BN = 16).
+  // each; down the token columns [0, kN0) and [kN0, BN) (BN >= 64; kN0 a
+  // multiple of 32 so each half's scale groups start a column group, both
+  // halves multiples of 16) or one half of each stage's K steps, into a second
+  // accumulator (BN = 16).
   static constexpr bool kSplitN = MODE == kModeDown && BN >= 64;
   static constexpr bool kSplitK = MODE == kModeDown && BN < 64;
+  static constexpr int kN0 = (BN / 2 + 31) / 32 * 32;
   static constexpr int kAccCols = (MODE == kModeUp || kSplitK ? 2 : 1) * BN;  // g, u (up); o (down)
   static constexpr int kNAcc = (MODE == kModeUp && BN >= 128) ? 1 : 2;
+  static constexpr int kStage = kNA * kATile + kBTile;  // shared memory of one ring stage
+  static constexpr int kStageCap0 = (kSmemBudget - 1024) / kStage;
+  static constexpr int kStageCap = kStageCap0 < kMaxStages ? kStageCap0 : kMaxStages;
   // Scale factors in TMEM, per stage: 4 columns per (weight matrix, chunk),
   // then per chunk the token scales (group of 32 tokens g at column g); with
   // the column split each half starts a 4-column group of its own (the MMA
@@ -102,9 +108,9 @@ struct Cfg {
   static constexpr int kBCols = kSplitN ? 8 : 4;
   static constexpr int kSfCols = kNA * 4 * CH + kBCols * CH;
   __host__ __device__ static constexpr int sfb_col(int c, int g) {
-    return kNA * 4 * CH + c * kBCols + (kSplitN ? (g / (BN / 64)) * 4 + g % (BN / 64) : g);
+    return kNA * 4 * CH + c * kBCols + (kSplitN ? (g < kN0 / 32 ? g : 4 + g - kN0 / 32) : g);
   }
-  static constexpr int kTmemCols = kNAcc * kAccCols + kMaxStages * kSfCols;
+  static constexpr int kTmemCols = kNAcc * kAccCols + kStageCap * kSfCols;
   static constexpr int kTmemAlloc = pow2_cols(kTmemCols);
   static_assert(kTmemCols <= 512, "TMEM budget");
 };
@@ -117,10 +123,8 @@ template <int MODE, int BN, int CH>
 void geometry(int K, int* n_stages, int* smem) {
   using C = Cfg<MODE, BN, CH>;
   (void)K;
-  const int stage = C::kNA * C::kATile + C::kBTile;
-  const int st = (kSmemBudget - 1024) / stage;
-  *n_stages = st > kMaxStages ? kMaxStages : st;
-  *smem = 1024 + *n_stages * stage;
+  *n_stages = C::kStageCap;
+  *smem = 1024 + C::kStageCap * C::kStage;
 }
 
 struct Unit {
@@ -360,7 +364,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // MMAs, so the empty and accumulator-full barriers count two arrivals.
     if (lane == 0) {
       const int j = warp == 1 ? 0 : 1;
-      constexpr int NI = C::kSplitN ? BN / 2 : BN;  // N of each MMA
+      // N of this thread's MMAs and the first of its token columns
+      const int NI = C::kSplitN ? (j == 0 ? C::kN0 : BN - C::kN0) : BN;
+      const int n0 = C::kSplitN ? j * C::kN0 : 0;
       uint32_t g = 0, it = 0;
       const uint32_t idesc_base = idesc_e2m1_e4m3(128, NI, 0);
       Sched sc = sc0;
@@ -403,9 +409,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
                 mma_mxf8f6f4(d_tmem + acc * BN, a_desc0 + (uint64_t)((m * C::kATile + c * 16384 + 32 * k) >> 4),
                              bdesc, idesc, sf + (acc * CH + c) * 4, sfb, (s != s_beg || c || k) ? 1u : 0u);
               } else if constexpr (C::kSplitN) {
-                // token columns [j * NI, (j + 1) * NI): B rows and their scale lanes
-                mma_mxf8f6f4(d_tmem + j * NI, a_desc0 + (uint64_t)((c * 16384 + 32 * k) >> 4),
-                             bdesc + (uint64_t)((j * NI * 128) >> 4), idesc, sf + c * 4, sf + C::sfb_col(c, j * NI / 32),
+                // token columns [n0, n0 + NI): B rows and their scale groups
+                mma_mxf8f6f4(d_tmem + n0, a_desc0 + (uint64_t)((c * 16384 + 32 * k) >> 4),
+                             bdesc + (uint64_t)((n0 * 128) >> 4), idesc, sf + c * 4, sf + C::sfb_col(c, n0 / 32),
                              (s != s_beg || c || k) ? 1u : 0u);
               } else {
                 // K steps i = 4c + k of the stage: the first half to accumulator 0
@@ -769,7 +775,7 @@ template <int MODE, int CH>
 cudaError_t launch_bn(MmaParams& p, int bn, int num_sms, cudaStream_t st) {
   if (bn == 16) return launch_one<MODE, 16, CH>(p, num_sms, st);
   if (bn == 64) return launch_one<MODE, 64, CH>(p, num_sms, st);
-  return launch_one<MODE, 128, CH>(p, num_sms, st);
+  return launch_one<MODE, 112, CH>(p, num_sms, st);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -842,14 +848,18 @@ struct MmaMaps {
   CUtensorMap gate, up, down, s_gate, s_up, s_down;
   CUtensorMap gu_pair, s_gu_pair;  // gate + up as one 4-D tensor (when possible)
   int merged[2], swap_gu[2];
-  CUtensorMap xg[3], hq[3];  // per token tile width: 16, 64, 128
+  CUtensorMap xg[3], hq[3];  // per token tile width: 16, 64, 112
   int ch_up, ch_down;
 };
 
 
 static int bn_index(int bn) { return bn == 16 ? 0 : (bn == 64 ? 1 : 2); }
 
-int mma_tile_for_tokens(int T) { return T <= 64 ? 16 : (T < 512 ? 64 : 128); }
+// Token tile width: 16 for decode, 64 below 512 tokens, else 112 — the widest
+// N for which the gate/up kernel's two accumulators fit TMEM twice (2 x 2 x
+// 112 columns + the stages' scale factors <= 512), so the epilogue of one unit
+// overlaps the MMAs of the next.
+int mma_tile_for_tokens(int T) { return T <= 64 ? 16 : (T < 512 ? 64 : 112); }
 
 MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Workspace& ws) {
   MmaMaps* m = new MmaMaps();
@@ -871,7 +881,7 @@ MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Worksp
     if (ns > 0)
       m->merged[1] = map_4d_pair(&m->s_gu_pair, w.s_gate.codes, w.s_up.codes, H, ns * I, m->ch_up, &m->swap_gu[1]);
   }
-  const uint32_t bns[3] = {16, 64, 128};
+  const uint32_t bns[3] = {16, 64, 112};
   for (int i = 0; ok && i < 3; ++i)
     ok = map_3d(&m->xg[i], false, ws.xg, H, P, bns[i], m->ch_up) &&
          map_3d(&m->hq[i], false, ws.hq, I, P, bns[i], m->ch_down);

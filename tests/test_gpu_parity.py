@@ -277,6 +277,23 @@ def test_forward_host_matches_device_path():
     L.close()
 
 
+# at least 512 tokens: 112-token tiles (several per expert, ragged), both MMA issuers
+# splitting the down tile's columns 64 + 48
+PREFILL_SMALL = Workload("prefill_h512_i256_e16_k4_t600", 512, 256, 16, 4, 1, 600, seed=27,
+                         scale_lo=-8, scale_hi=-4)
+
+
+def test_prefill_tiles_match_oracle():
+    wl = PREFILL_SMALL
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    idx, w = _oracle_routing(wl, x)
+    y = gu.run_forward(L, x, idx, w)
+    gu.assert_y_close(y, gu.oracle_layer(wl, 0, x, idx, w))
+    assert np.array_equal(gu.run_forward(L, x, idx, w), y)
+    L.close()
+
+
 STEP = SMALL + [
     Workload("step_h1024_i256_e64_k6_t64", 1024, 256, 64, 6, 1, 64, seed=24, scale_lo=-8, scale_hi=-4),
     Workload("step_h512_i256_e32_k4_t80", 512, 256, 32, 4, 1, 80, seed=25, scale_lo=-8, scale_hi=-4),
