@@ -39,6 +39,7 @@ struct MmaParams {
   CUtensorMap a_routed[2];   // up mode: gate, up banks; down mode: down bank in [0]
   CUtensorMap a_shared[2];
   CUtensorMap b;             // activations by position, 3-D view of [P][K] E4M3
+  CUtensorMap b_half;        // CTA pairs: the same view, half a token tile, one chunk per box
   const uint8_t* sa_routed[2];
   const uint8_t* sa_shared[2];
   const uint8_t* sb;         // activation scales by position, [P][K/32]
@@ -132,11 +133,13 @@ struct Unit {
 };
 
 // Unit u -> (token tile v, 128-row tile); row tiles innermost so consecutive
-// units share the activation tile.
-__device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_per_expert) {
-  const int v = u / mt_per_expert;
+// units share the activation tile.  For a CTA pair, u counts pairs of row
+// tiles (mt_units = row tiles / 2) and rank picks the pair's member.
+__device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_units, int rank = -1) {
+  const int v = u / mt_units;
   const int4 t = __ldg(p.tile_info + v);
-  return Unit{t.x, t.y, t.z, (u - v * mt_per_expert) * 128};
+  const int r = u - v * mt_units;
+  return Unit{t.x, t.y, t.z, (rank < 0 ? r : 2 * r + rank) * 128};
 }
 
 // Work partition.  Plain: whole units strided over the CTAs.  Split: when
@@ -157,9 +160,10 @@ constexpr int kMaxTopK = 8, kMaxShared = 4;  // layer limits (moe_config)
 struct Sched {
   int ti, g, end;  // split: stage iterations in all, cursor, end of this CTA's range
   int total, ks, u;
+  int cta, G;      // this worker and the number of workers (CTAs, or CTA pairs)
   bool split;
-  __device__ Sched(int total_, int ks_, int split_ok) : total(total_), ks(ks_) {
-    const int G = gridDim.x;
+  __device__ Sched(int total_, int ks_, int split_ok, int cta_, int G_)
+      : total(total_), ks(ks_), cta(cta_), G(G_) {
     split = false;
     if (split_ok && total < 4 * G) {
       ti = total * ks;
@@ -169,18 +173,18 @@ struct Sched {
       // no unit is cut into more than kMaxPieces pieces
       split = ti >= G && split_max * 20 < plain_max * 19 && ks <= (kMaxPieces - 2) * (ti / G);
     }
-    g = split ? begin(blockIdx.x) : 0;
-    end = split ? begin(blockIdx.x + 1) : 0;
-    u = blockIdx.x;
+    g = split ? begin(cta) : 0;
+    end = split ? begin(cta + 1) : 0;
+    u = cta;
   }
-  __device__ int begin(int c) const { return (int)(((unsigned)c * (unsigned)ti) / gridDim.x); }
+  __device__ int begin(int c) const { return (int)(((unsigned)c * (unsigned)ti) / G); }
   // the CTA whose range holds stage iteration it
-  __device__ int owner(int it) const { return (int)(((unsigned)(it + 1) * gridDim.x + ti - 1) / ti) - 1; }
+  __device__ int owner(int it) const { return (int)(((unsigned)(it + 1) * G + ti - 1) / ti) - 1; }
   __device__ Piece next() {
     Piece pc{-1, 0, 0};
     if (!split) {
       if (u < total) pc = Piece{u, 0, ks};
-      u += gridDim.x;
+      u += G;
       return pc;
     }
     if (g >= end) return pc;
@@ -193,7 +197,7 @@ struct Sched {
   // Unit uu is computed by CTAs first .. first + n - 1 (piece j by CTA first + j).
   __device__ void pieces(int uu, int& first, int& n) const {
     if (!split) {
-      first = blockIdx.x;
+      first = cta;
       n = 1;
       return;
     }
@@ -215,6 +219,37 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Multicast load into the same shared-memory offset of every CTA in mask (the
+// mbarrier at bar's offset in each of them receives the bytes).
+__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                               int32_t c2, uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+      "[%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+// tcgen05.commit whose arrival goes to the mbarrier at bar's offset in every
+// CTA of mask.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // h = silu(g) * u = g / (1 + e^-g) * u with the SFU exponential and the fast
 // divide: a few ulp from the correctly rounded form, far inside the FP8
 // rounding of h that follows (one E4M3 step is 2^-3 relative).
@@ -231,7 +266,10 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-template <int MODE, int BN, int CH>
+// PAIR: the grid is clusters of two CTAs that process the two row tiles of a
+// pair for the same token tile: each CTA loads half of the activation tile
+// and multicasts it to both, so each SM moves half the activation bytes.
+template <int MODE, int BN, int CH, bool PAIR>
 __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_constant__ MmaParams p) {
   using C = Cfg<MODE, BN, CH>;
   constexpr int NA = C::kNA;
@@ -261,7 +299,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&sf_bar[s], 4);
-      mbar_init(&empty_bar[s], 2);  // one commit per MMA-issuing thread
+      mbar_init(&empty_bar[s], PAIR ? 4 : 2);  // one commit per MMA-issuing thread (of both CTAs)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf_bar[b], 2);
@@ -273,6 +311,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   if (warp == 1) tmem_alloc(&tmem_slot, C::kTmemAlloc);
   fence_before();
   __syncthreads();
+  // a pair's barriers must be initialised before the peer multicasts into them
+  if constexpr (PAIR) cluster_sync_all();
   fence_after();
   const uint32_t tmem = tmem_slot;
   // Programmatic dependent launch.  Usually the tile table and the weights
@@ -282,8 +322,11 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   // kernel the tile table is that kernel's own output, so everything waits.
   if (p.wait_tiles) pdl_wait();
   pdl_trigger();
-  const int total = p.n_active[1] * mt_per_expert;
-  const Sched sc0(total, k_stages, BN <= 64 && p.split_ok);
+  const int rank = PAIR ? (int)cluster_ctarank() : -1;
+  const int mt_units = PAIR ? mt_per_expert / 2 : mt_per_expert;
+  const int total = p.n_active[1] * mt_units;
+  const Sched sc0(total, k_stages, BN <= 64 && p.split_ok, PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x,
+                  PAIR ? (int)gridDim.x / 2 : (int)gridDim.x);
 
   auto give_up = [&]() {
     atomicOr(p.err, kErrTimeout);
@@ -298,11 +341,24 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       int last_parity[kMaxStages];
       int deferred_pos[kMaxStages], deferred_s[kMaxStages], n_deferred = 0;
       bool waited = gather;  // gather mode: the TMA warp loads weights only
+      // the activation tile of a stage: whole (one op), or for a CTA pair this
+      // CTA's half of every chunk, multicast into both CTAs' slots
+      auto load_b = [&](int slot, int pos0, int st) {
+        uint8_t* sb = stage_base + slot * stage_bytes + NA * C::kATile;
+        if constexpr (PAIR) {
+#pragma unroll
+          for (int c = 0; c < CH; ++c)
+            tma_load_3d_mc(sb + (c * BN + rank * (BN / 2)) * 128, &p.b_half, 0, pos0 + rank * (BN / 2), st * CH + c,
+                           &full_bar[slot], 0x3);
+        } else {
+          tma_load_3d(sb, &p.b, 0, pos0, st * CH, &full_bar[slot]);
+        }
+      };
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
       Sched sc = sc0;
       for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next()) {
-        const Unit un = decode_unit(p, pc.u, mt_per_expert);
+        const Unit un = decode_unit(p, pc.u, mt_units, rank);
         const bool sh = un.e >= p.E;
         const int erow = (sh ? un.e - p.E : un.e) * p.rows + un.row0;
         bool ok = true;
@@ -314,9 +370,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             // ring full: wait for the previous kernel, then load the deferred activations
             pdl_wait();
             waited = true;
-            for (int i = 0; i < n_deferred; ++i)
-              tma_load_3d(stage_base + i * stage_bytes + NA * C::kATile, &p.b, 0, deferred_pos[i],
-                          deferred_s[i] * CH, &full_bar[i]);
+            for (int i = 0; i < n_deferred; ++i) load_b(i, deferred_pos[i], deferred_s[i]);
           }
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); ok = false; break; }
           uint8_t* sa = stage_base + slot * stage_bytes;
@@ -333,7 +387,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           if (gather) {
             // activations come from the scale-factor warps
           } else if (waited) {
-            tma_load_3d(sa + NA * C::kATile, &p.b, 0, un.pos0, s * CH, &full_bar[slot]);
+            load_b(slot, un.pos0, s);
           } else {
             deferred_pos[n_deferred] = un.pos0;  // slot == n_deferred while g < NS
             deferred_s[n_deferred++] = s;
@@ -346,14 +400,19 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       }
       if (!waited) {
         pdl_wait();
-        for (int i = 0; i < n_deferred; ++i)
-          tma_load_3d(stage_base + i * stage_bytes + NA * C::kATile, &p.b, 0, deferred_pos[i],
-                      deferred_s[i] * CH, &full_bar[i]);
+        for (int i = 0; i < n_deferred; ++i) load_b(i, deferred_pos[i], deferred_s[i]);
       }
       // never leave with copies in flight: wait for the last load into each slot
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s)
         if (last_parity[s] >= 0) mbar_wait(&full_bar[s], (uint32_t)last_parity[s], kWaitLimit);
+      if constexpr (PAIR) {
+        // nor with the pair's releases still on their way: wait until both CTAs
+        // have released the last fill of every slot
+#pragma unroll
+        for (int s = 0; s < kMaxStages; ++s)
+          if (last_parity[s] >= 0) mbar_wait(&empty_bar[s], (uint32_t)last_parity[s], kWaitLimit);
+      }
     }
   } else if (warp == 1 || warp == kIssuer2Warp) {
     // ---------------------------------------------------------------- MMA
@@ -378,7 +437,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         const uint32_t d_tmem = tmem + buf * C::kAccCols;
         int swap = 0;
         if (NA == 2) {
-          const int e = decode_unit(p, pc.u, mt_per_expert).e;
+          const int e = decode_unit(p, pc.u, mt_units, rank).e;
           const int sh = e >= p.E;
           swap = p.merged[sh] && p.swap_gu[sh];
         }
@@ -421,7 +480,10 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
                                sf + c * 4, sfb, (s != s_beg || i != first) ? 1u : 0u);
               }
             }
-          mma_commit(&empty_bar[slot]);
+          if constexpr (PAIR)
+            mma_commit_mc(&empty_bar[slot], 0x3);  // the slot is refilled in both CTAs at once
+          else
+            mma_commit(&empty_bar[slot]);
         }
         if (!ok) break;
         mma_commit(&accf_bar[buf]);
@@ -439,7 +501,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     bool ok = true;
     Sched sc = sc0;
     for (Piece pc = sc.next(); ok && pc.u >= 0 && !aborted(); pc = sc.next()) {
-      const Unit un = decode_unit(p, pc.u, mt_per_expert);
+      const Unit un = decode_unit(p, pc.u, mt_units, rank);
       const int s_end = pc.s1;
       const bool sh = un.e >= p.E;
       const size_t erow = (size_t)(sh ? un.e - p.E : un.e) * p.rows + un.row0 + 32 * q + lane;
@@ -658,7 +720,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     uint32_t it = 0;
     Sched sc = sc0;
     for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
-      const Unit un = decode_unit(p, pc.u, mt_per_expert);
+      const Unit un = decode_unit(p, pc.u, mt_units, rank);
       const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
       const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
       if (!mbar_wait(&accf_bar[buf], ph_acc, kWaitLimit)) { give_up(); break; }
@@ -689,7 +751,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         // the last piece to arrive adds all of them in piece order.  Each warp
         // owns its 32 rows, so the hand-off is per warp (one counter per unit
         // and quadrant) and no warp ever waits for another.
-        float* mine = p.part + (size_t)sc.slot(pc.u, first, blockIdx.x - first) * kSlot;
+        float* mine = p.part + (size_t)sc.slot(pc.u, first, sc.cta - first) * kSlot;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           uint32_t v[16], vu[16];
@@ -747,19 +809,21 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   }
   fence_before();
   __syncthreads();
+  // a CTA of a pair leaves only when the peer no longer writes into it
+  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     fence_after();
     tmem_dealloc(tmem, C::kTmemAlloc);
   }
 }
 
-template <int MODE, int BN, int CH>
+template <int MODE, int BN, int CH, bool PAIR>
 cudaError_t launch_one(MmaParams& p, int num_sms, cudaStream_t st) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_mma_kernel<MODE, BN, CH>,
+    cudaError_t e = cudaFuncSetAttribute(ffn_mma_kernel<MODE, BN, CH, PAIR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -767,15 +831,36 @@ cudaError_t launch_one(MmaParams& p, int num_sms, cudaStream_t st) {
   int smem = 0;
   geometry<MODE, BN, CH>(p.K, &p.n_stages, &smem);
   if (p.n_stages < 2) return cudaErrorInvalidConfiguration;
-  { cudaError_t le_ = launch_pdl(ffn_mma_kernel<MODE, BN, CH>, dim3(num_sms), dim3(kThreadsMma), smem, st, p); if (le_ != cudaSuccess) return le_; }
+  if (!PAIR) {
+    { cudaError_t le_ = launch_pdl(ffn_mma_kernel<MODE, BN, CH, false>, dim3(num_sms), dim3(kThreadsMma), smem, st, p); if (le_ != cudaSuccess) return le_; }
+    return cudaGetLastError();
+  }
+  // clusters of two CTAs, as a programmatic dependent launch
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms & ~1);
+  cfg.blockDim = dim3(kThreadsMma);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, ffn_mma_kernel<MODE, BN, CH, PAIR>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <int MODE, int CH>
-cudaError_t launch_bn(MmaParams& p, int bn, int num_sms, cudaStream_t st) {
-  if (bn == 16) return launch_one<MODE, 16, CH>(p, num_sms, st);
-  if (bn == 64) return launch_one<MODE, 64, CH>(p, num_sms, st);
-  return launch_one<MODE, 112, CH>(p, num_sms, st);
+cudaError_t launch_bn(MmaParams& p, int bn, bool pair, int num_sms, cudaStream_t st) {
+  if (bn == 16) return launch_one<MODE, 16, CH, false>(p, num_sms, st);
+  if (bn == 64) return launch_one<MODE, 64, CH, false>(p, num_sms, st);
+  if (pair) return launch_one<MODE, 112, CH, true>(p, num_sms, st);
+  return launch_one<MODE, 112, CH, false>(p, num_sms, st);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -849,6 +934,7 @@ struct MmaMaps {
   CUtensorMap gu_pair, s_gu_pair;  // gate + up as one 4-D tensor (when possible)
   int merged[2], swap_gu[2];
   CUtensorMap xg[3], hq[3];  // per token tile width: 16, 64, 112
+  CUtensorMap xg_half, hq_half;  // CTA pairs: half a 112-token tile, one chunk per box
   int ch_up, ch_down;
 };
 
@@ -885,6 +971,8 @@ MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Worksp
   for (int i = 0; ok && i < 3; ++i)
     ok = map_3d(&m->xg[i], false, ws.xg, H, P, bns[i], m->ch_up) &&
          map_3d(&m->hq[i], false, ws.hq, I, P, bns[i], m->ch_down);
+  if (ok)
+    ok = map_3d(&m->xg_half, false, ws.xg, H, P, 112 / 2, 1) && map_3d(&m->hq_half, false, ws.hq, I, P, 112 / 2, 1);
   if (!ok) {
     delete m;
     return nullptr;
@@ -961,10 +1049,13 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
     p.y = cmb->y;
     p.comb_cnt = ws.comb_cnt;
   }
+  // CTA pairs for the widest tiles: both row-tile counts even, an even grid
+  const bool pair = bn == 112 && (p.rows / 128) % 2 == 0 && num_sms >= 2;
+  if (pair) p.b_half = mode == kModeUp ? mm.xg_half : mm.hq_half;
   if (mode == kModeUp)
-    return ch == 2 ? launch_bn<kModeUp, 2>(p, bn, num_sms, st) : launch_bn<kModeUp, 1>(p, bn, num_sms, st);
-  if (ch == 3) return launch_bn<kModeDown, 3>(p, bn, num_sms, st);
-  return ch == 2 ? launch_bn<kModeDown, 2>(p, bn, num_sms, st) : launch_bn<kModeDown, 1>(p, bn, num_sms, st);
+    return ch == 2 ? launch_bn<kModeUp, 2>(p, bn, pair, num_sms, st) : launch_bn<kModeUp, 1>(p, bn, pair, num_sms, st);
+  if (ch == 3) return launch_bn<kModeDown, 3>(p, bn, pair, num_sms, st);
+  return ch == 2 ? launch_bn<kModeDown, 2>(p, bn, pair, num_sms, st) : launch_bn<kModeDown, 1>(p, bn, pair, num_sms, st);
 }
 
 }  // namespace moe

@@ -53,11 +53,11 @@ __global__ void quantize_gather_kernel(const uint16_t* __restrict__ x, int P, in
 // Expert segments in one CTA of 1024 threads (segments.cuh).
 __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restrict__ idx, int T,
                                                         int k, int E, int ns, int bn, Workspace ws,
-                                                        int stage_idx) {
+                                                        int scatter_smem) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ int32_t sm[];
-  segments_cta(idx, T, k, E, ns, bn, ws, sm, stage_idx != 0);
+  segments_cta(idx, T, k, E, ns, bn, ws, sm, scatter_smem != 0);
 }
 
 // y[t] = bf16( sum_s o[S + s*T + t] + sum_j w[t][j] * o[slot_pos[t*k + j]] ),
@@ -165,13 +165,13 @@ cudaError_t launch_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uin
 }
 
 size_t segments_smem_bytes(int E) { return (size_t)(36 * E + 2 * 4 + 1) * sizeof(int32_t); }
-constexpr size_t kSegmentsSmemMax = 200 * 1024;  // room for the staged ids of up to ~30k slots
+constexpr size_t kSegmentsSmemMax = 200 * 1024;  // room for the position table of up to ~30k slots
 
 cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared, int bn,
                             const Workspace& ws, cudaStream_t st) {
-  const size_t base = segments_smem_bytes(E), staged = base + (size_t)T * k * sizeof(int32_t);
-  const bool stage = staged <= kSegmentsSmemMax;
-  { cudaError_t le_ = launch_pdl(segments_kernel, dim3(1), dim3(1024), stage ? staged : base, st, idx, T, k, E, n_shared, bn, ws, stage ? 1 : 0); if (le_ != cudaSuccess) return le_; }
+  const size_t base = segments_smem_bytes(E), with_table = base + (size_t)T * k * sizeof(int32_t);
+  const bool scatter = with_table <= kSegmentsSmemMax;  // position table in shared memory
+  { cudaError_t le_ = launch_pdl(segments_kernel, dim3(1), dim3(1024), scatter ? with_table : base, st, idx, T, k, E, n_shared, bn, ws, scatter ? 1 : 0); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 

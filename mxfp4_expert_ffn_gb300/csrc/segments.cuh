@@ -105,15 +105,16 @@ __device__ __forceinline__ void scan_experts(const int32_t* cnt_s, int E, int T,
 // stable counting sort, identical on every run.
 // Needs blockDim.x == 1024 and sm = 36 * E + 2 * ns + 1 ints of shared memory; every
 // thread of the CTA must call it.
-__device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx_g, int T, int k, int E,
+__device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx, int T, int k, int E,
                                              int ns, int bn, const Workspace& ws, int32_t* sm,
-                                             bool stage_idx = false) {
+                                             bool scatter_smem = false) {
   const int NE = E + ns;
   int32_t* wcnt = sm;                  // [32][E] per-warp counts, then running bases
   int32_t* stot = sm + 32 * E;         // [E]     slots per expert
   int32_t* off_s = stot + E;           // [E]     first position per expert
   int32_t* act_s = off_s + E;          // [NE]    active experts
   int32_t* tp_s = act_s + NE;          // [NE+1]  token tiles before each active expert
+  int32_t* ps = tp_s + NE + 1;         // [S]     scatter_smem: the slot at each position
   __shared__ int n_act_s, routed_total_s;
   const int S = T * k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -122,30 +123,32 @@ __device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx_g, 
   for (int i = threadIdx.x; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
   // and so do the fused-combine counters
   for (int i = threadIdx.x; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
-  // with room, the slots' expert ids are staged in shared memory by one
-  // coalesced pass, so the two per-warp passes below never wait on global loads
-  const int32_t* idx = idx_g;
-  if (stage_idx) {
-    int32_t* sidx = tp_s + NE + 1;  // [S]
-    for (int i = threadIdx.x; i < S; i += blockDim.x) sidx[i] = idx_g[i];
-    idx = sidx;
-  }
   __syncthreads();
+  // Each warp owns slots [lo, hi) and reads their expert ids eight rows of 32
+  // at a time (all eight loads in flight before they are used).
+  constexpr int kU = 8;
   const int per = (S + 31) / 32;
   const int lo = min(S, warp * per), hi = min(S, lo + per);
-  for (int b = lo; b < hi; b += 32) {
-    const int s = b + lane;
-    int e = -1;
-    if (s < hi) {
-      e = idx[s];
-      if (e < 0 || e >= E) {
+  for (int b0 = lo; b0 < hi; b0 += 32 * kU) {
+    int er[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int s = b0 + 32 * u + lane;
+      er[u] = s < hi ? idx[s] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (b0 + 32 * u >= hi) break;  // warp-uniform
+      int e = er[u];
+      if (b0 + 32 * u + lane < hi && (e < 0 || e >= E)) {
         raise_error(ws.err, kErrExpertRange);
         e = -1;
       }
+      if (b0 + 32 * u + lane >= hi) e = -1;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+      __syncwarp();
     }
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
-    __syncwarp();
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -164,25 +167,47 @@ __device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx_g, 
     ws.tile_prefix[a] = tp_s[a];
     if (a < na) ws.active[a] = act_s[a];
   }
-  for (int b = lo; b < hi; b += 32) {
-    const int s = b + lane;
-    int e = -1;
-    if (s < hi) {
-      e = idx[s];
-      if (e < 0 || e >= E) e = -1;
+  // placement: position p = the expert's first position + the slots of that
+  // expert in earlier warps + the equal-expert lanes before this one
+  for (int b0 = lo; b0 < hi; b0 += 32 * kU) {
+    int er[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int s = b0 + 32 * u + lane;
+      er[u] = s < hi ? idx[s] : -1;
     }
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-    if (e >= 0) {
-      const int p = off_s[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
-      ws.perm[p] = s;
-      ws.slot_pos[s] = p;
-      ws.pos_tok[p] = s / k;
-    } else if (s < hi) {
-      ws.slot_pos[s] = -1;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (b0 + 32 * u >= hi) break;  // warp-uniform
+      const int s = b0 + 32 * u + lane;
+      int e = er[u];
+      if (s >= hi || e < 0 || e >= E) e = -1;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+      if (e >= 0) {
+        const int p = off_s[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
+        ws.slot_pos[s] = p;
+        if (scatter_smem) {
+          ps[p] = s;
+        } else {
+          ws.perm[p] = s;
+          ws.pos_tok[p] = s / k;
+        }
+      } else if (s < hi) {
+        ws.slot_pos[s] = -1;
+      }
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+      __syncwarp();
     }
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
-    __syncwarp();
+  }
+  if (scatter_smem) {
+    // the position-ordered tables leave shared memory in coalesced rows
+    __syncthreads();
+    for (int p = threadIdx.x; p < routed_total_s; p += blockDim.x) {
+      const int sl = ps[p];
+      ws.perm[p] = sl;
+      ws.pos_tok[p] = sl / k;
+    }
   }
   for (int i = threadIdx.x; i < ns * T; i += blockDim.x) ws.pos_tok[S + i] = i % T;
   // token tiles of width bn for the tensor-core path: (expert, first position, tokens)
