@@ -97,6 +97,9 @@ struct Cfg {
   static constexpr bool kSplitN = MODE == kModeDown && BN >= 64;
   static constexpr bool kSplitK = MODE == kModeDown && BN < 64;
   static constexpr int kN0 = (BN / 2 + 31) / 32 * 32;
+  // MMA width per tile from its token count (the 112-token tiles; narrower
+  // tiles are mostly full or one instruction step wide)
+  static constexpr bool kRagged = BN == 112;
   static constexpr int kAccCols = (MODE == kModeUp || kSplitK ? 2 : 1) * BN;  // g, u (up); o (down)
   static constexpr int kNAcc = (MODE == kModeUp && BN >= 128) ? 1 : 2;
   static constexpr int kStage = kNA * kATile + kBTile;  // shared memory of one ring stage
@@ -424,10 +427,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     if (lane == 0) {
       const int j = warp == 1 ? 0 : 1;
       // N of this thread's MMAs and the first of its token columns
-      const int NI = C::kSplitN ? (j == 0 ? C::kN0 : BN - C::kN0) : BN;
+      const int NI0 = C::kSplitN ? (j == 0 ? C::kN0 : BN - C::kN0) : BN;
       const int n0 = C::kSplitN ? j * C::kN0 : 0;
       uint32_t g = 0, it = 0;
-      const uint32_t idesc_base = idesc_e2m1_e4m3(128, NI, 0);
       Sched sc = sc0;
       for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
         const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
@@ -435,12 +437,20 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         if (!mbar_wait(&acce_bar[buf], ph_acc ^ 1, kWaitLimit)) { give_up(); break; }
         fence_after();
         const uint32_t d_tmem = tmem + buf * C::kAccCols;
-        int swap = 0;
-        if (NA == 2) {
-          const int e = decode_unit(p, pc.u, mt_units, rank).e;
-          const int sh = e >= p.E;
-          swap = p.merged[sh] && p.swap_gu[sh];
+        int swap = 0, NI = NI0;
+        if (NA == 2 || C::kRagged) {
+          const Unit un = decode_unit(p, pc.u, mt_units, rank);
+          const int sh = un.e >= p.E;
+          if (NA == 2) swap = p.merged[sh] && p.swap_gu[sh];
+          if (C::kRagged) {
+            // the wide tiles are often part-filled: N = the tile's tokens
+            // rounded up to the instruction's step of 16, so the MMAs cost
+            // only the columns in use (the epilogue reads no column past them)
+            const int nr = min(BN, (un.m_tile + 15) & ~15);
+            NI = C::kSplitN ? (j == 0 ? min(C::kN0, nr) : nr - C::kN0) : nr;
+          }
         }
+        const uint32_t idesc_base = idesc_e2m1_e4m3(128, NI > 0 ? NI : 16, 0);
         bool ok = true;
         const int s_beg = pc.s0, s_end = pc.s1;
         for (int s = s_beg; s < s_end; ++s, ++g) {
@@ -460,6 +470,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           for (int c = 0; c < CH; ++c)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
+              if (C::kRagged && NI <= 0) break;  // the second column half of a narrow tile is empty
               const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
               const uint64_t bdesc = b_desc0 + (uint64_t)((c * BN * 128 + 32 * k) >> 4);
               const uint32_t sfb = sf + C::sfb_col(c, 0);
@@ -729,14 +740,16 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       int first, n;
       sc.pieces(pc.u, first, n);
       if (n == 1) {
-        // the whole unit: straight from TMEM to the outputs
+        // the whole unit: straight from TMEM to the outputs (the columns the
+        // MMAs wrote)
+        const int c_end = C::kRagged ? min(BN, (un.m_tile + 15) & ~15) : BN;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
+        for (int c = 0; c < c_end; c += 16) {
           uint32_t v[16], vu[16];
           tmem_ld16(t_base + c, v);
           if (MODE == kModeUp || C::kSplitK) tmem_ld16(t_base + BN + c, vu);
           tmem_ld_wait();
-          if (c + 16 >= BN) {
+          if (c + 16 >= c_end) {
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce_bar[buf]);
