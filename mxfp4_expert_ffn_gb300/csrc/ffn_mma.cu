@@ -299,6 +299,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   const uint32_t sf_col0 = C::kNAcc * C::kAccCols;
 
   if (threadIdx.x == 0) {
+    // bring the tensor maps this CTA reads into the descriptor cache while
+    // the previous kernel finishes
+#pragma unroll
+    for (int m = 0; m < NA; ++m) {
+      prefetch_tensormap(&p.a_routed[m]);
+      prefetch_tensormap(&p.a_shared[m]);
+    }
+    prefetch_tensormap(PAIR ? &p.b_half : &p.b);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&sf_bar[s], 4);

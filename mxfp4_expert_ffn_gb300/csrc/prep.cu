@@ -14,7 +14,8 @@
 //      and a share of the x quantisation;
 //   2. the last CTA of each 8-token block to finish adds the K chunks of its
 //      tokens' logits in a fixed order, selects top-k and writes the weights;
-//   3. the last token block to finish builds the expert segments.
+//   3. the last token block to finish builds the expert segments (with one
+//      warp's match and ballot operations when there are at most 32 slots).
 // "Last" is decided by an acquire-release atomic counter; the finisher resets
 // the counter, so the next launch starts from zero.  The sums
 // are the same fixed-order sums as the split-K router kernels, so the logits
@@ -51,7 +52,10 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
   pdl_trigger();  // the expert GEMM may start its prologue; it waits for all of this
   extern __shared__ int32_t sm[];
   __shared__ int last;
+  __shared__ int32_t sid_s[32];  // tiny batches: the slot ids for the segments
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // at most 32 slots, each expert's in one token tile, one token block
+  const bool tiny = p.T * p.k <= 32 && p.T <= p.bn && gridDim.y == 1;
 
   // ---- 1a. router partial sums: warp = expert, CTA = (expert group, token block, K chunk);
   // the CTA's x chunk (8 tokens x H/ks) is staged in shared memory once
@@ -123,8 +127,11 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
         l[i] = e < p.E ? lg[warp * p.E + e] : -INFINITY;
       }
       topk_keys(l, p.E, lane, p.sg, key, sc);
-      select_topk(key, sc, t0 + warp, p.E, p.k, lane, p.sg, p.idx, p.w);
+      const int pick = select_topk(key, sc, t0 + warp, p.E, p.k, lane, p.sg, p.idx, p.w);
+      if (tiny && lane < p.k) sid_s[(t0 + warp) * p.k + lane] = pick;
     }
+  } else if (tiny && (int)threadIdx.x < p.T * p.k) {
+    sid_s[threadIdx.x] = p.idx[threadIdx.x];
   }
 
   // ---- 3. the last token block builds the expert segments
@@ -137,7 +144,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
     __syncthreads();
     if (!last) return;
   }
-  if (p.T * p.k <= (int)blockDim.x)
+  if (tiny)
+    segments_tiny(sid_s, p.T, p.k, p.E, p.ns, p.ws);
+  else if (p.T * p.k <= (int)blockDim.x)
     segments_small_cta(p.idx, p.T, p.k, p.E, p.ns, p.bn, p.ws, sm);
   else
     segments_cta(p.idx, p.T, p.k, p.E, p.ns, p.bn, p.ws, sm);

@@ -87,33 +87,16 @@ __device__ __forceinline__ float router_sum_partials(const float* __restrict__ p
   return f + (b ? b[e] : 0.f);
 }
 
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
+// Order-preserving map of a non-NaN float key to an unsigned integer, with
+// -0 and +0 mapped alike (they compare equal as floats, so the lower expert
+// index decides between them).  Every key maps above 0, which marks "not a
+// candidate".
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(__fadd_rn(v, 0.0f));  // -0 -> +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
-
-// The k selected experts in rank order -> idx[t][r] and their weights:
-// softmax: w_r = exp(v_r - v_0) / sum_r' exp(v_r' - v_0) with v the logits;
-// sigmoid: w_r = s_r / sum_r' s_r' with s the sigmoid scores; sums in rank
-// order; then times the routed scale.
-__device__ __forceinline__ void topk_weights_write(const float* sv, const float* ss, const int* si, int t,
-                                                   int k, const Scoring& sg, int32_t* __restrict__ idx,
-                                                   float* __restrict__ w) {
-  if (sg.sigmoid) {
-    float den = 0.f;
-    for (int r = 0; r < k; ++r) den = __fadd_rn(den, ss[r]);
-    for (int r = 0; r < k; ++r) {
-      idx[(size_t)t * k + r] = si[r];
-      w[(size_t)t * k + r] = __fmul_rn(__fdiv_rn(ss[r], den), sg.scale);
-    }
-    return;
-  }
-  const float m = sv[0];
-  float den = 0.f;
-  for (int r = 0; r < k; ++r) den += expf(sv[r] - m);
-  for (int r = 0; r < k; ++r) {
-    idx[(size_t)t * k + r] = si[r];
-    w[(size_t)t * k + r] = (expf(sv[r] - m) / den) * sg.scale;
-  }
+__device__ __forceinline__ float order_key_value(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
 // Per-lane selection keys and scores from the logits l[e] of one token held by
@@ -139,46 +122,64 @@ __device__ __forceinline__ void topk_keys(const float (&l)[16], int E, int lane,
   }
 }
 
-// k rounds of a warp arg-max over (value desc, index asc) on the 16 values
-// per lane (v[i] is expert lane + 32 i), then the softmax over the k chosen.
-__device__ __forceinline__ void select_topk(const float (&v)[16], const float (&sc)[16], int t, int E, int k,
-                                            int lane, const Scoring& sg, int32_t* __restrict__ idx,
-                                            float* __restrict__ w) {
-  uint32_t taken = 0;
-  float sv[8], ss[8];
-  int si[8];
+// k rounds of a warp arg-max over (key desc, index asc) on the 16 keys per
+// lane (key[i] is expert lane + 32 i): the largest key by an integer warp
+// reduction of the order-preserving codes, then the lowest index holding it
+// by a second one.  Lane r < k ends with the r-th pick and writes idx[t][r]
+// and its weight: softmax w_r = exp(v_r - v_0) / sum_r' exp(v_r' - v_0) with
+// v the logits; sigmoid w_r = s_r / sum_r' s_r' with s the sigmoid scores;
+// both sums in rank order; then times the routed scale.  Returns the lane's
+// pick (-1 for lanes >= k).
+__device__ __forceinline__ int select_topk(const float (&key)[16], const float (&sc)[16], int t, int E, int k,
+                                           int lane, const Scoring& sg, int32_t* __restrict__ idx,
+                                           float* __restrict__ w) {
+  uint32_t ok[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ok[i] = lane + 32 * i < E ? order_key(key[i]) : 0u;
+  int my_i = -1;
+  float my_v = 0.f, my_s = 0.f;
   for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
+    uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && ranks_before(v[i], e, bv, bi)) {
-        bv = v[i];
-        bi = e;
+    for (int i = 0; i < 16; ++i) m = max(m, ok[i]);
+    const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, m);
+    unsigned cand = 0xFFFFFFFFu;
+#pragma unroll
+    for (int i = 15; i >= 0; --i)
+      if (ok[i] == wm) cand = (unsigned)(lane + 32 * i);
+    const int wi = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
+    float s_w = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (lane + 32 * i == wi) {
+        ok[i] = 0u;
+        s_w = sc[i];
       }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      if (ranks_before(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    sv[r] = bv;
-    si[r] = bi;
-    if (sg.sigmoid) {  // the winner's score, from the lane that holds it
-      float mine = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (i == (bi >> 5)) mine = sc[i];
-      ss[r] = __shfl_sync(0xFFFFFFFFu, mine, bi & 31);
+    if (sg.sigmoid) s_w = __shfl_sync(0xFFFFFFFFu, s_w, wi & 31);  // the winner's score
+    if (lane == r) {
+      my_i = wi;
+      my_v = order_key_value(wm);
+      my_s = s_w;
     }
   }
-  if (lane == 0) topk_weights_write(sv, ss, si, t, k, sg, idx, w);
+  // weights: every lane forms the same rank-order sum, lane r < k its own term
+  float wr;
+  if (sg.sigmoid) {
+    float den = 0.f;
+    for (int r = 0; r < k; ++r) den = __fadd_rn(den, __shfl_sync(0xFFFFFFFFu, my_s, r));
+    wr = __fmul_rn(__fdiv_rn(my_s, den), sg.scale);
+  } else {
+    const float m0 = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+    const float ex = lane < k ? expf(my_v - m0) : 0.f;
+    float den = 0.f;
+    for (int r = 0; r < k; ++r) den += __shfl_sync(0xFFFFFFFFu, ex, r);
+    wr = (ex / den) * sg.scale;
+  }
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_i;
+    w[(size_t)t * k + lane] = wr;
+  }
+  return my_i;
 }
 
 }  // namespace moe

@@ -283,4 +283,77 @@ __device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ i
   for (int p = routed_total_s + tid; p < S; p += blockDim.x) ws.pos_tok[p] = 0;
 }
 
+// Expert segments of at most 32 slots when every expert's slots fit one
+// token tile (T <= bn), without a CTA-wide barrier: every thread fills the
+// count and first position of its experts from the slot ids, and warp 0
+// places the slots (one lane each) with match and ballot operations -- the
+// same stable counting sort as segments_cta, so the same outputs.
+// sid: the S slot ids in shared memory, visible to every calling thread.
+__device__ __forceinline__ void segments_tiny(const int32_t* sid, int T, int k, int E, int ns,
+                                              const Workspace& ws) {
+  const int S = T * k, NE = E + ns, tid = threadIdx.x, lane = tid & 31;
+  for (int i = tid; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
+  for (int i = tid; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
+  for (int e = tid; e < E; e += blockDim.x) {
+    int c = 0, off = 0;
+    for (int j = 0; j < S; ++j) {
+      const int x = sid[j];
+      const bool v = x >= 0 && x < E;
+      c += v && x == e;
+      off += v && x < e;
+    }
+    ws.cnt[e] = c;
+    ws.off[e] = off;
+  }
+  for (int i = tid; i < ns * T; i += blockDim.x) ws.pos_tok[S + i] = i % T;
+  if (tid >= 32) return;
+  const unsigned full = 0xFFFFFFFFu;
+  const int x = lane < S ? sid[lane] : -1;
+  const bool v = lane < S && x >= 0 && x < E;
+  if (lane < S && !v) raise_error(ws.err, kErrExpertRange);
+  const unsigned same = __match_any_sync(full, v ? x : -1 - lane);  // lanes with this slot's expert
+  const int rank = __popc(same & ((1u << lane) - 1u));            // earlier slots of that expert
+  const bool leader = v && (__ffs(same) - 1 == lane);              // the expert's first slot
+  int less = 0, dless = 0;  // valid slots / active experts with a lower expert id
+  for (int j = 0; j < S; ++j) {
+    const int xj = __shfl_sync(full, v ? x : 0x7FFFFFFF, j);
+    const int lj = __shfl_sync(full, leader ? 1 : 0, j);
+    less += xj < x;
+    dless += lj && xj < x;
+  }
+  const int routed_total = __popc(__ballot_sync(full, v));
+  const int n_routed = __popc(__ballot_sync(full, leader));
+  if (lane < S) {
+    if (v) {
+      const int p = less + rank;
+      ws.perm[p] = lane;
+      ws.slot_pos[lane] = p;
+      ws.pos_tok[p] = lane / k;
+    } else {
+      ws.slot_pos[lane] = -1;
+    }
+    if (lane >= routed_total) ws.pos_tok[lane] = 0;  // positions freed by invalid ids
+  }
+  if (leader) {  // active expert dless: one token tile of its slots
+    ws.active[dless] = x;
+    ws.tile_prefix[dless] = dless;
+    ws.tile_info[dless] = make_int4(x, less, __popc(same), 0);
+  }
+  if (lane < ns) {  // the shared experts after the routed ones, every token once
+    const int a = n_routed + lane;
+    ws.cnt[E + lane] = T;
+    ws.off[E + lane] = S + lane * T;
+    ws.active[a] = E + lane;
+    ws.tile_prefix[a] = a;
+    ws.tile_info[a] = make_int4(E + lane, S + lane * T, T, 0);
+  }
+  if (lane == 0) {
+    const int na = n_routed + ns;
+    ws.off[NE] = S + ns * T;
+    ws.tile_prefix[na] = na;
+    ws.n_active[0] = na;
+    ws.n_active[1] = na;
+  }
+}
+
 }  // namespace moe

@@ -439,3 +439,45 @@ def test_router_many_tokens_tensor_core(wl):
     ridx, _ = oracle.topk(lg, wl.top_k)
     assert np.array_equal(np.sort(idx[sure], 1), np.sort(ridx[sure], 1))
     L.close()
+
+
+# ---- small batches of at most 32 slots (the one-warp segments in the
+# preparation launch), with repeated experts across tokens and no or two
+# shared experts
+TINY_SLOTS = [
+    Workload("tiny_h256_i128_e16_k6_t1", 256, 128, 16, 6, 1, 1, seed=31, scale_lo=-6, scale_hi=-2),
+    Workload("tiny_h256_i128_e8_k8_s0_t4", 256, 128, 8, 8, 0, 4, seed=32, scale_lo=-6, scale_hi=-2),
+    Workload("tiny_h384_i256_e8_k6_s2_t5", 384, 256, 8, 6, 2, 5, seed=33, scale_lo=-6, scale_hi=-2),
+]
+
+
+@pytest.mark.parametrize("wl", TINY_SLOTS, ids=lambda w: w.name)
+def test_tiny_batches_step_forward_and_oracle(wl):
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    T, E, k = wl.tokens, wl.n_experts, wl.top_k
+    xt = sg.bf16_tensor(x)
+    y = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=gu.DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=gu.DEV)
+    lo = torch.empty((T, E), dtype=torch.float32, device=gu.DEV)
+    L.step(xt, T, y, idx=idx, w=w, logits_out=lo)
+    assert L.sync() == m.MOE_OK
+    y, idx, w, lo = (y.cpu().numpy().view(np.uint16), idx.cpu().numpy(), w.cpu().numpy(),
+                     lo.cpu().numpy())
+    ridx, rw = oracle.topk(lo.astype(np.float32), k)
+    assert np.array_equal(idx, ridx)
+    assert np.allclose(w, rw, rtol=2e-6, atol=1e-7)
+    assert np.array_equal(gu.run_forward(L, x, idx, w), y)
+    gu.assert_y_close(y, gu.oracle_layer(wl, 0, x, idx, rw))
+    # every token on the same few experts, in different slot orders
+    dup = np.stack([np.roll(np.arange(k, dtype=np.int32), t) for t in range(T)])
+    gu.assert_y_close(gu.run_forward(L, x, dup, rw), gu.oracle_layer(wl, 0, x, dup, rw))
+    # an out-of-range id is reported, then the next call is clean
+    bad = idx.copy()
+    bad[T - 1, k - 1] = E + 1
+    yb = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    L.forward(xt, T, torch.from_numpy(bad).to(gu.DEV), torch.from_numpy(rw.astype(np.float32)).to(gu.DEV), yb)
+    assert L.sync() == m.MOE_ERR_INTERNAL
+    assert np.array_equal(gu.run_forward(L, x, idx, w), y)
+    L.close()
