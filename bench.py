@@ -235,7 +235,10 @@ def run_ours(args):
     for L in Ls:
         L.set_option(m.MOE_OPT_PATH, args.path)
     n_in = args.steps + args.warmup
-    xs = sg.bf16_tensor(synth.activations(wl, tokens=n_in * T, stream=100 + rank), dev).view(n_in, T, H)
+    # distinct token blocks: one per step, up to 2^29 values in all (the
+    # largest prefill sweeps cycle through fewer; every block is far above L2)
+    n_x = max(1, min(n_in, (1 << 29) // (T * H)))
+    xs = sg.bf16_tensor(synth.activations(wl, tokens=n_x * T, stream=100 + rank), dev).view(n_x, T, H)
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
     wt = torch.empty((T, k), dtype=torch.float32, device=dev)
     bufs = [torch.empty((T, H), dtype=torch.int16, device=dev) for _ in range(3)]
@@ -252,7 +255,7 @@ def run_ours(args):
     def step(i, y_out=None):
         # one call per layer: moe_step = route + forward (for up to 64 tokens the
         # router, top-k, x codes and segments are a single launch)
-        x = xs[i]
+        x = xs[i % n_x]
         if nl == 1:
             Ls[0].step(x, T, bufs[0] if y_out is None else y_out)
             return
@@ -311,7 +314,7 @@ def run_ours(args):
     unions = []
     for i in range(args.warmup, n_in):
         if nl == 1:
-            Ls[0].route(xs[i], T, idx, wt)
+            Ls[0].route(xs[i % n_x], T, idx, wt)
             torch.cuda.synchronize()
             unions.append(len(np.unique(idx.cpu().numpy())))
     mean_union = float(np.mean(unions)) if unions else None
@@ -351,17 +354,17 @@ def run_ours(args):
     # end to end through the host entry point (copies inside the timed region)
     e2e = None
     if nl == 1:
-        xh = torch.empty((n_in, T, H), dtype=torch.int16).pin_memory()
+        xh = torch.empty((n_x, T, H), dtype=torch.int16).pin_memory()
         xh.copy_(xs.cpu())
         yh = torch.empty((T, H), dtype=torch.int16).pin_memory()
         for i in range(args.warmup):
-            Ls[0].forward_host(xh[i], T, yh)
+            Ls[0].forward_host(xh[i % n_x], T, yh)
         tt = 0.0
         for i in range(args.warmup, n_in):
             flush_l2(i)
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            Ls[0].forward_host(xh[i], T, yh)
+            Ls[0].forward_host(xh[i % n_x], T, yh)
             tt += time.perf_counter() - t0
         e2e = {"value": world * T * args.steps / tt, "unit": "tokens/s",
                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2}
@@ -384,7 +387,9 @@ def run_ours(args):
                            "experts": E, "top_k": k, "shared": wl.n_shared, "layers": nl,
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                            "launch": "cuda_graph" if args.graph else "stream",
-                           "l2": "flushed between steps (512 MB write + read), fresh tokens each step",
+                           "l2": "flushed between steps (512 MB write + read), " +
+                                 ("fresh tokens each step" if n_x == n_in else
+                                  f"{n_x} distinct token block(s) of {T * H * 2 / 1e6:.0f} MB cycled"),
                            "mean_expert_union": mean_union},
                 "layer_gbs": layer_gbs,
                 "kernels": {n: {"ms_per_launch": a[0] / a[1], "launches": a[1]}
@@ -392,7 +397,19 @@ def run_ours(args):
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": per_step_launches * args.steps, "clocks": clocks}
         if wl.tokens >= 512:
-            line["tflops"] = layer_flops(wl, T) / (ms_step / 1e3) / 1e12
+            # useful MMA work (routed + shared slots, no tile padding) against the
+            # tensor peaks of the FP8-activation kind and of FP4, each the measured
+            # bf16 GEMM rate times the nominal ratio (2x, 6x)
+            tf = layer_flops(wl, T) / (ms_step / 1e3) / 1e12
+            line["tflops"] = tf
+            fp8, fp4 = 2 * pk["bf16_tflops"], 6 * pk["bf16_tflops"]
+            up_ms = ktimes.get("ffn_up_mma", [0.0, 1])
+            up_tf = (2 / 3) * layer_flops(wl, T) / (up_ms[0] / up_ms[1] / 1e3) / 1e12 if up_ms[0] else None
+            line["tensor"] = {"useful_tflops": tf, "peak_fp8_kind": fp8, "frac_fp8_kind": tf / fp8,
+                              "peak_fp4": fp4, "frac_fp4": tf / fp4,
+                              "gate_up_kernel_tflops": up_tf,
+                              "gate_up_frac_fp8_kind": up_tf / fp8 if up_tf else None,
+                              "peak_src": pk["src"] + " bf16 GEMM x nominal ratio"}
         print(json.dumps(line), flush=True)
     for L in Ls:
         L.close()

@@ -66,7 +66,7 @@ typedef struct {
 } moe_mx_mat;
 
 /* Shapes.  hidden and inter: multiples of 128 (128..16384); n_experts 1..512;
- * top_k 1..8 and <= n_experts; n_shared 0..4; max_tokens 1..65535 bounds T
+ * top_k 1..8 and <= n_experts; n_shared 0..4; max_tokens 1..65536 bounds T
  * of every call and sizes the workspace.  Anything else returns
  * MOE_ERR_UNSUPPORTED. */
 typedef struct {

@@ -97,7 +97,7 @@ moe_status validate_config(const moe_config* c) {
                   c->inter >= 128 && c->inter <= 16384 && c->inter % 128 == 0 &&
                   c->n_experts >= 1 && c->n_experts <= 512 && c->top_k >= 1 && c->top_k <= 8 &&
                   c->top_k <= c->n_experts && c->n_shared >= 0 && c->n_shared <= 4 &&
-                  c->max_tokens >= 1 && c->max_tokens <= 65535;
+                  c->max_tokens >= 1 && c->max_tokens <= 65536;
   return ok ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 

@@ -68,8 +68,8 @@ __global__ void combine_kernel(const float* __restrict__ o, const int32_t* __res
                                const uint16_t* __restrict__ res, uint16_t* __restrict__ y) {
   pdl_wait();
   pdl_trigger();
-  const int t = blockIdx.y;
-  const int h = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  const int t = blockIdx.x;  // tokens on x: up to 2^31 - 1 of them
+  const int h = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (h >= H) return;
   const size_t S = (size_t)T * k;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -192,7 +192,7 @@ cudaError_t prepare_segments_kernel(int E) {
 cudaError_t launch_combine(const Workspace& ws, int T, int H, int k, int n_shared, const float* w,
                            const uint16_t* residual, uint16_t* y, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  dim3 grid((H / 4 + 255) / 256, T);
+  dim3 grid(T, (H / 4 + 255) / 256);
   { cudaError_t le_ = launch_pdl(combine_kernel, dim3(grid), dim3(256), 0, st, ws.o, ws.slot_pos, w, T, H, k, n_shared, residual, y); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }

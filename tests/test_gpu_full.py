@@ -16,7 +16,7 @@ import mxfp4_expert_ffn_gb300 as m
 import oracle
 import synth
 from synth import gpu as sg
-from synth.workloads import DECODE_T1, PREFILL_T4096, STACK8_T64, VERIFY_T5, VERIFY_T32
+from synth.workloads import DECODE_T1, PREFILL_T4096, PREFILL_T64K, STACK8_T64, VERIFY_T5, VERIFY_T32
 from tests import gpu_util as gu
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -63,6 +63,19 @@ def test_prefill_4096_tokens():
     L, W = gu.make_layer(wl)
     x = synth.activations(wl)
     sample = np.sort(np.random.default_rng(1).choice(wl.tokens, 16, replace=False))
+    _check_layer(wl, 0, L, x, sample)
+    L.close()
+    del W
+    _free()
+
+
+def test_prefill_65536_tokens():
+    """The largest batch a layer takes: routing of every token bit-exact given
+    the oracle's logits, the layer on sampled tokens."""
+    wl = PREFILL_T64K
+    L, W = gu.make_layer(wl)
+    x = synth.activations(wl)
+    sample = np.sort(np.random.default_rng(2).choice(wl.tokens, 8, replace=False))
     _check_layer(wl, 0, L, x, sample)
     L.close()
     del W
