@@ -57,6 +57,16 @@ def _declare(L):
     L.orc_bf16_round.restype = C.c_uint16
     L.orc_bf16_round.argtypes = [C.c_double]
     L.orc_quantize_act.argtypes = [P, C.c_int, C.c_int, P, P]
+    L.orc_e2m1_encode.restype = C.c_int
+    L.orc_e2m1_encode.argtypes = [C.c_double]
+    L.orc_block_exponent4.restype = C.c_int
+    L.orc_block_exponent4.argtypes = [C.c_double]
+    L.orc_quantize_block4.argtypes = [P, C.c_int, P, P]
+    L.orc_quantize_act4.argtypes = [P, C.c_int, C.c_int, P, P]
+    L.orc_expert_ffn_fmt.restype = C.c_int
+    L.orc_expert_ffn_fmt.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P, P, P, P, P]
+    L.orc_moe_layer_fmt.restype = C.c_int
+    L.orc_moe_layer_fmt.argtypes = [C.c_int] * 7 + [P, P, P, P, P, P, P, P, C.c_int]
     L.orc_router_logits.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P, P, C.c_int]
     L.orc_topk.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
     L.orc_exp_f32.restype = C.c_float
@@ -112,6 +122,33 @@ def quantize_block(v) -> tuple[np.ndarray, int]:
     s = np.zeros(1, np.uint8)
     lib().orc_quantize_block(_p(v), v.size, _p(q), _p(s))
     return q, int(s[0])
+
+
+def e2m1_encode(v: float) -> int:
+    return lib().orc_e2m1_encode(float(v))
+
+
+def block_exponent4(amax: float) -> int:
+    return lib().orc_block_exponent4(float(amax))
+
+
+def quantize_block4(v) -> tuple[np.ndarray, int]:
+    v = _c(v, np.float64)
+    q = np.zeros(v.size, np.uint8)
+    s = np.zeros(1, np.uint8)
+    lib().orc_quantize_block4(_p(v), v.size, _p(q), _p(s))
+    return q, int(s[0])
+
+
+def quantize_act4(x_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """FP4 variant: packed E2M1 codes [T][H/2] (even element in the low nibble)
+    and UE8M0 scale bytes [T][H/32]."""
+    x = _c(x_bits, np.uint16)
+    T, H = x.shape
+    q = np.zeros((T, H // 2), np.uint8)
+    s = np.zeros((T, H // 32), np.uint8)
+    lib().orc_quantize_act4(_p(x), T, H, _p(q), _p(s))
+    return q, s
 
 
 def bf16_value(b: int) -> float:
@@ -203,8 +240,9 @@ def _expert_struct(ex: dict | None, keep: list) -> _Expert:
     return s
 
 
-def expert_ffn(ex: dict, xq_row, xs_row) -> dict:
-    """One expert on one FP8-quantised token: h (fp64), its codes, o (fp64)."""
+def expert_ffn(ex: dict, xq_row, xs_row, act4: bool = False) -> dict:
+    """One expert on one quantised token (one code per element: E4M3, or E2M1
+    with act4): h (fp64), its codes, o (fp64)."""
     keep: list = []
     st = _expert_struct(ex, keep)
     I, H2 = ex["gate_codes"].shape
@@ -215,16 +253,18 @@ def expert_ffn(ex: dict, xq_row, xs_row) -> dict:
     hq = np.zeros(I, np.uint8)
     hs = np.zeros(I // 32, np.uint8)
     o = np.zeros(H, np.float64)
-    rc = lib().orc_expert_ffn(C.byref(st), H, I, _p(xq), _p(xs), _p(h), _p(hq), _p(hs), _p(o))
+    rc = lib().orc_expert_ffn_fmt(C.byref(st), H, I, int(act4), _p(xq), _p(xs), _p(h), _p(hq), _p(hs),
+                                  _p(o))
     if rc != 0:
         raise ValueError("oracle: expert weights missing")
     return {"h": h, "hq": hq, "hs": hs, "o": o}
 
 
 def moe_layer(x_bits, idx, w, experts: dict, shared: list, n_experts: int, inter: int,
-              residual=None, threads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+              residual=None, threads: int = 0, act4: bool = False) -> tuple[np.ndarray, np.ndarray]:
     """The layer on T tokens.  experts maps expert id -> six arrays (only the
-    ids that idx uses are needed).  Returns (y bf16 bits [T][H], y fp64)."""
+    ids that idx uses are needed); act4 selects the FP4-activation variant.
+    Returns (y bf16 bits [T][H], y fp64)."""
     x = _c(x_bits, np.uint16)
     T, H = x.shape
     ix = _c(idx, np.int32)
@@ -240,7 +280,7 @@ def moe_layer(x_bits, idx, w, experts: dict, shared: list, n_experts: int, inter
     res = None if residual is None else _c(residual, np.uint16)
     y = np.zeros((T, H), np.uint16)
     y64 = np.zeros((T, H), np.float64)
-    rc = lib().orc_moe_layer(T, H, inter, n_experts, k, len(shared), _p(x), _p(ix), _p(ww),
+    rc = lib().orc_moe_layer_fmt(T, H, inter, n_experts, k, len(shared), int(act4), _p(x), _p(ix), _p(ww),
                              C.cast(arr, C.c_void_p), C.cast(sh, C.c_void_p),
                              None if res is None else _p(res), _p(y), _p(y64),
                              threads or max_threads())

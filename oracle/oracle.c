@@ -151,6 +151,66 @@ void orc_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s) {
     }
 }
 
+/* ------------------------------------------------- FP4 activations (variant) */
+/* The FP4-activation variant quantises x and h to E2M1 per 32 with a UE8M0
+ * scale instead of E4M3 (reading: the same dynamic block rule with the E2M1
+ * maximum 6 in place of 448; the pages measure FP4-block activation error as
+ * large, so this stays an option).  Finite inputs only. */
+
+/* Nearest E2M1 value, ties to the even code, saturating at 6: an exhaustive
+ * search over the eight non-negative codes.  The sign is kept for every input,
+ * so a negative value that rounds to zero gives code 8. */
+int orc_e2m1_encode(double v) {
+  int sign = signbit(v) ? 1 : 0;
+  double a = fabs(v);
+  int best = 0;
+  double bestd = INFINITY;
+  if (a > 6.0) return (sign << 3) | 7;
+  for (int c = 0; c <= 7; ++c) {
+    double d = fabs(orc_e2m1_value(c) - a);
+    if (d < bestd || (d == bestd && (c % 2) == 0)) {
+      best = c;
+      bestd = d;
+    }
+  }
+  return (sign << 3) | best;
+}
+
+/* The block exponent of the FP4 variant: the smallest integer e with
+ * amax <= 6 * 2^e, limited to [-127, 127]; an all-zero block takes e = 0. */
+int orc_block_exponent4(double amax) {
+  int e = -127;
+  if (amax == 0.0) return 0;
+  while (e < 127 && amax > ldexp(6.0, e)) ++e;
+  return e;
+}
+
+/* Quantise n values (one block) to E2M1 codes (one per byte, 0..15) with a
+ * shared UE8M0 scale. */
+void orc_quantize_block4(const double* v, int n, uint8_t* q, uint8_t* s) {
+  double amax = 0.0;
+  for (int i = 0; i < n; ++i)
+    if (fabs(v[i]) > amax) amax = fabs(v[i]);
+  int e = orc_block_exponent4(amax);
+  *s = (uint8_t)(e + 127);
+  for (int i = 0; i < n; ++i) q[i] = (uint8_t)orc_e2m1_encode(ldexp(v[i], -e));
+}
+
+/* Per-32 FP4 quantisation of bf16 activations x[T][H] into packed codes
+ * q[T][H/2] (element 2i in the low nibble of byte i, as the weights) and
+ * scale bytes s[T][H/32]. */
+void orc_quantize_act4(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s) {
+  double blk[32];
+  uint8_t c[32];
+  for (int t = 0; t < T; ++t)
+    for (int b = 0; b < H / 32; ++b) {
+      for (int i = 0; i < 32; ++i) blk[i] = orc_bf16_value(x[(size_t)t * H + b * 32 + i]);
+      orc_quantize_block4(blk, 32, c, s + (size_t)t * (H / 32) + b);
+      for (int i = 0; i < 16; ++i)
+        q[(size_t)t * (H / 2) + b * 16 + i] = (uint8_t)(c[2 * i] | (c[2 * i + 1] << 4));
+    }
+}
+
 /* ------------------------------------------------------------------ routing */
 
 /* Router logits l[t][e] = sum_h x[t][h] * W[e][h] + b[e], in fp64, then
@@ -313,21 +373,36 @@ static double orc_mx_weight(const orc_mat* m, int K, int r, int c) {
   return orc_e2m1_value(code) * orc_ue8m0_table[m->scales[(size_t)r * (K / 32) + c / 32]];
 }
 
-/* One expert on one token whose activation is already FP8-quantised:
+/* One activation code (one per byte) of the given format: E4M3 (act4 = 0) or
+ * E2M1 (act4 = 1). */
+static double orc_act_value(int act4, uint8_t code) {
+  return act4 ? orc_e2m1_value(code & 15) : orc_e4m3_value(code);
+}
+
+static void orc_quantize_block_fmt(int act4, const double* v, int n, uint8_t* q, uint8_t* s) {
+  if (act4)
+    orc_quantize_block4(v, n, q, s);
+  else
+    orc_quantize_block(v, n, q, s);
+}
+
+/* One expert on one token whose activation is already quantised (one code per
+ * element, E4M3 or, act4 = 1, E2M1):
  *   g = Wg x^, u = Wu x^, h = silu(g) * u = g / (1 + e^-g) * u,
- *   h quantised per 32 (same rule as x), o = Wd h^.
+ *   h quantised per 32 (same rule and format as x), o = Wd h^.
  * (Readings: SwiGLU with silu on the gate projection and no clamp; h is
- * FP8-quantised before the down projection like every activation under the
+ * quantised before the down projection like every activation under the
  * checkpoint's dynamic scheme.)  h_out (I), hq (I), hs (I/32) may be NULL. */
-int orc_expert_ffn(const orc_expert* ex, int H, int I, const uint8_t* xq, const uint8_t* xs,
-                   double* h_out, uint8_t* hq_out, uint8_t* hs_out, double* o) {
+int orc_expert_ffn_fmt(const orc_expert* ex, int H, int I, int act4, const uint8_t* xq,
+                       const uint8_t* xs, double* h_out, uint8_t* hq_out, uint8_t* hs_out,
+                       double* o) {
   if (!ex || !ex->gate.codes || !ex->up.codes || !ex->down.codes) return -1;
   double* xh = (double*)malloc(sizeof(double) * (size_t)H);
   double* h = (double*)malloc(sizeof(double) * (size_t)I);
   double* hh = (double*)malloc(sizeof(double) * (size_t)I);
   uint8_t* hq = (uint8_t*)malloc((size_t)I);
   uint8_t* hs = (uint8_t*)malloc((size_t)I / 32);
-  for (int c = 0; c < H; ++c) xh[c] = orc_e4m3_value(xq[c]) * orc_ue8m0_value(xs[c / 32]);
+  for (int c = 0; c < H; ++c) xh[c] = orc_act_value(act4, xq[c]) * orc_ue8m0_value(xs[c / 32]);
   for (int i = 0; i < I; ++i) {
     double g = 0.0, u = 0.0;
     for (int c = 0; c < H; ++c) {
@@ -336,8 +411,8 @@ int orc_expert_ffn(const orc_expert* ex, int H, int I, const uint8_t* xq, const 
     }
     h[i] = g / (1.0 + exp(-g)) * u;
   }
-  for (int b = 0; b < I / 32; ++b) orc_quantize_block(h + b * 32, 32, hq + b * 32, hs + b);
-  for (int i = 0; i < I; ++i) hh[i] = orc_e4m3_value(hq[i]) * orc_ue8m0_value(hs[i / 32]);
+  for (int b = 0; b < I / 32; ++b) orc_quantize_block_fmt(act4, h + b * 32, 32, hq + b * 32, hs + b);
+  for (int i = 0; i < I; ++i) hh[i] = orc_act_value(act4, hq[i]) * orc_ue8m0_value(hs[i / 32]);
   for (int r = 0; r < H; ++r) {
     double acc = 0.0;
     for (int i = 0; i < I; ++i) acc += orc_mx_weight(&ex->down, I, r, i) * hh[i];
@@ -354,16 +429,22 @@ int orc_expert_ffn(const orc_expert* ex, int H, int I, const uint8_t* xq, const 
   return 0;
 }
 
+/* The FP8-activation expert (the layer's definition). */
+int orc_expert_ffn(const orc_expert* ex, int H, int I, const uint8_t* xq, const uint8_t* xs,
+                   double* h_out, uint8_t* hq_out, uint8_t* hs_out, double* o) {
+  return orc_expert_ffn_fmt(ex, H, I, 0, xq, xs, h_out, hq_out, hs_out, o);
+}
+
 /* The layer on T tokens given the routing (idx[T][k], w[T][k]):
  *   y[t] = bf16( sum_shared o_s + sum_j w[t][j] * o_{idx[t][j]} )
  * and, with a residual r, y[t] = bf16(r[t] + bf16(...)).  The shared experts
  * see every token with weight 1.  experts[e] may hold NULL pointers for
  * experts no token uses; returns -1 if a used expert is missing.
  * y64 (may be NULL) receives the sum before bf16 rounding. */
-int orc_moe_layer(int T, int H, int I, int E, int k, int n_shared, const uint16_t* x,
-                  const int32_t* idx, const double* w, const orc_expert* experts,
-                  const orc_expert* shared, const uint16_t* residual, uint16_t* y, double* y64,
-                  int nthreads) {
+int orc_moe_layer_fmt(int T, int H, int I, int E, int k, int n_shared, int act4, const uint16_t* x,
+                      const int32_t* idx, const double* w, const orc_expert* experts,
+                      const orc_expert* shared, const uint16_t* residual, uint16_t* y, double* y64,
+                      int nthreads) {
   int* bad = (int*)calloc((size_t)(T > 0 ? T : 1), sizeof(int));
   int status = 0;
 #ifdef _OPENMP
@@ -374,15 +455,21 @@ int orc_moe_layer(int T, int H, int I, int E, int k, int n_shared, const uint16_
     uint8_t* xs = (uint8_t*)malloc((size_t)H / 32);
     double* o = (double*)malloc(sizeof(double) * (size_t)H);
     double* acc = (double*)calloc((size_t)H, sizeof(double));
-    orc_quantize_act(x + (size_t)t * H, 1, H, xq, xs);
+    {
+      double blk[32];
+      for (int b = 0; b < H / 32; ++b) {
+        for (int i = 0; i < 32; ++i) blk[i] = orc_bf16_value(x[(size_t)t * H + b * 32 + i]);
+        orc_quantize_block_fmt(act4, blk, 32, xq + b * 32, xs + b);
+      }
+    }
     for (int s = 0; s < n_shared; ++s) {
-      if (orc_expert_ffn(&shared[s], H, I, xq, xs, NULL, NULL, NULL, o) != 0) bad[t] = 1;
+      if (orc_expert_ffn_fmt(&shared[s], H, I, act4, xq, xs, NULL, NULL, NULL, o) != 0) bad[t] = 1;
       else
         for (int r = 0; r < H; ++r) acc[r] += o[r];
     }
     for (int j = 0; j < k; ++j) {
       int e = idx[(size_t)t * k + j];
-      if (e < 0 || e >= E || orc_expert_ffn(&experts[e], H, I, xq, xs, NULL, NULL, NULL, o) != 0) {
+      if (e < 0 || e >= E || orc_expert_ffn_fmt(&experts[e], H, I, act4, xq, xs, NULL, NULL, NULL, o) != 0) {
         bad[t] = 1;
         continue;
       }
@@ -405,6 +492,15 @@ int orc_moe_layer(int T, int H, int I, int E, int k, int n_shared, const uint16_
   free(bad);
   (void)nthreads;
   return status;
+}
+
+/* The layer with FP8 activations (its definition). */
+int orc_moe_layer(int T, int H, int I, int E, int k, int n_shared, const uint16_t* x,
+                  const int32_t* idx, const double* w, const orc_expert* experts,
+                  const orc_expert* shared, const uint16_t* residual, uint16_t* y, double* y64,
+                  int nthreads) {
+  return orc_moe_layer_fmt(T, H, I, E, k, n_shared, 0, x, idx, w, experts, shared, residual, y, y64,
+                           nthreads);
 }
 
 /* Root-mean-square normalisation of each token row (no learned gain):

@@ -101,3 +101,36 @@ def bf16_bits_torch(v: np.ndarray) -> np.ndarray:
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---- FP4-activation variant: closed forms for the E2M1 rounding and the
+# block exponent (amax <= 6 * 2**e), independent of the oracle's search
+
+def block_exponent4_closed_form(amax: np.ndarray) -> np.ndarray:
+    """Smallest e with amax <= 6 * 2**e: with amax = f * 2**E (f in [0.5, 1))
+    and 6 = 0.75 * 2**3, e = E - 3 if f <= 0.75 else E - 2."""
+    f, E = np.frexp(np.asarray(amax, dtype=np.float64))
+    e = np.where(f <= 0.75, E - 3, E - 2)
+    e = np.clip(e, -127, 127)
+    return np.where(np.asarray(amax) == 0, 0, e).astype(np.int64)
+
+
+def e2m1_round_closed_form(v: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 value (grid 0, .5, 1, 1.5, 2, 3, 4, 6), ties to the even
+    code, saturating at 6: spacing 0.5 below 2, 1 on [2, 4), 2 on [4, 6], and
+    on each piece the code's parity is the parity of the grid index, so
+    numpy's half-to-even rounding of a / spacing is the tie rule."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    r = np.where(a < 2, np.round(a * 2) / 2, np.where(a < 4, np.round(a), 2 * np.round(a / 2)))
+    r = np.minimum(r, 6.0)
+    return np.copysign(r, v)
+
+
+def fp4_block_quant_f64(v: np.ndarray) -> np.ndarray:
+    """Dequantised per-32 FP4 values of fp64 inputs (closed form)."""
+    v = np.asarray(v, dtype=np.float64)
+    blocks = v.reshape(v.shape[:-1] + (v.shape[-1] // 32, 32))
+    e = block_exponent4_closed_form(np.abs(blocks).max(axis=-1))
+    r = e2m1_round_closed_form(np.ldexp(blocks, -e[..., None]))
+    return np.ldexp(r, e[..., None]).reshape(v.shape)

@@ -449,3 +449,112 @@ def test_rmsnorm_closed_form():
     # scale invariance by a power of two is exact
     x2 = synth.f32_to_bf16_bits((mx_ref.bf16_to_f64(x) * 8).astype(np.float32))
     assert np.array_equal(oracle.rmsnorm(x2, 0.0), oracle.rmsnorm(x, 0.0))
+
+
+# ---- FP4-activation variant (x and h as E2M1 per 32 with a UE8M0 scale)
+
+def test_e2m1_encode_grid_midpoints_and_sign():
+    tab = mx_ref.e2m1_table()
+    for c in range(8):                       # every grid value encodes to itself
+        assert oracle.e2m1_encode(tab[c]) == c
+        assert oracle.e2m1_encode(-tab[c]) == c | 8
+    # midpoints between neighbours go to the even code
+    for lo, hi, want in [(0, 1, 0), (1, 2, 2), (2, 3, 2), (3, 4, 4), (4, 5, 4), (5, 6, 6), (6, 7, 6)]:
+        assert oracle.e2m1_encode((tab[lo] + tab[hi]) / 2) == want, (lo, hi)
+    assert oracle.e2m1_encode(7.0) == 7 and oracle.e2m1_encode(-100.0) == 15   # saturate
+    assert oracle.e2m1_encode(-0.0) == 8 and oracle.e2m1_encode(-0.1) == 8      # sign kept at zero
+
+
+def test_e2m1_encode_random_doubles_match_closed_form():
+    rng = np.random.default_rng(17)
+    v = rng.uniform(-7, 7, 20000)
+    v[:64] = np.repeat(np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0]), 8) * np.tile([1, -1], 32)
+    tab = mx_ref.e2m1_table()
+    got = np.array([tab[oracle.e2m1_encode(x)] for x in v])
+    assert np.array_equal(got, mx_ref.e2m1_round_closed_form(v))
+
+
+def test_block_exponent4_matches_closed_form():
+    rng = np.random.default_rng(19)
+    a = np.concatenate([
+        np.abs(rng.standard_normal(2000)) * np.ldexp(1.0, rng.integers(-140, 140, 2000)),
+        6.0 * np.ldexp(1.0, np.arange(-127, 127)),            # exactly on the boundary
+        np.nextafter(6.0 * np.ldexp(1.0, np.arange(-120, 120)), np.inf),
+        [0.0, 1e-45, 3e38]])
+    got = np.array([oracle.block_exponent4(x) for x in a])
+    assert np.array_equal(got, mx_ref.block_exponent4_closed_form(a))
+
+
+def test_quantize_act4_matches_closed_form_and_packs_low_nibble_first():
+    wl = TINY
+    x = synth.activations(wl, tokens=16)
+    x[0, :32] = 0                          # an all-zero block: scale 2^0, codes 0
+    q, s = oracle.quantize_act4(x)
+    assert q.shape == (16, wl.hidden // 2) and s.shape == (16, wl.hidden // 32)
+    assert s[0, 0] == 127 and (q[0, :16] == 0).all()
+    tab = mx_ref.e2m1_table()
+    codes = np.empty((16, wl.hidden), np.uint8)
+    codes[:, 0::2], codes[:, 1::2] = q & 15, q >> 4
+    deq = tab[codes] * np.repeat(np.ldexp(1.0, s.astype(np.int64) - 127), 32, axis=1)
+    assert np.array_equal(deq, mx_ref.fp4_block_quant_f64(mx_ref.bf16_to_f64(x)))
+
+
+def _brute_dense_layer4(x_bits, idx, w, experts, shared):
+    """Independent evaluation of the FP4 variant: numpy matmuls over all
+    experts with the closed-form FP4 activation rounding."""
+    xh = mx_ref.fp4_block_quant_f64(mx_ref.bf16_to_f64(x_bits))
+    T = xh.shape[0]
+
+    def ffn(d):
+        g = xh @ d["gate"].T
+        u = xh @ d["up"].T
+        h = g / (1 + np.exp(-g)) * u
+        return mx_ref.fp4_block_quant_f64(h) @ d["down"].T
+
+    acc = sum(ffn(_dense(s)) for s in shared)
+    for e, ex in experts.items():
+        m = np.zeros(T)
+        for j in range(idx.shape[1]):
+            m += np.where(idx[:, j] == e, w[:, j], 0.0)
+        acc = acc + m[:, None] * ffn(_dense(ex))
+    return acc
+
+
+def test_brute_force_dense_tiny_layer_fp4_activations():
+    wl = TINY
+    experts, shared = _tiny_bank(wl)
+    x = synth.activations(wl)
+    lg = oracle.router_logits(x, synth.router_weights(wl))
+    idx, w = oracle.topk(lg, wl.top_k)
+    y, y64 = oracle.moe_layer(x, idx, w, experts, shared, wl.n_experts, wl.inter, act4=True)
+    ref = _brute_dense_layer4(x, idx, w, experts, shared)
+    assert np.allclose(y64, ref, rtol=1e-9, atol=1e-9 * np.abs(ref).max())
+    # and it is a different layer from the FP8 one (the variant is not a no-op)
+    _, y64_8 = oracle.moe_layer(x, idx, w, experts, shared, wl.n_experts, wl.inter)
+    assert not np.allclose(y64, y64_8, rtol=1e-3, atol=0)
+
+
+def test_identity_like_expert_closed_form_fp4_activations():
+    H, I, E = 256, 128, 4
+    rng = np.random.default_rng(23)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((6, H)).astype(np.float32) * 3)
+    experts = {e: _identity_expert(H, I, e - 1, 1 - e, e % 2) for e in range(E)}
+    shared = [_identity_expert(H, I, 0, 0, -1)]
+    idx = np.array([[0, 1], [2, 3], [1, 0], [3, 2], [0, 3], [2, 1]], np.int32)
+    w = np.array([[0.75, 0.25]] * 6)
+    _, y64 = oracle.moe_layer(x, idx, w, experts, shared, E, I, act4=True)
+    xh = mx_ref.fp4_block_quant_f64(mx_ref.bf16_to_f64(x))[:, :I]
+
+    def expert_out(a, b, c):
+        h = (2.0 ** a * xh) / (1 + np.exp(-(2.0 ** a * xh))) * (2.0 ** b * xh)
+        o = np.zeros((x.shape[0], H))
+        o[:, :I] = 2.0 ** c * mx_ref.fp4_block_quant_f64(h)
+        return o
+
+    ref = expert_out(0, 0, -1)
+    for j in range(2):
+        for t in range(x.shape[0]):
+            e = idx[t, j]
+            ref[t] += w[t, j] * expert_out(e - 1, 1 - e, e % 2)[t]
+    assert np.allclose(y64, ref, rtol=1e-12, atol=0)
+    assert (y64[:, I:] == 0).all()
