@@ -45,6 +45,8 @@ def parse():
     p.add_argument("--path", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor cores")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--graph", type=int, default=1, help="1: launch each step as a captured CUDA graph, 0: stream launches")
+    p.add_argument("--act", default="fp8", choices=["fp8", "fp4"],
+                   help="activation format: fp8 (the layer) or fp4 (the FP4-activation variant)")
     return p.parse_args()
 
 
@@ -234,6 +236,8 @@ def run_ours(args):
     Ls = [m.Layer(H, wl.inter, E, k, wl.n_shared, T, W[l]) for l in range(nl)]
     for L in Ls:
         L.set_option(m.MOE_OPT_PATH, args.path)
+        if args.act == "fp4":
+            L.set_act_format(m.MOE_ACT_FP4)
     n_in = args.steps + args.warmup
     # distinct token blocks: one per step, up to 2^29 values in all (the
     # largest prefill sweeps cycle through fewer; every block is far above L2)
@@ -382,8 +386,8 @@ def run_ours(args):
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "fp4xfp8->f32", "data": "synthetic",
-                "config": {"workload": wl.name, "tokens": T, "hidden": H, "inter": wl.inter,
+                "dtype": "fp4xfp4->f32" if args.act == "fp4" else "fp4xfp8->f32", "data": "synthetic",
+                "config": {"workload": wl.name + ("_act_fp4" if args.act == "fp4" else ""), "tokens": T, "hidden": H, "inter": wl.inter,
                            "experts": E, "top_k": k, "shared": wl.n_shared, "layers": nl,
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                            "launch": "cuda_graph" if args.graph else "stream",

@@ -155,6 +155,17 @@ moe_status moe_forward_host(moe_layer* layer, const void* x_host, int32_t T, voi
 moe_status moe_quantize_act(moe_layer* layer, const void* x, int32_t T, uint8_t* q, uint8_t* s,
                             void* stream);
 
+/* The FP4-activation variant's quantiser (MOE_OPT_ACT_FORMAT): q [T][H/2]
+ * packed E2M1 codes (element 2i in the low nibble of byte i, as the weight
+ * codes) and s [T][H/32] UE8M0 bytes, by the rule: per block of 32, e = the
+ * smallest integer with max|x| <= 6 * 2^e (e = 0 for an all-zero block,
+ * limited to [-127, 127]), s = e + 127, code = E2M1(x / 2^e) rounded to
+ * nearest, ties to the even code, sign kept for zero results.  Inputs must be
+ * finite; H a multiple of 256 (MOE_ERR_UNSUPPORTED otherwise); q 4-byte
+ * aligned. */
+moe_status moe_quantize_act4(moe_layer* layer, const void* x, int32_t T, uint8_t* q, uint8_t* s,
+                             void* stream);
+
 /* The expert segments the forward pass builds from topk_idx [T][k]:
  * offsets [E+1] (offsets[e] = number of slots routed to experts below e) and
  * perm [T*k], the slots s = t*k + j listed expert by expert, in increasing
@@ -218,9 +229,22 @@ moe_status moe_sync(moe_layer* layer, void* stream);
  *  MOE_OPT_ROUTED_SCALE  routed weights are multiplied by this factor (the
  *                  shared experts keep weight 1): value = the IEEE-754 bits
  *                  of a positive finite float in the low 32 bits; default 1.
+ *  MOE_OPT_ACT_FORMAT  MOE_ACT_FP8 (default): x and h quantised to E4M3 per
+ *                  32, the checkpoint's dynamic scheme; MOE_ACT_FP4: both as
+ *                  E2M1 per 32 (moe_quantize_act4's rule) and the expert
+ *                  GEMMs on the FP4 x FP4 tensor-core kind -- a different,
+ *                  noisier layer (the pages measure FP4 blocks of 32 losing
+ *                  far more than FP8: ai.rs, "What remains is the reference
+ *                  rounding itself", the table of round-trip errors), kept as
+ *                  an option for compute-bound batches.  Tensor-core path
+ *                  only: MOE_ERR_UNSUPPORTED when H or I is not a multiple of
+ *                  256 or the layer has no tensor-core path; MOE_OPT_PATH = 1
+ *                  (SIMT) is refused while it is set.
  * moe_route_static always uses softmax scoring with scale 1.             */
-enum { MOE_OPT_PATH = 1, MOE_OPT_TIMING = 2, MOE_OPT_SCORING = 3, MOE_OPT_ROUTED_SCALE = 4 };
+enum { MOE_OPT_PATH = 1, MOE_OPT_TIMING = 2, MOE_OPT_SCORING = 3, MOE_OPT_ROUTED_SCALE = 4,
+       MOE_OPT_ACT_FORMAT = 5 };
 enum { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 };
+enum { MOE_ACT_FP8 = 0, MOE_ACT_FP4 = 1 };
 moe_status moe_set_option(moe_layer* layer, int32_t option, int64_t value);
 
 /* Per-kernel timing gathered while MOE_OPT_TIMING is on (synchronises the

@@ -15,13 +15,14 @@ LIB_PATH = os.path.join(_HERE, "libmoe_ffn.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_INTERNAL = 4, 5, 6
-MOE_OPT_PATH, MOE_OPT_TIMING, MOE_OPT_SCORING, MOE_OPT_ROUTED_SCALE = 1, 2, 3, 4
+MOE_OPT_PATH, MOE_OPT_TIMING, MOE_OPT_SCORING, MOE_OPT_ROUTED_SCALE, MOE_OPT_ACT_FORMAT = 1, 2, 3, 4, 5
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
+MOE_ACT_FP8, MOE_ACT_FP4 = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_MMA = 0, 1, 2
 
 # every symbol include/moe_ffn.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward", "moe_step",
-           "moe_forward_host", "moe_quantize_act", "moe_segments", "moe_rmsnorm", "moe_sync",
+           "moe_forward_host", "moe_quantize_act", "moe_quantize_act4", "moe_segments", "moe_rmsnorm", "moe_sync",
            "moe_set_option", "moe_get_kernel_times", "moe_status_string", "moe_abi_version",
            "moe_route_static")
 ROUTE_STATIC_MAX_LOGITS = 64 * 512
@@ -69,6 +70,7 @@ def lib():
         L.moe_step.argtypes = [P, P, I32, P, P, P, P, P, P]
         L.moe_forward_host.argtypes = [P, P, I32, P, P]
         L.moe_quantize_act.argtypes = [P, P, I32, P, P, P]
+        L.moe_quantize_act4.argtypes = [P, P, I32, P, P, P]
         L.moe_segments.argtypes = [P, P, I32, P, P, P]
         L.moe_rmsnorm.argtypes = [P, I32, I32, C.c_float, P, P]
         L.moe_sync.argtypes = [P, P]
@@ -159,6 +161,11 @@ def moe_quantize_act(h, x, T, q, s, stream=None) -> None:
            "moe_quantize_act")
 
 
+def moe_quantize_act4(h, x, T, q, s, stream=None) -> None:
+    _check(lib().moe_quantize_act4(h, ptr(x), T, ptr(q), ptr(s), stream_handle(stream)),
+           "moe_quantize_act4")
+
+
 def moe_segments(h, topk_idx, T, offsets, perm, stream=None) -> None:
     _check(lib().moe_segments(h, ptr(topk_idx), T, ptr(offsets), ptr(perm), stream_handle(stream)),
            "moe_segments")
@@ -227,6 +234,13 @@ class Layer:
 
     def quantize_act(self, x, T, q, s, stream=None):
         moe_quantize_act(self.handle, x, T, q, s, stream)
+
+    def quantize_act4(self, x, T, q, s, stream=None):
+        moe_quantize_act4(self.handle, x, T, q, s, stream)
+
+    def set_act_format(self, fmt: int):
+        """MOE_ACT_FP8 (the layer's definition) or MOE_ACT_FP4 (the variant)."""
+        moe_set_option(self.handle, MOE_OPT_ACT_FORMAT, fmt)
 
     def segments(self, idx, T, offsets, perm, stream=None):
         moe_segments(self.handle, idx, T, offsets, perm, stream)

@@ -276,6 +276,7 @@ moe_status moe_set_option(moe_layer* L, int32_t option, int64_t value) {
   if (option == MOE_OPT_PATH) {
     if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
     if (value == 2 && !L->maps) return MOE_ERR_UNSUPPORTED;
+    if (value == 1 && L->act_format == MOE_ACT_FP4) return MOE_ERR_UNSUPPORTED;  // no SIMT FP4 path
     L->path = (int)value;
     return MOE_OK;
   }
@@ -291,6 +292,13 @@ moe_status moe_set_option(moe_layer* L, int32_t option, int64_t value) {
     memcpy(&f, &bits, sizeof f);
     if (!(f > 0.f) || f > 3.0e38f) return MOE_ERR_INVALID_ARG;  // positive, finite (NaN fails too)
     L->routed_scale = f;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_ACT_FORMAT) {
+    if (value != MOE_ACT_FP8 && value != MOE_ACT_FP4) return MOE_ERR_INVALID_ARG;
+    // FP4 activations run on the tensor cores only, for H and I multiples of 256
+    if (value == MOE_ACT_FP4 && (!L->maps || !mma_act4_supported(L->cfg))) return MOE_ERR_UNSUPPORTED;
+    L->act_format = (int)value;
     return MOE_OK;
   }
   if (option == MOE_OPT_TIMING) {
@@ -404,6 +412,8 @@ bool use_mma(const moe_layer* L, int T) {
   return L->path != 1;
 }
 
+bool act4_of(const moe_layer* L) { return L->act_format == MOE_ACT_FP4; }
+
 // gate/up, down and combine on the tensor cores, once the segments and the
 // activation codes are in the workspace.
 moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool gather, const float* w,
@@ -413,7 +423,7 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool gather, const float* w
   cudaError_t e;
   {
     TimedScope ts(L, st, "ffn_up_mma");
-    e = launch_ffn_mma(*L->maps, bank, 0, bn, gather, L->ws, L->num_sms, st);
+    e = launch_ffn_mma(*L->maps, bank, 0, bn, gather, L->ws, L->num_sms, st, nullptr, act4_of(L));
   }
   if (e != cudaSuccess) return cuda_fail(e);
   if (gather && c.n_shared > 0) {
@@ -422,11 +432,11 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool gather, const float* w
     const CombineArgs cmb{T, c.top_k, c.n_shared, w, static_cast<const uint16_t*>(residual),
                           static_cast<uint16_t*>(y)};
     TimedScope ts(L, st, "ffn_down_mma");
-    return cuda_fail(launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, &cmb));
+    return cuda_fail(launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, &cmb, act4_of(L)));
   }
   {
     TimedScope ts(L, st, "ffn_down_mma");
-    e = launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st);
+    e = launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, nullptr, act4_of(L));
   }
   if (e != cudaSuccess) return cuda_fail(e);
   {
@@ -449,7 +459,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
       TimedScope ts(L, st, "prep");
       e = launch_prep(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts, c.top_k, c.n_shared,
                       bn, nullptr, nullptr, scoring_of(L), nullptr, const_cast<int32_t*>(idx), nullptr, false,
-                      L->ws, st);
+                      act4_of(L), L->ws, st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return ffn_tail(L, T, bn, true, w, residual, y, st);
@@ -464,11 +474,12 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
     {
       TimedScope ts(L, st, "quantize_gather");
       e = launch_quantize_gather(static_cast<const uint16_t*>(x), P, c.hidden, L->ws.pos_tok,
-                                 L->ws.xg, L->ws.xgs, st);
+                                 L->ws.xg, L->ws.xgs, act4_of(L), st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return ffn_tail(L, T, bn, false, w, residual, y, st);
   } else {
+    if (act4_of(L)) return MOE_ERR_UNSUPPORTED;  // FP4 activations: tensor cores only
     {
       TimedScope ts(L, st, "quantize_act");
       e = launch_quantize_act(static_cast<const uint16_t*>(x), T, c.hidden, L->ws.xq, L->ws.xs, st);
@@ -506,7 +517,8 @@ moe_status step_impl(moe_layer* L, const void* x, int32_t T, const void* residua
     {
       TimedScope ts(L, st, "prep");
       e = launch_prep(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts, c.top_k, c.n_shared,
-                      bn, L->w.router_w, L->w.router_b, scoring_of(L), logits_out, idx, w, true, L->ws, st);
+                      bn, L->w.router_w, L->w.router_b, scoring_of(L), logits_out, idx, w, true, act4_of(L),
+                      L->ws, st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return ffn_tail(L, T, bn, true, w, residual, y, st);
@@ -588,6 +600,19 @@ moe_status moe_quantize_act(moe_layer* L, const void* x, int32_t T, uint8_t* q, 
   TimedScope ts(L, static_cast<cudaStream_t>(stream), "quantize_act");
   return cuda_fail(launch_quantize_act(static_cast<const uint16_t*>(x), T, L->cfg.hidden, q, s,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_quantize_act4(moe_layer* L, const void* x, int32_t T, uint8_t* q, uint8_t* s,
+                             void* stream) {
+  moe_status st = check_tokens(L, T);
+  if (st != MOE_OK || T == 0) return st;
+  if (!x || !q || !s || !aligned(x, 16) || !aligned(q, 4)) return MOE_ERR_INVALID_ARG;
+  if (L->cfg.hidden % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  DeviceGuard g(L->device);
+  if (g.status != cudaSuccess) return cuda_fail(g.status);
+  TimedScope ts(L, static_cast<cudaStream_t>(stream), "quantize_act4");
+  return cuda_fail(launch_quantize_act4(static_cast<const uint16_t*>(x), T, L->cfg.hidden, q, s,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_segments(moe_layer* L, const int32_t* topk_idx, int32_t T, int32_t* offsets,

@@ -108,6 +108,58 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, unsigned quad, int* e_out
   return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
+// FP4-activation variant: the smallest integer e with amax <= 6 * 2^e,
+// limited to [-127, 127]; amax = 0 gives 0.  With amax = 1.f * 2^E (normal)
+// and 6 = 1.5 * 2^2: E - 2 when the significand is at most 1.5, else E - 1.
+// A subnormal amax is below 6 * 2^-127, so e = -127.
+__device__ __forceinline__ int fp4_block_exponent(float amax) {
+  const uint32_t u = __float_as_uint(amax);
+  if (u == 0u) return 0;
+  const int ebits = (int)(u >> 23);
+  if (ebits == 0) return -127;
+  const int E = ebits - 127;
+  int e = ((u & 0x7FFFFFu) <= 0x400000u) ? E - 2 : E - 1;  // 0x400000 = significand 1.5
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// Two fp32 values (already scaled into [-6, 6]) -> one byte of two E2M1
+// codes, lo in the low nibble; nearest-even.  The sign bit of each code is
+// taken from its input, so a negative value that rounds to zero gives -0.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "mov.b16 %0, {t, t};\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return ((uint32_t)r & 0x77u) | ((__float_as_uint(lo) >> 28) & 0x8u) | ((__float_as_uint(hi) >> 24) & 0x80u);
+}
+
+// Quantises 8 consecutive bf16 values to E2M1 (the FP4-activation variant);
+// the four lanes of a quad (one 32-block) agree on the block exponent.
+// Returns the 8 codes packed in 4 bytes (element 0 in the low nibble of byte
+// 0); *e gets the exponent.
+__device__ __forceinline__ uint32_t quant4(const uint4 v, unsigned quad, int* e_out) {
+  float f[8];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 2));
+  const int e = fp4_block_exponent(amax);
+  uint32_t c = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) c |= e2m1x2(scale_pow2_neg(f[2 * j], e), scale_pow2_neg(f[2 * j + 1], e)) << (8 * j);
+  *e_out = e;
+  return c;
+}
+
 // *p += v at device scope with acquire-release order; returns the old value.
 // Used by one thread after a CTA barrier: it publishes the writes the barrier
 // ordered before it and, for the thread that sees the final count, acquires

@@ -1,888 +1,13 @@
-// Grouped block-scaled expert GEMM on the 5th-generation tensor cores.
-//
-// D[w_row][token] = sum_k E2M1(W)[w_row][k] * 2^(sw-127) * E4M3(x)[token][k] * 2^(sx-127)
-// with tcgen05.mma kind::mxf8f6f4 (A = weights in MXFP4, B = activations in
-// FP8 E4M3, one UE8M0 scale per 32 along K for both), fp32 accumulators in
-// TMEM.  The checkpoint's routed experts are FP4 with UE8M0 block scales and
-// its activations are quantised dynamically to FP8 (FreeToken issue #444, "Is
-// the quantization already supported"; janit's comment item 2).
-//
-// One persistent CTA per SM, ten warps:
-//   warp 0      TMA producer.  Weights go through a 3-D view (128-element
-//               chunk, row, chunk index) of the canonical [row][K] bank with
-//               the 4-bit-unpacking tensor-map type, so that one TMA op moves
-//               128 rows x CH chunks (16 KB of HBM for CH = 2) and lands as CH
-//               standard 128-row swizzled tiles, one byte per element, as the
-//               f8f6f4 MMA reads them.  Large ops matter: a TMA unit completes
-//               a roughly fixed number of ops per second.
-//   warp 1      MMA issuer and TMEM owner;
-//   warps 2..5  epilogue (one TMEM lane quadrant each);
-//   warps 6..9  scale-factor writers: per stage they copy the UE8M0 bytes of
-//               the weight rows and tokens into TMEM (tcgen05.st): row r at
-//               lane r, column r/32 of its group, k-block j in byte j.
-// Work unit = (active expert, 128 weight rows, token tile of BN).  gate/up
-// units hold 128 gate rows and the same 128 up rows in two accumulators, so
-// every epilogue warp has g and u of its 32 intermediate rows: it writes
-// h = silu(g) * u as FP8 with one scale per 32 rows.  down units write fp32
-// expert outputs per position.
-#include <math.h>
-
-#include "common.cuh"
-#include "internal.h"
-#include "sm100.cuh"
+// Host side of the grouped block-scaled expert GEMM: tensor maps of the
+// weight banks and activations, and the launch of the kernel of
+// ffn_mma_kernel.cuh for a layer's shapes and activation format.
+#define MOE_FFN_MMA_INSTANTIATE launch_ffn_mma_fp8
+#define MOE_FFN_MMA_A4 0
+#include "ffn_mma_kernel.cuh"
 
 namespace moe {
 
-enum { kModeUp = 0, kModeDown = 1 };
-
-struct MmaParams {
-  CUtensorMap a_routed[2];   // up mode: gate, up banks; down mode: down bank in [0]
-  CUtensorMap a_shared[2];
-  CUtensorMap b;             // activations by position, 3-D view of [P][K] E4M3
-  CUtensorMap b_half;        // CTA pairs: the same view, half a token tile, one chunk per box
-  const uint8_t* sa_routed[2];
-  const uint8_t* sa_shared[2];
-  const uint8_t* sb;         // activation scales by position, [P][K/32]
-  int E, K, rows;            // rows per expert of the weight matrices (I up, H down)
-  int out_cols;              // I (h row length) in up mode, H in down mode
-  const int32_t* n_active;   // [0] active experts, [1] token tiles in all
-  const int32_t* tile_prefix;
-  int wait_tiles;            // the tile table comes from the previous kernel itself
-  const int4* tile_info;
-  int n_stages;              // ring depth (runtime: fits the shared memory)
-  int merged[2];             // up mode, routed / shared: gate and up load as one 4-D op
-  int swap_gu[2];            // ... whose first matrix is the up bank
-  uint8_t* hq;
-  uint8_t* hs;
-  float* o;
-  float* part;               // split partition: fp32 partial tiles, 2 slots per CTA
-  int32_t* cnt;              // split partition: pieces finished per (unit, row quadrant)
-  int split_ok;              // part/cnt are large enough for this launch
-  int gather;                // up mode, BN 16: activation rows gathered by token from xq
-  int fuse_combine;          // down mode, BN <= 64: the last writer of a token's rows combines them
-  int T, k, ns;              // fuse_combine: tokens, top-k, shared experts
-  const int32_t* slot_pos;   // fuse_combine: position of slot t*k + j (-1: invalid id)
-  const float* w;            // fuse_combine: combine weights [T][k]
-  const uint16_t* res;       // fuse_combine: bf16 residual [T][H] or null
-  uint16_t* y;               // fuse_combine: bf16 output [T][H]
-  int32_t* comb_cnt;         // fuse_combine: writers finished per (token, 128-row tile, quadrant)
-  const uint8_t* xq;         // gather: E4M3 codes of x by token, [T][K]
-  const int32_t* pos_tok;    // gather: token of each position
-  int32_t* err;
-};
-
 namespace {
-
-using namespace sm100;
-
-constexpr int kThreadsMma = 352;  // 11 warps: TMA, MMA, 4 epilogue, 4 scale-factor, 2nd MMA
-constexpr int kIssuer2Warp = 10;
-constexpr uint32_t kWaitLimit = 1u << 24;
-constexpr int kSmemBudget = 227 * 1024 - 2048;
-
-constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
-
-constexpr int kMaxStages = 6;
-
-template <int MODE, int BN, int CH>
-struct Cfg {
-  static constexpr int kNA = MODE == kModeUp ? 2 : 1;     // weight matrices per unit
-  static constexpr int kATile = 128 * 128 * CH;           // one matrix, one stage
-  static constexpr int kBTile = BN * 128 * CH;
-  // MMA issue is split over two threads (see the kernel): gate/up one matrix
-  // each; down the token columns [0, kN0) and [kN0, BN) (BN >= 64; kN0 a
-  // multiple of 32 so each half's scale groups start a column group, both
-  // halves multiples of 16) or one half of each stage's K steps, into a second
-  // accumulator (BN = 16).
-  static constexpr bool kSplitN = MODE == kModeDown && BN >= 64;
-  static constexpr bool kSplitK = MODE == kModeDown && BN < 64;
-  static constexpr int kN0 = (BN / 2 + 31) / 32 * 32;
-  // MMA width per tile from its token count (the 112-token tiles; narrower
-  // tiles are mostly full or one instruction step wide)
-  static constexpr bool kRagged = BN == 112;
-  static constexpr int kAccCols = (MODE == kModeUp || kSplitK ? 2 : 1) * BN;  // g, u (up); o (down)
-  static constexpr int kNAcc = (MODE == kModeUp && BN >= 128) ? 1 : 2;
-  static constexpr int kStage = kNA * kATile + kBTile;  // shared memory of one ring stage
-  static constexpr int kStageCap0 = (kSmemBudget - 1024) / kStage;
-  static constexpr int kStageCap = kStageCap0 < kMaxStages ? kStageCap0 : kMaxStages;
-  // Scale factors in TMEM, per stage: 4 columns per (weight matrix, chunk),
-  // then per chunk the token scales (group of 32 tokens g at column g); with
-  // the column split each half starts a 4-column group of its own (the MMA
-  // is handed a 4-column-aligned scale address).
-  static constexpr int kBCols = kSplitN ? 8 : 4;
-  static constexpr int kSfCols = kNA * 4 * CH + kBCols * CH;
-  __host__ __device__ static constexpr int sfb_col(int c, int g) {
-    return kNA * 4 * CH + c * kBCols + (kSplitN ? (g < kN0 / 32 ? g : 4 + g - kN0 / 32) : g);
-  }
-  static constexpr int kTmemCols = kNAcc * kAccCols + kStageCap * kSfCols;
-  static constexpr int kTmemAlloc = pow2_cols(kTmemCols);
-  static_assert(kTmemCols <= 512, "TMEM budget");
-};
-
-// Pipeline geometry: as many stages as fit the shared memory (at most
-// kMaxStages).  The bytes in flight per SM bound the bandwidth (about ten TMA
-// ops in flight, a few microseconds each), so every byte of shared memory goes
-// to the ring.
-template <int MODE, int BN, int CH>
-void geometry(int K, int* n_stages, int* smem) {
-  using C = Cfg<MODE, BN, CH>;
-  (void)K;
-  *n_stages = C::kStageCap;
-  *smem = 1024 + C::kStageCap * C::kStage;
-}
-
-struct Unit {
-  int e, pos0, m_tile, row0;
-};
-
-// Unit u -> (token tile v, 128-row tile); row tiles innermost so consecutive
-// units share the activation tile.  For a CTA pair, u counts pairs of row
-// tiles (mt_units = row tiles / 2) and rank picks the pair's member.
-__device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_units, int rank = -1) {
-  const int v = u / mt_units;
-  const int4 t = __ldg(p.tile_info + v);
-  const int r = u - v * mt_units;
-  return Unit{t.x, t.y, t.z, (rank < 0 ? r : 2 * r + rank) * 128};
-}
-
-// Work partition.  Plain: whole units strided over the CTAs.  Split: when
-// there are few units (a decode step), the units' K stages form one sequence
-// that is cut into gridDim.x nearly equal contiguous ranges, so that every SM
-// streams the same number of weight bytes.  A unit cut between CTAs is
-// finished by the last of them to arrive, which adds the fp32 partial tiles in
-// piece order (fixed, so results do not depend on arrival order).
-struct Piece {
-  int u, s0, s1;  // unit, stage range [s0, s1)
-};
-
-constexpr int kMaxPieces = 16;  // pieces per unit in the split partition
-constexpr int kMaxTopK = 8, kMaxShared = 4;  // layer limits (moe_config)
-
-// All arithmetic in 32 bits: split mode needs total < 4 * gridDim.x, so the
-// stage iterations stay below 2^20.
-struct Sched {
-  int ti, g, end;  // split: stage iterations in all, cursor, end of this CTA's range
-  int total, ks, u;
-  int cta, G;      // this worker and the number of workers (CTAs, or CTA pairs)
-  bool split;
-  __device__ Sched(int total_, int ks_, int split_ok, int cta_, int G_)
-      : total(total_), ks(ks_), cta(cta_), G(G_) {
-    split = false;
-    if (split_ok && total < 4 * G) {
-      ti = total * ks;
-      const int split_max = (ti + G - 1) / G;
-      const int plain_max = ((total + G - 1) / G) * ks;
-      // worth it when the busiest CTA gets at least 5 % fewer stages, and
-      // no unit is cut into more than kMaxPieces pieces
-      split = ti >= G && split_max * 20 < plain_max * 19 && ks <= (kMaxPieces - 2) * (ti / G);
-    }
-    g = split ? begin(cta) : 0;
-    end = split ? begin(cta + 1) : 0;
-    u = cta;
-  }
-  __device__ int begin(int c) const { return (int)(((unsigned)c * (unsigned)ti) / G); }
-  // the CTA whose range holds stage iteration it
-  __device__ int owner(int it) const { return (int)(((unsigned)(it + 1) * G + ti - 1) / ti) - 1; }
-  __device__ Piece next() {
-    Piece pc{-1, 0, 0};
-    if (!split) {
-      if (u < total) pc = Piece{u, 0, ks};
-      u += G;
-      return pc;
-    }
-    if (g >= end) return pc;
-    pc.u = g / ks;
-    pc.s0 = g - pc.u * ks;
-    pc.s1 = min(ks, pc.s0 + (end - g));
-    g += pc.s1 - pc.s0;
-    return pc;
-  }
-  // Unit uu is computed by CTAs first .. first + n - 1 (piece j by CTA first + j).
-  __device__ void pieces(int uu, int& first, int& n) const {
-    if (!split) {
-      first = cta;
-      n = 1;
-      return;
-    }
-    first = owner(uu * ks);
-    n = owner((uu + 1) * ks - 1) - first + 1;
-  }
-  // Partial slot of piece j: 2c for the first piece of CTA c's range, 2c + 1 for its last.
-  __device__ int slot(int uu, int first, int j) const {
-    return (j == 0 && begin(first) != uu * ks) ? 2 * first + 1 : 2 * (first + j);
-  }
-};
-
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
-                                            int32_t c2, int32_t c3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Multicast load into the same shared-memory offset of every CTA in mask (the
-// mbarrier at bar's offset in each of them receives the bytes).
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
-                                               int32_t c2, uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
-      "[%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
-// tcgen05.commit whose arrival goes to the mbarrier at bar's offset in every
-// CTA of mask.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// h = silu(g) * u = g / (1 + e^-g) * u with the SFU exponential and the fast
-// divide: a few ulp from the correctly rounded form, far inside the FP8
-// rounding of h that follows (one E4M3 step is 2^-3 relative).
-__device__ __forceinline__ float swiglu(float g, float u) {
-  return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
-                                            int32_t c2, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// PAIR: the grid is clusters of two CTAs that process the two row tiles of a
-// pair for the same token tile: each CTA loads half of the activation tile
-// and multicasts it to both, so each SM moves half the activation bytes.
-template <int MODE, int BN, int CH, bool PAIR>
-__global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_constant__ MmaParams p) {
-  using C = Cfg<MODE, BN, CH>;
-  constexpr int NA = C::kNA;
-  constexpr int NC = (BN + 31) / 32;  // 32-token groups of the B scale factors
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full_bar[kMaxStages], sf_bar[kMaxStages], empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
-  __shared__ uint32_t tmem_slot;
-  __shared__ int abort_flag;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt_per_expert = p.rows / 128;
-  const int k_stages = p.K / (128 * CH);
-  const int NS = p.n_stages;
-  uint8_t* stage_base = smem;
-  const int stage_bytes = NA * C::kATile + C::kBTile;
-  // Gather mode (gate/up at 16-token tiles, i.e. decode): the scale-factor
-  // warps copy each position's activation row from the per-token codes into
-  // the stage (swizzled like a TMA tile), so no slot-ordered copy of x exists.
-  constexpr bool kGatherCapable = MODE == kModeUp && BN == 16;
-  const bool gather = kGatherCapable && p.gather;
-  const uint32_t tx_stage = NA * 128 * 64 * CH + (gather ? 0 : BN * 128 * CH);
-  const uint32_t sf_col0 = C::kNAcc * C::kAccCols;
-
-  if (threadIdx.x == 0) {
-    // bring the tensor maps this CTA reads into the descriptor cache while
-    // the previous kernel finishes
-#pragma unroll
-    for (int m = 0; m < NA; ++m) {
-      prefetch_tensormap(&p.a_routed[m]);
-      prefetch_tensormap(&p.a_shared[m]);
-    }
-    prefetch_tensormap(PAIR ? &p.b_half : &p.b);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&sf_bar[s], 4);
-      mbar_init(&empty_bar[s], PAIR ? 4 : 2);  // one commit per MMA-issuing thread (of both CTAs)
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&accf_bar[b], 2);
-      mbar_init(&acce_bar[b], 4);
-    }
-    abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) tmem_alloc(&tmem_slot, C::kTmemAlloc);
-  fence_before();
-  __syncthreads();
-  // a pair's barriers must be initialised before the peer multicasts into them
-  if constexpr (PAIR) cluster_sync_all();
-  fence_after();
-  const uint32_t tmem = tmem_slot;
-  // Programmatic dependent launch.  Usually the tile table and the weights
-  // were final before the previous kernel started, so they are read right
-  // away and only the activations (and the outputs' readers) wait for the
-  // previous kernel in pdl_wait() below; after the small-batch preparation
-  // kernel the tile table is that kernel's own output, so everything waits.
-  if (p.wait_tiles) pdl_wait();
-  pdl_trigger();
-  const int rank = PAIR ? (int)cluster_ctarank() : -1;
-  const int mt_units = PAIR ? mt_per_expert / 2 : mt_per_expert;
-  const int total = p.n_active[1] * mt_units;
-  const Sched sc0(total, k_stages, BN <= 64 && p.split_ok, PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x,
-                  PAIR ? (int)gridDim.x / 2 : (int)gridDim.x);
-
-  auto give_up = [&]() {
-    atomicOr(p.err, kErrTimeout);
-    *(volatile int*)&abort_flag = 1;
-  };
-  auto aborted = [&]() { return *(volatile int*)&abort_flag != 0; };
-
-  if (warp == 0) {
-    // ---------------------------------------------------------------- TMA
-    if (lane == 0) {
-      uint32_t g = 0;
-      int last_parity[kMaxStages];
-      int deferred_pos[kMaxStages], deferred_s[kMaxStages], n_deferred = 0;
-      bool waited = gather;  // gather mode: the TMA warp loads weights only
-      // the activation tile of a stage: whole (one op), or for a CTA pair this
-      // CTA's half of every chunk, multicast into both CTAs' slots
-      auto load_b = [&](int slot, int pos0, int st) {
-        uint8_t* sb = stage_base + slot * stage_bytes + NA * C::kATile;
-        if constexpr (PAIR) {
-#pragma unroll
-          for (int c = 0; c < CH; ++c)
-            tma_load_3d_mc(sb + (c * BN + rank * (BN / 2)) * 128, &p.b_half, 0, pos0 + rank * (BN / 2), st * CH + c,
-                           &full_bar[slot], 0x3);
-        } else {
-          tma_load_3d(sb, &p.b, 0, pos0, st * CH, &full_bar[slot]);
-        }
-      };
-#pragma unroll
-      for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
-      Sched sc = sc0;
-      for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next()) {
-        const Unit un = decode_unit(p, pc.u, mt_units, rank);
-        const bool sh = un.e >= p.E;
-        const int erow = (sh ? un.e - p.E : un.e) * p.rows + un.row0;
-        bool ok = true;
-        const int s_end = pc.s1;
-        for (int s = pc.s0; s < s_end; ++s, ++g) {
-          const int slot = g % NS;
-          const uint32_t ph = (g / NS) & 1;
-          if (!waited && g >= (uint32_t)NS) {
-            // ring full: wait for the previous kernel, then load the deferred activations
-            pdl_wait();
-            waited = true;
-            for (int i = 0; i < n_deferred; ++i) load_b(i, deferred_pos[i], deferred_s[i]);
-          }
-          if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); ok = false; break; }
-          uint8_t* sa = stage_base + slot * stage_bytes;
-          mbar_expect_tx(&full_bar[slot], tx_stage);
-          if (NA == 2 && p.merged[sh]) {
-            // gate and up rows of the stage in one op: {chunk elems, rows, chunks, matrix}
-            tma_load_4d(sa, sh ? &p.a_shared[0] : &p.a_routed[0], 0, erow, s * CH, 0, &full_bar[slot]);
-          } else {
-#pragma unroll
-            for (int m = 0; m < NA; ++m)
-              tma_load_3d(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
-                          &full_bar[slot]);
-          }
-          if (gather) {
-            // activations come from the scale-factor warps
-          } else if (waited) {
-            load_b(slot, un.pos0, s);
-          } else {
-            deferred_pos[n_deferred] = un.pos0;  // slot == n_deferred while g < NS
-            deferred_s[n_deferred++] = s;
-          }
-#pragma unroll
-          for (int i = 0; i < kMaxStages; ++i)
-            if (i == slot) last_parity[i] = (int)ph;
-        }
-        if (!ok) break;
-      }
-      if (!waited) {
-        pdl_wait();
-        for (int i = 0; i < n_deferred; ++i) load_b(i, deferred_pos[i], deferred_s[i]);
-      }
-      // never leave with copies in flight: wait for the last load into each slot
-#pragma unroll
-      for (int s = 0; s < kMaxStages; ++s)
-        if (last_parity[s] >= 0) mbar_wait(&full_bar[s], (uint32_t)last_parity[s], kWaitLimit);
-      if constexpr (PAIR) {
-        // nor with the pair's releases still on their way: wait until both CTAs
-        // have released the last fill of every slot
-#pragma unroll
-        for (int s = 0; s < kMaxStages; ++s)
-          if (last_parity[s] >= 0) mbar_wait(&empty_bar[s], (uint32_t)last_parity[s], kWaitLimit);
-      }
-    }
-  } else if (warp == 1 || warp == kIssuer2Warp) {
-    // ---------------------------------------------------------------- MMA
-    // Two issuing threads.  A thread that also commits (tcgen05.commit in the
-    // same loop) issues tcgen05.mma at ~105 cycles per instruction for N <=
-    // 128; two such threads keep the tensor pipe at its throughput (measured:
-    // ~39 cycles at N = 16, ~64 at N = 128).  Each thread commits its own
-    // MMAs, so the empty and accumulator-full barriers count two arrivals.
-    if (lane == 0) {
-      const int j = warp == 1 ? 0 : 1;
-      // N of this thread's MMAs and the first of its token columns
-      const int NI0 = C::kSplitN ? (j == 0 ? C::kN0 : BN - C::kN0) : BN;
-      const int n0 = C::kSplitN ? j * C::kN0 : 0;
-      uint32_t g = 0, it = 0;
-      Sched sc = sc0;
-      for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
-        const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
-        const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
-        if (!mbar_wait(&acce_bar[buf], ph_acc ^ 1, kWaitLimit)) { give_up(); break; }
-        fence_after();
-        const uint32_t d_tmem = tmem + buf * C::kAccCols;
-        int swap = 0, NI = NI0;
-        if (NA == 2 || C::kRagged) {
-          const Unit un = decode_unit(p, pc.u, mt_units, rank);
-          const int sh = un.e >= p.E;
-          if (NA == 2) swap = p.merged[sh] && p.swap_gu[sh];
-          if (C::kRagged) {
-            // the wide tiles are often part-filled: N = the tile's tokens
-            // rounded up to the instruction's step of 16, so the MMAs cost
-            // only the columns in use (the epilogue reads no column past them)
-            const int nr = min(BN, (un.m_tile + 15) & ~15);
-            NI = C::kSplitN ? (j == 0 ? min(C::kN0, nr) : nr - C::kN0) : nr;
-          }
-        }
-        const uint32_t idesc_base = idesc_e2m1_e4m3(128, NI > 0 ? NI : 16, 0);
-        bool ok = true;
-        const int s_beg = pc.s0, s_end = pc.s1;
-        for (int s = s_beg; s < s_end; ++s, ++g) {
-          const int slot = g % NS;
-          const uint32_t ph = (g / NS) & 1;
-          if (!mbar_wait(&full_bar[slot], ph, kWaitLimit) || !mbar_wait(&sf_bar[slot], ph, kWaitLimit)) {
-            give_up();
-            ok = false;
-            break;
-          }
-          fence_after();
-          const uint32_t sa = smem_u32(stage_base + slot * stage_bytes);
-          // descriptors differ only in the start-address field (bits 0..13, address / 16)
-          const uint64_t a_desc0 = sw128_desc(sa), b_desc0 = sw128_desc(sa + NA * C::kATile);
-          const uint32_t sf = tmem + sf_col0 + slot * C::kSfCols;
-#pragma unroll
-          for (int c = 0; c < CH; ++c)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              if (C::kRagged && NI <= 0) break;  // the second column half of a narrow tile is empty
-              const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
-              const uint64_t bdesc = b_desc0 + (uint64_t)((c * BN * 128 + 32 * k) >> 4);
-              const uint32_t sfb = sf + C::sfb_col(c, 0);
-              if constexpr (MODE == kModeUp) {
-                const int m = j, acc = swap ? 1 - m : m;  // gate -> accumulator 0, up -> 1
-                mma_mxf8f6f4(d_tmem + acc * BN, a_desc0 + (uint64_t)((m * C::kATile + c * 16384 + 32 * k) >> 4),
-                             bdesc, idesc, sf + (acc * CH + c) * 4, sfb, (s != s_beg || c || k) ? 1u : 0u);
-              } else if constexpr (C::kSplitN) {
-                // token columns [n0, n0 + NI): B rows and their scale groups
-                mma_mxf8f6f4(d_tmem + n0, a_desc0 + (uint64_t)((c * 16384 + 32 * k) >> 4),
-                             bdesc + (uint64_t)((n0 * 128) >> 4), idesc, sf + c * 4, sf + C::sfb_col(c, n0 / 32),
-                             (s != s_beg || c || k) ? 1u : 0u);
-              } else {
-                // K steps i = 4c + k of the stage: the first half to accumulator 0
-                const int i = c * 4 + k, first = j * CH * 2;
-                if ((i < CH * 2) == (j == 0))
-                  mma_mxf8f6f4(d_tmem + j * BN, a_desc0 + (uint64_t)((c * 16384 + 32 * k) >> 4), bdesc, idesc,
-                               sf + c * 4, sfb, (s != s_beg || i != first) ? 1u : 0u);
-              }
-            }
-          if constexpr (PAIR)
-            mma_commit_mc(&empty_bar[slot], 0x3);  // the slot is refilled in both CTAs at once
-          else
-            mma_commit(&empty_bar[slot]);
-        }
-        if (!ok) break;
-        mma_commit(&accf_bar[buf]);
-      }
-    }
-  } else if (warp >= 6) {
-    // ------------------------------------------------------- scale factors
-    // The scale words of NB stages are fetched at once (double-buffered in
-    // registers), so a global-load latency is paid per NB stages.
-    constexpr int NB = 4, NW = NA * CH + NC * CH;  // words per stage
-    constexpr int BCH = kGatherCapable ? CH : 1;   // gathered 16-byte granules per stage
-    const int q = warp & 3;
-    pdl_wait();  // the activation scales come from the previous kernel
-    uint32_t g = 0;
-    bool ok = true;
-    Sched sc = sc0;
-    for (Piece pc = sc.next(); ok && pc.u >= 0 && !aborted(); pc = sc.next()) {
-      const Unit un = decode_unit(p, pc.u, mt_units, rank);
-      const int s_end = pc.s1;
-      const bool sh = un.e >= p.E;
-      const size_t erow = (size_t)(sh ? un.e - p.E : un.e) * p.rows + un.row0 + 32 * q + lane;
-      const uint8_t* sa_row[NA];
-#pragma unroll
-      for (int m = 0; m < NA; ++m) sa_row[m] = (sh ? p.sa_shared[m] : p.sa_routed[m]) + erow * (p.K / 32);
-      const uint8_t* sb_row[NC];
-#pragma unroll
-      for (int cb = 0; cb < NC; ++cb) {
-        const int n = lane + 32 * cb;
-        sb_row[cb] = nullptr;
-        if (n < un.m_tile) {
-          const size_t row = gather ? (size_t)p.pos_tok[un.pos0 + n] : (size_t)(un.pos0 + n);
-          sb_row[cb] = p.sb + row * (p.K / 32);
-        }
-      }
-      // gather: this thread copies 16-byte granule bg of activation row br of
-      // every chunk (128 threads x 2 chunks = the 16 x 256-byte B stage)
-      const int br = (32 * q + lane) >> 3, bg = lane & 7;
-      const uint8_t* xrow = nullptr;
-      if (gather && br < un.m_tile) xrow = p.xq + (size_t)p.pos_tok[un.pos0 + br] * p.K + bg * 16;
-      const int b_off = NA * C::kATile + br * 128 + ((bg ^ (br & 7)) << 4);  // 128-byte swizzle
-      auto load_b = [&](uint4 (&bw)[NB][BCH], int s0) {
-        if constexpr (kGatherCapable) {
-#pragma unroll
-          for (int i = 0; i < NB; ++i)
-#pragma unroll
-            for (int c = 0; c < BCH; ++c)
-              bw[i][c] = (xrow && s0 + i < s_end)
-                             ? __ldg(reinterpret_cast<const uint4*>(xrow + ((s0 + i) * CH + c) * 128))
-                             : make_uint4(0u, 0u, 0u, 0u);
-        }
-      };
-      auto load = [&](uint32_t (&w)[NB][NW], int s0) {
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          if (s0 + i < s_end) {
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-              const int kb = 4 * ((s0 + i) * CH + c);  // first k-block of the chunk
-#pragma unroll
-              for (int m = 0; m < NA; ++m) w[i][m * CH + c] = __ldg(reinterpret_cast<const uint32_t*>(sa_row[m] + kb));
-#pragma unroll
-              for (int cb = 0; cb < NC; ++cb)
-                w[i][NA * CH + c * NC + cb] =
-                    sb_row[cb] ? __ldg(reinterpret_cast<const uint32_t*>(sb_row[cb] + kb)) : 0x7F7F7F7Fu;
-            }
-          }
-        }
-      };
-      auto store = [&](const uint32_t (&w)[NB][NW], const uint4 (&bw)[NB][BCH], int s0) -> bool {
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          if (s0 + i >= s_end) break;
-          const int slot = g % NS;
-          const uint32_t ph = (g / NS) & 1;
-          if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); return false; }
-          fence_after();
-          if constexpr (kGatherCapable) {
-            if (gather) {
-              uint8_t* dst = stage_base + slot * stage_bytes + b_off;
-#pragma unroll
-              for (int c = 0; c < BCH; ++c) *reinterpret_cast<uint4*>(dst + c * BN * 128) = bw[i][c];
-              fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
-            }
-          }
-          const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + sf_col0 + slot * C::kSfCols;
-#pragma unroll
-          for (int c = 0; c < CH; ++c) {
-#pragma unroll
-            for (int m = 0; m < NA; ++m) tmem_st_x1(col + (m * CH + c) * 4 + q, w[i][m * CH + c]);
-#pragma unroll
-            for (int cb = 0; cb < NC; ++cb) tmem_st_x1(col + C::sfb_col(c, cb), w[i][NA * CH + c * NC + cb]);
-          }
-          tmem_st_wait();
-          fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sf_bar[slot]);
-          ++g;
-        }
-        return true;
-      };
-      uint32_t w0[NB][NW], w1[NB][NW];
-      uint4 b0[NB][BCH], b1[NB][BCH];
-      load(w0, pc.s0);
-      load_b(b0, pc.s0);
-      for (int s0 = pc.s0; s0 < s_end; s0 += 2 * NB) {
-        if (s0 + NB < s_end) {
-          load(w1, s0 + NB);
-          load_b(b1, s0 + NB);
-        }
-        if (!(ok = store(w0, b0, s0))) break;
-        if (s0 + NB >= s_end) break;
-        if (s0 + 2 * NB < s_end) {
-          load(w0, s0 + 2 * NB);
-          load_b(b0, s0 + 2 * NB);
-        }
-        if (!(ok = store(w1, b1, s0 + NB))) break;
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;        // TMEM lane quadrant of this warp
-    const int rl = 32 * q + lane;  // row within the 128-row tile
-    pdl_wait();
-    // One output column (a token position) of the tile: all 32 lanes of the
-    // warp take part (the h block scale is a max over the warp's 32 rows).
-    auto emit = [&](const Unit& un, int col, float a, float b) {
-      const size_t pos = (size_t)(un.pos0 + col);
-      const int row = un.row0 + rl;  // weight row (I row for up, H row for down)
-      if (MODE == kModeDown) {
-        p.o[pos * p.out_cols + row] = a;
-      } else {
-        const float h = swiglu(a, b);
-        const int ex = fp8_block_exponent(warp_max(fabsf(h)));
-        p.hq[pos * p.out_cols + row] = (uint8_t)(e4m3x2(scale_pow2_neg(h, ex), 0.f) & 0xFFu);
-        if (lane == 0) p.hs[pos * (p.out_cols / 32) + (un.row0 + 32 * q) / 32] = (uint8_t)(ex + 127);
-      }
-    };
-    // Sixteen columns at once (the main path): the SwiGLU values of all of them
-    // first, then the sixteen 32-row maxima as interleaved shuffle trees, so
-    // the shuffle latency is paid once per group rather than once per column.
-    // Same operations per column as emit(), so the same bits.
-    auto emit16 = [&](const Unit& un, int c, const uint32_t (&v)[16], const uint32_t (&vu)[16]) {
-      const int row = un.row0 + rl;
-      if constexpr (MODE == kModeDown) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (c + j >= un.m_tile) break;  // warp-uniform
-          const float a = C::kSplitK ? __uint_as_float(v[j]) + __uint_as_float(vu[j]) : __uint_as_float(v[j]);
-          p.o[(size_t)(un.pos0 + c + j) * p.out_cols + row] = a;
-        }
-      } else {
-        float h[16], am[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float g = __uint_as_float(v[j]);
-          h[j] = swiglu(g, __uint_as_float(vu[j]));
-          am[j] = fabsf(h[j]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-          for (int j = 0; j < 16; ++j) am[j] = fmaxf(am[j], __shfl_xor_sync(0xFFFFFFFFu, am[j], o));
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (c + j >= un.m_tile) break;  // warp-uniform
-          const size_t pos = (size_t)(un.pos0 + c + j);
-          const int ex = fp8_block_exponent(am[j]);
-          p.hq[pos * p.out_cols + row] = (uint8_t)(e4m3x2(scale_pow2_neg(h[j], ex), 0.f) & 0xFFu);
-          if (lane == 0) p.hs[pos * (p.out_cols / 32) + (un.row0 + 32 * q) / 32] = (uint8_t)(ex + 127);
-        }
-      }
-    };
-    // Down mode with the combine fused (small batches): after a warp has
-    // written the o rows of its unit, each of the unit's positions counts one
-    // arrival for its token; the warp that brings a token's count to the
-    // number of its positions (valid routed slots + shared experts) adds that
-    // token's o rows for these 32 output rows in the fixed order of the
-    // combine (shared experts, then slots j = 0..k-1) and writes y.
-    auto combine_tail = [&](const Unit& un) {
-      if constexpr (MODE == kModeDown && BN <= 64) {
-        if (!p.fuse_combine) return;
-        __threadfence();
-        __syncwarp();
-        const int n_rt = p.out_cols / 128, rt = un.row0 / 128;
-        int done = -1;
-        if (lane < un.m_tile) {
-          const int t = p.pos_tok[un.pos0 + lane];
-          int sp[kMaxTopK];
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) sp[j] = j < p.k ? p.slot_pos[t * p.k + j] : -1;
-          int need = p.ns;
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) need += sp[j] >= 0;
-          if (atomicAdd(&p.comb_cnt[(t * n_rt + rt) * 4 + q], 1) == need - 1) done = t;
-        }
-        unsigned todo = __ballot_sync(0xFFFFFFFFu, done >= 0);
-        if (todo) __threadfence();
-        const int row = un.row0 + rl;
-        const size_t S = (size_t)p.T * p.k, H = (size_t)p.out_cols;
-        while (todo) {
-          const int t = __shfl_sync(0xFFFFFFFFu, done, __ffs(todo) - 1);
-          todo &= todo - 1;
-          // lane j < k holds slot j's position and weight; then every o load is in flight at once
-          const int my_pp = lane < p.k ? p.slot_pos[t * p.k + lane] : -1;
-          const float my_w = lane < p.k ? p.w[t * p.k + lane] : 0.f;
-          float osh[kMaxShared], ov[kMaxTopK];
-#pragma unroll
-          for (int j = 0; j < kMaxShared; ++j)
-            osh[j] = j < p.ns ? __ldcg(p.o + (S + (size_t)j * p.T + t) * H + row) : 0.f;
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) {
-            const int pp = __shfl_sync(0xFFFFFFFFu, my_pp, j);
-            ov[j] = pp >= 0 ? __ldcg(p.o + (size_t)pp * H + row) : 0.f;
-          }
-          // the combine's fixed order: shared experts, then slots j = 0..k-1
-          float acc = 0.f;
-#pragma unroll
-          for (int j = 0; j < kMaxShared; ++j)
-            if (j < p.ns) acc += osh[j];
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) {
-            const float wj = __shfl_sync(0xFFFFFFFFu, my_w, j);
-            if (__shfl_sync(0xFFFFFFFFu, my_pp, j) >= 0) acc = fmaf(wj, ov[j], acc);
-          }
-          uint16_t yb = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-          if (p.res)
-            yb = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits_to_float(p.res[(size_t)t * H + row]) +
-                                                          bf16_bits_to_float(yb)));
-          p.y[(size_t)t * H + row] = yb;
-        }
-      }
-    };
-    constexpr int kSlot = NA * BN * 128;  // floats per partial slot: [matrix][column][row]
-    uint32_t it = 0;
-    Sched sc = sc0;
-    for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
-      const Unit un = decode_unit(p, pc.u, mt_units, rank);
-      const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
-      const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
-      if (!mbar_wait(&accf_bar[buf], ph_acc, kWaitLimit)) { give_up(); break; }
-      fence_after();
-      const uint32_t t_base = tmem + ((uint32_t)(32 * q) << 16) + buf * C::kAccCols;
-      int first, n;
-      sc.pieces(pc.u, first, n);
-      if (n == 1) {
-        // the whole unit: straight from TMEM to the outputs (the columns the
-        // MMAs wrote)
-        const int c_end = C::kRagged ? min(BN, (un.m_tile + 15) & ~15) : BN;
-#pragma unroll 1
-        for (int c = 0; c < c_end; c += 16) {
-          uint32_t v[16], vu[16];
-          tmem_ld16(t_base + c, v);
-          if (MODE == kModeUp || C::kSplitK) tmem_ld16(t_base + BN + c, vu);
-          tmem_ld_wait();
-          if (c + 16 >= c_end) {
-            fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acce_bar[buf]);
-          }
-          if (c < un.m_tile) emit16(un, c, v, vu);  // down split-K: the two K halves, in fixed order
-        }
-        combine_tail(un);
-        continue;
-      }
-      if constexpr (BN <= 64) {
-        // A piece of a unit cut between CTAs: publish the fp32 partial tile;
-        // the last piece to arrive adds all of them in piece order.  Each warp
-        // owns its 32 rows, so the hand-off is per warp (one counter per unit
-        // and quadrant) and no warp ever waits for another.
-        float* mine = p.part + (size_t)sc.slot(pc.u, first, sc.cta - first) * kSlot;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
-          uint32_t v[16], vu[16];
-          tmem_ld16(t_base + c, v);
-          if (MODE == kModeUp || C::kSplitK) tmem_ld16(t_base + BN + c, vu);
-          tmem_ld_wait();
-          if (c + 16 >= BN) {
-            fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acce_bar[buf]);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c + j >= un.m_tile) break;  // warp-uniform
-            if constexpr (C::kSplitK)
-              mine[(c + j) * 128 + rl] = __uint_as_float(v[j]) + __uint_as_float(vu[j]);
-            else
-              mine[(c + j) * 128 + rl] = __uint_as_float(v[j]);
-            if (MODE == kModeUp) mine[(BN + c + j) * 128 + rl] = __uint_as_float(vu[j]);
-          }
-        }
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(&p.cnt[pc.u * 4 + q], 1) == n - 1;
-        if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-          __threadfence();
-          const float* src[kMaxPieces];
-#pragma unroll
-          for (int j = 0; j < kMaxPieces; ++j)
-            src[j] = p.part + (size_t)sc.slot(pc.u, first, j < n ? j : 0) * kSlot + rl;
-#pragma unroll 1
-          for (int col = 0; col < un.m_tile; ++col) {
-            float pa[kMaxPieces], pb[kMaxPieces];
-#pragma unroll
-            for (int j = 0; j < kMaxPieces; ++j) {  // all loads in flight, then the fixed-order sum
-              pa[j] = j < n ? __ldcg(src[j] + col * 128) : 0.f;
-              pb[j] = (MODE == kModeUp && j < n) ? __ldcg(src[j] + (BN + col) * 128) : 0.f;
-            }
-            float a = 0.f, b = 0.f;
-#pragma unroll
-            for (int j = 0; j < kMaxPieces; ++j) {
-              if (j < n) {
-                a += pa[j];
-                b += pb[j];
-              }
-            }
-            emit(un, col, a, b);
-          }
-          if (lane == 0) p.cnt[pc.u * 4 + q] = 0;
-          combine_tail(un);
-        }
-      }
-    }
-  }
-  fence_before();
-  __syncthreads();
-  // a CTA of a pair leaves only when the peer no longer writes into it
-  if constexpr (PAIR) cluster_sync_all();
-  if (warp == 1) {
-    fence_after();
-    tmem_dealloc(tmem, C::kTmemAlloc);
-  }
-}
-
-template <int MODE, int BN, int CH, bool PAIR>
-cudaError_t launch_one(MmaParams& p, int num_sms, cudaStream_t st) {
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_mma_kernel<MODE, BN, CH, PAIR>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
-  int smem = 0;
-  geometry<MODE, BN, CH>(p.K, &p.n_stages, &smem);
-  if (p.n_stages < 2) return cudaErrorInvalidConfiguration;
-  if (!PAIR) {
-    { cudaError_t le_ = launch_pdl(ffn_mma_kernel<MODE, BN, CH, false>, dim3(num_sms), dim3(kThreadsMma), smem, st, p); if (le_ != cudaSuccess) return le_; }
-    return cudaGetLastError();
-  }
-  // clusters of two CTAs, as a programmatic dependent launch
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_sms & ~1);
-  cfg.blockDim = dim3(kThreadsMma);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, ffn_mma_kernel<MODE, BN, CH, PAIR>, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-template <int MODE, int CH>
-cudaError_t launch_bn(MmaParams& p, int bn, bool pair, int num_sms, cudaStream_t st) {
-  if (bn == 16) return launch_one<MODE, 16, CH, false>(p, num_sms, st);
-  if (bn == 64) return launch_one<MODE, 64, CH, false>(p, num_sms, st);
-  if (pair) return launch_one<MODE, 112, CH, true>(p, num_sms, st);
-  return launch_one<MODE, 112, CH, false>(p, num_sms, st);
-}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -931,34 +56,43 @@ int chunks_per_stage(int K, bool allow3) {
 // matrix}: the matrix stride is the distance between the two banks, so one
 // box {128, 128, ch, 2} loads the same rows of both.  Needs the distance to be
 // a multiple of 32 bytes; *swap tells that the up bank comes first.
+// packed: the bytes as they are (FP4-activation variant: 128-byte chunks of
+// 256 elements, for kind::mxf4) instead of the one-byte-per-element expansion.
 bool map_4d_pair(CUtensorMap* m, const void* gate, const void* up, uint64_t K, uint64_t rows,
-                 uint32_t ch, int* swap) {
+                 uint32_t ch, int* swap, bool packed = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !gate || !up) return false;
   const uintptr_t g = (uintptr_t)gate, u = (uintptr_t)up;
   const uintptr_t lo = g < u ? g : u, dist = g < u ? u - g : g - u;
   if (dist == 0 || dist % 32 != 0 || dist >= (1ull << 40)) return false;
   *swap = u < g;
-  cuuint64_t dims[4] = {128, rows, K / 128, 2};
-  cuuint64_t strides[3] = {K / 2, 64, (cuuint64_t)dist};
+  cuuint64_t dims[4] = {128, rows, K / (packed ? 256 : 128), 2};
+  cuuint64_t strides[3] = {K / 2, packed ? 128u : 64u, (cuuint64_t)dist};
   cuuint32_t box[4] = {128, 128, ch, 2};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, reinterpret_cast<void*>(lo), dims, strides, box,
+  return enc(m, packed ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4,
+             reinterpret_cast<void*>(lo), dims, strides, box,
              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
-struct MmaMaps {
+// Tensor maps of one activation format: weights (FP8 activations: FP4 codes
+// expanded to a byte each; FP4 activations: packed bytes) and activations.
+struct FormatMaps {
   CUtensorMap gate, up, down, s_gate, s_up, s_down;
   CUtensorMap gu_pair, s_gu_pair;  // gate + up as one 4-D tensor (when possible)
   int merged[2], swap_gu[2];
   CUtensorMap xg[3], hq[3];  // per token tile width: 16, 64, 112
   CUtensorMap xg_half, hq_half;  // CTA pairs: half a 112-token tile, one chunk per box
   int ch_up, ch_down;
+  bool ok;
 };
 
+struct MmaMaps {
+  FormatMaps f[2];  // [0] FP8 activations, [1] FP4 activations (f[1].ok: shapes allow it)
+};
 
 static int bn_index(int bn) { return bn == 16 ? 0 : (bn == 64 ? 1 : 2); }
 
@@ -968,43 +102,61 @@ static int bn_index(int bn) { return bn == 16 ? 0 : (bn == 64 ? 1 : 2); }
 // overlaps the MMAs of the next.
 int mma_tile_for_tokens(int T) { return T <= 64 ? 16 : (T < 512 ? 64 : 112); }
 
-MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Workspace& ws) {
-  MmaMaps* m = new MmaMaps();
+// a4: packed operands (the FP4-activation variant): a chunk is 128 bytes of
+// a row, 256 elements, one per stage; rows of K elements are K/2 bytes for
+// weights and activations alike.
+static bool format_maps(FormatMaps* m, bool a4, const moe_config& c, const moe_weights& w, const Workspace& ws) {
   const uint64_t H = c.hidden, I = c.inter, E = c.n_experts, ns = c.n_shared;
   const uint64_t P = (uint64_t)c.max_tokens * (c.top_k + c.n_shared);
-  m->ch_up = chunks_per_stage((int)H, false);
-  m->ch_down = chunks_per_stage((int)I, true);
-  bool ok = map_3d(&m->gate, true, w.gate.codes, H, E * I, 128, m->ch_up) &&
-            map_3d(&m->up, true, w.up.codes, H, E * I, 128, m->ch_up) &&
-            map_3d(&m->down, true, w.down.codes, I, E * H, 128, m->ch_down);
+  m->ch_up = a4 ? 1 : chunks_per_stage((int)H, false);
+  m->ch_down = a4 ? 1 : chunks_per_stage((int)I, true);
+  // weights: a4 views [rows][K/2] bytes as 128-byte chunks; else the 4-bit expansion
+  auto wmap = [&](CUtensorMap* t, const void* codes, uint64_t K, uint64_t rows, int ch) {
+    return a4 ? map_3d(t, false, codes, K / 2, rows, 128, ch) : map_3d(t, true, codes, K, rows, 128, ch);
+  };
+  bool ok = wmap(&m->gate, w.gate.codes, H, E * I, m->ch_up) && wmap(&m->up, w.up.codes, H, E * I, m->ch_up) &&
+            wmap(&m->down, w.down.codes, I, E * H, m->ch_down);
   if (ok && ns > 0)
-    ok = map_3d(&m->s_gate, true, w.s_gate.codes, H, ns * I, 128, m->ch_up) &&
-         map_3d(&m->s_up, true, w.s_up.codes, H, ns * I, 128, m->ch_up) &&
-         map_3d(&m->s_down, true, w.s_down.codes, I, ns * H, 128, m->ch_down);
+    ok = wmap(&m->s_gate, w.s_gate.codes, H, ns * I, m->ch_up) && wmap(&m->s_up, w.s_up.codes, H, ns * I, m->ch_up) &&
+         wmap(&m->s_down, w.s_down.codes, I, ns * H, m->ch_down);
   m->merged[0] = m->merged[1] = 0;
   m->swap_gu[0] = m->swap_gu[1] = 0;
   if (ok) {
-    m->merged[0] = map_4d_pair(&m->gu_pair, w.gate.codes, w.up.codes, H, E * I, m->ch_up, &m->swap_gu[0]);
+    m->merged[0] = map_4d_pair(&m->gu_pair, w.gate.codes, w.up.codes, H, E * I, m->ch_up, &m->swap_gu[0], a4);
     if (ns > 0)
-      m->merged[1] = map_4d_pair(&m->s_gu_pair, w.s_gate.codes, w.s_up.codes, H, ns * I, m->ch_up, &m->swap_gu[1]);
+      m->merged[1] =
+          map_4d_pair(&m->s_gu_pair, w.s_gate.codes, w.s_up.codes, H, ns * I, m->ch_up, &m->swap_gu[1], a4);
   }
   const uint32_t bns[3] = {16, 64, 112};
+  const uint64_t xk = a4 ? H / 2 : H, hk = a4 ? I / 2 : I;  // activation row bytes
   for (int i = 0; ok && i < 3; ++i)
-    ok = map_3d(&m->xg[i], false, ws.xg, H, P, bns[i], m->ch_up) &&
-         map_3d(&m->hq[i], false, ws.hq, I, P, bns[i], m->ch_down);
+    ok = map_3d(&m->xg[i], false, ws.xg, xk, P, bns[i], m->ch_up) &&
+         map_3d(&m->hq[i], false, ws.hq, hk, P, bns[i], m->ch_down);
   if (ok)
-    ok = map_3d(&m->xg_half, false, ws.xg, H, P, 112 / 2, 1) && map_3d(&m->hq_half, false, ws.hq, I, P, 112 / 2, 1);
-  if (!ok) {
+    ok = map_3d(&m->xg_half, false, ws.xg, xk, P, 112 / 2, 1) && map_3d(&m->hq_half, false, ws.hq, hk, P, 112 / 2, 1);
+  m->ok = ok;
+  return ok;
+}
+
+bool mma_act4_supported(const moe_config& c) { return c.hidden % 256 == 0 && c.inter % 256 == 0; }
+
+MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Workspace& ws) {
+  MmaMaps* m = new MmaMaps();
+  if (!format_maps(&m->f[0], false, c, w, ws)) {
     delete m;
     return nullptr;
   }
+  m->f[1].ok = false;
+  if (mma_act4_supported(c)) format_maps(&m->f[1], true, c, w, ws);
   return m;
 }
 
 void mma_maps_destroy(MmaMaps* m) { delete m; }
 
-cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn, bool gather,
-                           const Workspace& ws, int num_sms, cudaStream_t st, const CombineArgs* cmb) {
+cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, int bn, bool gather,
+                           const Workspace& ws, int num_sms, cudaStream_t st, const CombineArgs* cmb, bool act4) {
+  const FormatMaps& mm = maps.f[act4 ? 1 : 0];
+  if (!mm.ok) return cudaErrorInvalidValue;
   MmaParams p;
   memset(&p, 0, sizeof(p));
   const int bi = bn_index(bn);
@@ -1073,10 +225,8 @@ cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, in
   // CTA pairs for the widest tiles: both row-tile counts even, an even grid
   const bool pair = bn == 112 && (p.rows / 128) % 2 == 0 && num_sms >= 2;
   if (pair) p.b_half = mode == kModeUp ? mm.xg_half : mm.hq_half;
-  if (mode == kModeUp)
-    return ch == 2 ? launch_bn<kModeUp, 2>(p, bn, pair, num_sms, st) : launch_bn<kModeUp, 1>(p, bn, pair, num_sms, st);
-  if (ch == 3) return launch_bn<kModeDown, 3>(p, bn, pair, num_sms, st);
-  return ch == 2 ? launch_bn<kModeDown, 2>(p, bn, pair, num_sms, st) : launch_bn<kModeDown, 1>(p, bn, pair, num_sms, st);
+  return act4 ? launch_ffn_mma_fp4(p, mode, bn, ch, pair, num_sms, st)
+              : launch_ffn_mma_fp8(p, mode, bn, ch, pair, num_sms, st);
 }
 
 }  // namespace moe

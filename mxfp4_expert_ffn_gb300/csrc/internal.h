@@ -83,6 +83,7 @@ struct moe_layer {
   int path = 0;
   int scoring = 0;            // MOE_SCORING_SOFTMAX / MOE_SCORING_SIGMOID
   float routed_scale = 1.0f;  // routed weights are multiplied by it
+  int act_format = 0;         // MOE_ACT_FP8 / MOE_ACT_FP4
   bool timing = false;
   moe::Workspace ws;
   moe::MmaMaps* maps = nullptr;  // TMA descriptors of the tensor-core path
@@ -128,7 +129,10 @@ cudaError_t launch_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uin
 cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared, int bn,
                             const Workspace& ws, cudaStream_t st);
 cudaError_t launch_quantize_gather(const uint16_t* x, int P, int H, const int32_t* pos_tok,
-                                   uint8_t* xg, uint8_t* xgs, cudaStream_t st);
+                                   uint8_t* xg, uint8_t* xgs, bool act4, cudaStream_t st);
+// The FP4-activation variant's quantiser of x by token: q [T][H/2], s [T][H/32].
+cudaError_t launch_quantize_act4(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s,
+                                 cudaStream_t st);
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const float* W,
                                  const float* b, float* logits, int num_sms, cudaStream_t st);
 int router_ksplit(int H);
@@ -166,16 +170,20 @@ struct CombineArgs {
 // gather (gate/up at bn 16 only): activation rows are read by token from xq/xs
 // through pos_tok instead of from the slot-ordered copy xg/xgs.  cmb (down,
 // bn <= 64): the combine runs inside the down GEMM (needs T <= kPrepMaxTokens).
+// act4: the FP4-activation variant (xg/xq/hq hold packed E2M1 codes).
 cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn, bool gather,
                            const Workspace& ws, int num_sms, cudaStream_t st,
-                           const CombineArgs* cmb = nullptr);
+                           const CombineArgs* cmb = nullptr, bool act4 = false);
+// FP4 activations need H and I multiples of 256 (whole 128-byte chunks).
+bool mma_act4_supported(const moe_config& c);
 // Small batches (T <= kPrepMaxTokens): router + top-k (route) or the given
 // routing, FP8 codes of x by token (xq/xs) and the segments, in one launch.
 constexpr int kPrepMaxTokens = 64;
 cudaError_t prepare_prep_kernel(int E, int H);
 cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, int bn,
                         const float* W, const float* b, const Scoring& sg, float* logits_out,
-                        int32_t* idx, float* w, bool route, const Workspace& ws, cudaStream_t st);
+                        int32_t* idx, float* w, bool route, bool act4, const Workspace& ws,
+                        cudaStream_t st);
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out,
                            cudaStream_t st);
 

@@ -44,6 +44,7 @@ struct PrepParams {
   float* w;              // [T][k] written (route)
   int32_t* counters;     // [token blocks + 1], zero between launches
   Scoring sg;            // how the weights follow from the logits
+  int act4;              // x codes as packed E2M1 (the FP4-activation variant)
   Workspace ws;
 };
 
@@ -91,9 +92,13 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
     const unsigned quad = 0xFu << (lane & ~3);
     const uint4* x8 = reinterpret_cast<const uint4*>(p.x);
     uint2* q8 = reinterpret_cast<uint2*>(p.ws.xq);
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(p.ws.xq);
     for (int i = cta * blockDim.x + threadIdx.x; i < n8; i += stride) {
       int ex;
-      q8[i] = quant8(x8[i], quad, &ex);
+      if (p.act4)
+        q4[i] = quant4(x8[i], quad, &ex);
+      else
+        q8[i] = quant8(x8[i], quad, &ex);
       if ((lane & 3) == 0) p.ws.xs[i >> 2] = (uint8_t)(ex + 127);
     }
   }
@@ -170,7 +175,8 @@ cudaError_t prepare_prep_kernel(int E, int H) {
 
 cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, int bn,
                         const float* W, const float* b, const Scoring& sg, float* logits_out,
-                        int32_t* idx, float* w, bool route, const Workspace& ws, cudaStream_t st) {
+                        int32_t* idx, float* w, bool route, bool act4, const Workspace& ws,
+                        cudaStream_t st) {
   if (T <= 0 || T > kPrepMaxTokens) return cudaErrorInvalidValue;
   PrepParams p;
   p.x = x;
@@ -190,6 +196,7 @@ cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, i
   p.w = w;
   p.counters = ws.prep_cnt;
   p.sg = sg;
+  p.act4 = act4 ? 1 : 0;
   p.ws = ws;
   dim3 grid;
   if (route) {

@@ -50,6 +50,40 @@ __global__ void quantize_gather_kernel(const uint16_t* __restrict__ x, int P, in
   }
 }
 
+// The FP4-activation variant of the two quantisers above: 8 values -> 4 bytes.
+__global__ void quantize_act4_kernel(const uint4* __restrict__ x, int n8, uint32_t* __restrict__ q,
+                                     uint8_t* __restrict__ s) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const unsigned quad = 0xFu << (lane & ~3);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += gridDim.x * blockDim.x) {
+    int e;
+    q[i] = quant4(x[i], quad, &e);
+    if ((lane & 3) == 0) s[i >> 2] = (uint8_t)(e + 127);
+  }
+}
+
+__global__ void quantize_gather4_kernel(const uint16_t* __restrict__ x, int P, int H,
+                                        const int32_t* __restrict__ pos_tok, uint32_t* __restrict__ xg,
+                                        uint8_t* __restrict__ xgs) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const unsigned quad = 0xFu << (lane & ~3);
+  const int per_row = H / 8;
+  for (int p = blockIdx.x; p < P; p += gridDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)pos_tok[p] * H);
+    uint32_t* dst = xg + (size_t)p * per_row;
+    uint8_t* dsts = xgs + (size_t)p * (H / 32);
+    for (int j = threadIdx.x; j < per_row; j += blockDim.x) {
+      int e;
+      dst[j] = quant4(src[j], quad, &e);
+      if ((lane & 3) == 0) dsts[j >> 2] = (uint8_t)(e + 127);
+    }
+  }
+}
+
 // Expert segments in one CTA of 1024 threads (segments.cuh).
 __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restrict__ idx, int T,
                                                         int k, int E, int ns, int bn, Workspace ws,
@@ -175,10 +209,25 @@ cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_share
   return cudaGetLastError();
 }
 
+cudaError_t launch_quantize_act4(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s,
+                                 cudaStream_t st) {
+  const int n8 = T * (H / 8);
+  if (n8 == 0) return cudaSuccess;
+  int blocks = (n8 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  { cudaError_t le_ = launch_pdl(quantize_act4_kernel, dim3(blocks), dim3(256), 0, st, reinterpret_cast<const uint4*>(x), n8,
+                                 reinterpret_cast<uint32_t*>(q), s); if (le_ != cudaSuccess) return le_; }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_gather(const uint16_t* x, int P, int H, const int32_t* pos_tok,
-                                   uint8_t* xg, uint8_t* xgs, cudaStream_t st) {
+                                   uint8_t* xg, uint8_t* xgs, bool act4, cudaStream_t st) {
   if (P == 0) return cudaSuccess;
   const int blocks = P < 65536 ? P : 65536;
+  if (act4) {
+    { cudaError_t le_ = launch_pdl(quantize_gather4_kernel, dim3(blocks), dim3(256), 0, st, x, P, H, pos_tok, reinterpret_cast<uint32_t*>(xg), xgs); if (le_ != cudaSuccess) return le_; }
+    return cudaGetLastError();
+  }
   { cudaError_t le_ = launch_pdl(quantize_gather_kernel, dim3(blocks), dim3(256), 0, st, x, P, H, pos_tok, reinterpret_cast<uint2*>(xg), xgs); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }

@@ -128,6 +128,26 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, u
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem));
 }
 
+// Instruction descriptor of kind::mxf4 (A and B packed E2M1, UE8M0 scales,
+// fp32 accumulate, both K-major); sf_id picks scale bytes 0-1 or 2-3 of the
+// scale words (two 32-blocks per K = 64 instruction).
+__device__ __forceinline__ uint32_t idesc_e2m1_e2m1(int m, int n, uint32_t sf_id) {
+  return (sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(m >> 4) << 24) | (sf_id << 29);
+}
+
+// D (+)= A * B with both operands packed E2M1 in shared memory (K = 64 per
+// instruction: 32 bytes of each 128-byte swizzled row), two UE8M0 scales per
+// row and instruction from TMEM.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{.reg .pred p; setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], "
+      "[%6], p;}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem));
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -63,11 +63,11 @@ def run_forward(L, x_bits, idx, w, residual_bits=None, H=None):
     return y.cpu().numpy().view(np.uint16)
 
 
-def oracle_layer(wl, layer, x_bits, idx, w, residual=None):
+def oracle_layer(wl, layer, x_bits, idx, w, residual=None, act4=False):
     ids = np.unique(idx)
     ids = ids[(ids >= 0) & (ids < wl.n_experts)]
     experts = sg.host_experts(wl, layer, ids)
     shared = [synth.host_expert(wl, layer, wl.n_experts + s) for s in range(wl.n_shared)]
     y, _ = oracle.moe_layer(x_bits, idx, w, experts, shared, wl.n_experts, wl.inter,
-                            residual=residual)
+                            residual=residual, act4=act4)
     return y

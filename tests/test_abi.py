@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def _declared():
     src = open(os.path.join(ROOT, "include", "moe_ffn.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src))
+    return set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src))
 
 
 def test_header_declares_the_binding_exports():

@@ -481,3 +481,77 @@ def test_tiny_batches_step_forward_and_oracle(wl):
     assert L.sync() == m.MOE_ERR_INTERNAL
     assert np.array_equal(gu.run_forward(L, x, idx, w), y)
     L.close()
+
+
+# ---- FP4-activation variant (MOE_OPT_ACT_FORMAT): x and h as E2M1 per 32,
+# expert GEMMs on kind::mxf4
+
+def test_quantize_act4_bit_exact_exhaustive_bf16():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = synth.bf16_bits_to_f32(bits)
+    fin = bits[np.isfinite(vals)]
+    rng = np.random.default_rng(4)
+    a = fin[: fin.size // 256 * 256].reshape(-1, 256)
+    b = rng.permutation(fin)[: fin.size // 256 * 256].reshape(-1, 256)
+    x = np.concatenate([a, b, np.zeros((1, 256), np.uint16), np.full((1, 256), 0x8000, np.uint16)])
+    wl = TINY  # hidden 256
+    L, _ = gu.make_layer(wl, max_tokens=x.shape[0])
+    q = torch.empty((x.shape[0], x.shape[1] // 2), dtype=torch.uint8, device=gu.DEV)
+    s = torch.empty((x.shape[0], x.shape[1] // 32), dtype=torch.uint8, device=gu.DEV)
+    L.quantize_act4(sg.bf16_tensor(x), x.shape[0], q, s)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quantize_act4(x)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    qq = q.cpu().numpy()
+    bad = np.argwhere(qq != rq)
+    assert bad.size == 0, [(x[i, 2 * j:2 * j + 2], qq[i, j], rq[i, j]) for i, j in bad[:5]]
+    L.close()
+
+
+ACT4 = [
+    Workload("a4_h512_i256_e16_k6_t3", 512, 256, 16, 6, 1, 3, seed=41, scale_lo=-6, scale_hi=-2),
+    Workload("a4_h512_i256_e32_k4_s2_t80", 512, 256, 32, 4, 2, 80, seed=42, scale_lo=-6, scale_hi=-2),
+    Workload("a4_h512_i256_e16_k4_t600", 512, 256, 16, 4, 1, 600, seed=43, scale_lo=-8, scale_hi=-4),
+    SPLIT[2],  # 5120 x 2304: the split partition on both GEMMs
+]
+
+
+@pytest.mark.parametrize("wl", ACT4, ids=lambda w: w.name)
+def test_fp4_activation_layer_matches_oracle(wl):
+    L, _ = gu.make_layer(wl)
+    L.set_act_format(m.MOE_ACT_FP4)
+    x = _x(wl)
+    T, E, k = wl.tokens, wl.n_experts, wl.top_k
+    xt = sg.bf16_tensor(x)
+    y = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=gu.DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=gu.DEV)
+    L.step(xt, T, y, idx=idx, w=w)
+    assert L.sync() == m.MOE_OK
+    y, idx, w = y.cpu().numpy().view(np.uint16), idx.cpu().numpy(), w.cpu().numpy()
+    # route then forward gives the same bits; the layer is the oracle's FP4 variant
+    assert np.array_equal(gu.run_forward(L, x, idx, w), y)
+    gu.assert_y_close(y, gu.oracle_layer(wl, 0, x, idx, w, act4=True))
+    # and not the FP8 layer
+    y8 = gu.oracle_layer(wl, 0, x, idx, w)
+    d4 = np.abs(synth.bf16_bits_to_f32(y) - synth.bf16_bits_to_f32(y8)).max()
+    assert d4 > 0
+    L.close()
+
+
+def test_fp4_activation_option_rules():
+    L, _ = gu.make_layer(TINY)  # inter 128: not a multiple of 256
+    with pytest.raises(m.MoeError) as e:
+        L.set_act_format(m.MOE_ACT_FP4)
+    assert e.value.status == m.MOE_ERR_UNSUPPORTED
+    L.close()
+    L, _ = gu.make_layer(ACT4[0])
+    L.set_act_format(m.MOE_ACT_FP4)
+    with pytest.raises(m.MoeError) as e:
+        L.set_option(m.MOE_OPT_PATH, m.PATH_SIMT)
+    assert e.value.status == m.MOE_ERR_UNSUPPORTED
+    with pytest.raises(m.MoeError):
+        L.set_act_format(7)
+    L.set_act_format(m.MOE_ACT_FP8)
+    L.set_option(m.MOE_OPT_PATH, m.PATH_SIMT)  # allowed again with FP8 activations
+    L.close()
