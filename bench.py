@@ -45,6 +45,8 @@ def parse():
     p.add_argument("--path", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor cores")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--graph", type=int, default=1, help="1: launch each step as a captured CUDA graph, 0: stream launches")
+    p.add_argument("--mma-rates", action="store_true",
+                   help="build and run the tensor-core MMA issue-rate microbenchmark, then exit")
     p.add_argument("--act", default="fp8", choices=["fp8", "fp4"],
                    help="activation format: fp8 (the layer) or fp4 (the FP4-activation variant)")
     return p.parse_args()
@@ -130,18 +132,21 @@ def layer_bytes(wl, n_experts_touched: int, T: int) -> dict:
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu capture
 # summarised in profiles/ffn_mma_decode_e24_t1_full.md; valid only for the kernel source it was
 # taken on and for a decode token (7 experts streamed per launch, as in that capture).
-_TRAFFIC_SRC = "mxfp4_expert_ffn_gb300/csrc/ffn_mma.cu"
-_TRAFFIC_SHA256 = "61d8ccfb1a5b688dc3c0b2574e1d72be49e3955e6987f6d8f2681087d700cbec"
-_TRAFFIC = {("v41_layer_decode_t1", "ffn_up_mma"): (88.534272 + 2.638336) * 1e6,
-            ("v41_layer_decode_t1", "ffn_down_mma"): (43.983872 + 0.027136) * 1e6}
+_TRAFFIC_SRC = ("mxfp4_expert_ffn_gb300/csrc/ffn_mma_kernel.cuh", "mxfp4_expert_ffn_gb300/csrc/ffn_mma.cu")
+_TRAFFIC_SHA256 = "c97268edcc356ae643b8d6dfc798cea6cd3af75d9f1454b7ebb02f6d81c9029b"
+_TRAFFIC = {("v41_layer_decode_t1", "ffn_up_mma"): (88.489472 + 2.591744) * 1e6,
+            ("v41_layer_decode_t1", "ffn_down_mma"): (43.978752 + 0.014336) * 1e6}
 
 
 def measured_traffic(workload: str, kernel: str):
     import hashlib
     try:
-        with open(os.path.join(ROOT, _TRAFFIC_SRC), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != _TRAFFIC_SHA256:
-                return None  # the kernel changed since the counters were taken
+        h = hashlib.sha256()
+        for src in _TRAFFIC_SRC:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != _TRAFFIC_SHA256:
+            return None  # the kernel changed since the counters were taken
     except OSError:
         return None
     return _TRAFFIC.get((workload, kernel))
@@ -422,8 +427,22 @@ def run_ours(args):
     return 0
 
 
+def run_mma_rates() -> int:
+    """Cycles per block-scaled tcgen05.mma (no memory traffic), both kinds the
+    expert GEMM uses; prints the microbenchmark's table."""
+    import subprocess
+    import tempfile
+    src = os.path.join(ROOT, "mxfp4_expert_ffn_gb300", "mma_rate.cu")
+    with tempfile.TemporaryDirectory() as d:
+        exe = os.path.join(d, "mma_rate")
+        subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe, src])
+        return subprocess.call([exe])
+
+
 def main():
     args = parse()
+    if args.mma_rates:
+        return run_mma_rates()
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
