@@ -221,7 +221,7 @@ _MAT_KEYS = ("gate", "up", "down")
 
 
 class _Mat(C.Structure):
-    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p)]
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("fmt", C.c_int)]
 
 
 class _Expert(C.Structure):
@@ -236,7 +236,7 @@ def _expert_struct(ex: dict | None, keep: list) -> _Expert:
         c = _c(ex[f"{m}_codes"], np.uint8)
         sc = _c(ex[f"{m}_scales"], np.uint8)
         keep += [c, sc]
-        setattr(s, m, _Mat(c.ctypes.data, sc.ctypes.data))
+        setattr(s, m, _Mat(c.ctypes.data, sc.ctypes.data, int(ex.get("fmt", 0))))
     return s
 
 
@@ -246,7 +246,7 @@ def expert_ffn(ex: dict, xq_row, xs_row, act4: bool = False) -> dict:
     keep: list = []
     st = _expert_struct(ex, keep)
     I, H2 = ex["gate_codes"].shape
-    H = 2 * H2
+    H = H2 if int(ex.get("fmt", 0)) == 1 else 2 * H2  # FP8 codes: one byte per element
     xq = _c(xq_row, np.uint8)
     xs = _c(xs_row, np.uint8)
     h = np.zeros(I, np.float64)

@@ -350,9 +350,20 @@ void orc_segments(const int32_t* idx, int T, int k, int E, int32_t* off, int32_t
 
 /* ------------------------------------------------------------------ experts */
 
+/* A weight matrix with N output rows and K inputs, in one of two formats:
+ *  fmt 0 (MXFP4, every expert by default): codes [N][K/2], two E2M1 per byte,
+ *        low nibble = even k, high nibble = odd k; scales [N][K/32] UE8M0, one per
+ *        row and 32 inputs;
+ *  fmt 1 (FP8 with 32 x 32 blocks, the shared-expert variant): codes [N][K] E4M3;
+ *        scales [N/32][K/32] UE8M0, one per block of 32 rows x 32 inputs -- the
+ *        checkpoint's dense-layer scheme (FreeToken issue #444, "Is the quantization
+ *        already supported": quant_method fp8, weight_block_size [32, 32],
+ *        scale_fmt ue8m0; ai.rs, "The defect that never raised an error": the
+ *        fp8 scale block is 32 x 32). */
 typedef struct {
-  const uint8_t* codes;  /* [N][K/2], low nibble = even k, high nibble = odd k */
-  const uint8_t* scales; /* [N][K/32] UE8M0 */
+  const uint8_t* codes;
+  const uint8_t* scales;
+  int fmt;
 } orc_mat;
 
 typedef struct {
@@ -366,8 +377,11 @@ __attribute__((constructor)) static void orc_fill_tables(void) {
   for (int s = 0; s < 256; ++s) orc_ue8m0_table[s] = orc_ue8m0_value(s);
 }
 
-/* Element (r, c) of an MXFP4 matrix with K columns. */
+/* Element (r, c) of a weight matrix with K columns. */
 static double orc_mx_weight(const orc_mat* m, int K, int r, int c) {
+  if (m->fmt == 1)
+    return orc_e4m3_value(m->codes[(size_t)r * K + c]) *
+           orc_ue8m0_table[m->scales[(size_t)(r / 32) * (K / 32) + c / 32]];
   uint8_t byte = m->codes[(size_t)r * (K / 2) + c / 2];
   int code = (c % 2 == 0) ? (byte & 15) : (byte >> 4);
   return orc_e2m1_value(code) * orc_ue8m0_table[m->scales[(size_t)r * (K / 32) + c / 32]];

@@ -135,6 +135,42 @@ def host_expert(wl: "Workload", layer: int, expert: int) -> dict:
     }
 
 
+# The shared-expert FP8 variant: E4M3 codes with one UE8M0 scale per 32 x 32
+# block, drawn from streams of their own (matrix ids 4..6).  Scale exponents
+# sit 6 below the MXFP4 range, since E4M3 reaches 448 where E2M1 reaches 6.
+FP8_STREAM_OFFSET = 4
+
+
+def fp8_code_bytes(seed, layer, matrix, expert, n_rows, k_cols) -> np.ndarray:
+    """E4M3 codes of one FP8 matrix, [n_rows][k_cols]: uniform bytes with the two
+    NaN codes (0x7F, 0xFF) moved to +-448 (0x7E, 0xFE)."""
+    b = stream_bytes(stream_key(seed, layer, matrix + FP8_STREAM_OFFSET, CODES, expert), n_rows * k_cols)
+    b = np.where((b & 0x7F) == 0x7F, b ^ 1, b).astype(np.uint8)
+    return b.reshape(n_rows, k_cols)
+
+
+def fp8_block_scale_bytes(seed, layer, matrix, expert, n_rows, k_cols, lo, hi) -> np.ndarray:
+    """UE8M0 scale bytes of one FP8 matrix, one per 32 x 32 block: [n_rows/32][k_cols/32]."""
+    n = (n_rows // 32) * (k_cols // 32)
+    b = stream_bytes(stream_key(seed, layer, matrix + FP8_STREAM_OFFSET, SCALES, expert), n, SCALES, lo, hi)
+    return b.reshape(n_rows // 32, k_cols // 32)
+
+
+def host_expert_fp8(wl: "Workload", layer: int, expert: int) -> dict:
+    """A shared expert in the FP8 (32 x 32 block) format; "fmt": 1 tells the oracle."""
+    H, I, sd = wl.hidden, wl.inter, wl.seed
+    lo, hi = wl.scale_lo - 6, wl.scale_hi - 6
+    return {
+        "fmt": 1,
+        "gate_codes": fp8_code_bytes(sd, layer, GATE, expert, I, H),
+        "gate_scales": fp8_block_scale_bytes(sd, layer, GATE, expert, I, H, lo, hi),
+        "up_codes": fp8_code_bytes(sd, layer, UP, expert, I, H),
+        "up_scales": fp8_block_scale_bytes(sd, layer, UP, expert, I, H, lo, hi),
+        "down_codes": fp8_code_bytes(sd, layer, DOWN, expert, H, I),
+        "down_scales": fp8_block_scale_bytes(sd, layer, DOWN, expert, H, I, lo, hi),
+    }
+
+
 def f32_to_bf16_bits(f: np.ndarray) -> np.ndarray:
     """Round float32 to bf16 (nearest, ties to even) and return the 16-bit patterns."""
     u = np.ascontiguousarray(f, dtype=np.float32).view(np.uint32).astype(np.uint64)

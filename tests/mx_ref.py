@@ -134,3 +134,12 @@ def fp4_block_quant_f64(v: np.ndarray) -> np.ndarray:
     e = block_exponent4_closed_form(np.abs(blocks).max(axis=-1))
     r = e2m1_round_closed_form(np.ldexp(blocks, -e[..., None]))
     return np.ldexp(r, e[..., None]).reshape(v.shape)
+
+
+def dequant_fp8_block32(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Dense fp64 matrix from E4M3 codes [N][K] (torch's float8_e4m3fn decoding)
+    and one UE8M0 scale per 32 x 32 block [N/32][K/32]."""
+    vals = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    vals = vals.to(torch.float64).numpy()
+    sc = np.ldexp(1.0, np.asarray(scales, dtype=np.int64) - 127)
+    return vals * np.repeat(np.repeat(sc, 32, axis=0), 32, axis=1)

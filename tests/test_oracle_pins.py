@@ -558,3 +558,64 @@ def test_identity_like_expert_closed_form_fp4_activations():
             ref[t] += w[t, j] * expert_out(e - 1, 1 - e, e % 2)[t]
     assert np.allclose(y64, ref, rtol=1e-12, atol=0)
     assert (y64[:, I:] == 0).all()
+
+
+# ---- FP8 shared expert (E4M3 weights, one UE8M0 scale per 32 x 32 block)
+
+def _dense_any(ex):
+    if ex.get("fmt", 0) == 1:
+        return {m: mx_ref.dequant_fp8_block32(ex[f"{m}_codes"], ex[f"{m}_scales"]) for m in ("gate", "up", "down")}
+    return _dense(ex)
+
+
+def test_brute_force_dense_tiny_layer_fp8_shared_expert():
+    wl = TINY
+    experts, _ = _tiny_bank(wl)
+    shared = [synth.host_expert_fp8(wl, 0, wl.n_experts)]
+    x = synth.activations(wl)
+    lg = oracle.router_logits(x, synth.router_weights(wl))
+    idx, w = oracle.topk(lg, wl.top_k)
+    _, y64 = oracle.moe_layer(x, idx, w, experts, shared, wl.n_experts, wl.inter)
+    xq, xs = mx_ref.fp8_block_quant_torch(mx_ref.bf16_to_f64(x))
+    xh = mx_ref.fp8_block_dequant_torch(xq, xs)
+
+    def ffn(d):
+        g, u = xh @ d["gate"].T, xh @ d["up"].T
+        return mx_ref.fp8_block_quant_f64(g / (1 + np.exp(-g)) * u) @ d["down"].T
+
+    ref = ffn(_dense_any(shared[0]))
+    for e, ex in experts.items():
+        m = np.zeros(wl.tokens)
+        for j in range(idx.shape[1]):
+            m += np.where(idx[:, j] == e, w[:, j], 0.0)
+        ref = ref + m[:, None] * ffn(_dense(ex))
+    assert np.allclose(y64, ref, rtol=1e-9, atol=1e-9 * np.abs(ref).max())
+
+
+def test_fp8_shared_expert_identity_closed_form_and_block_scales():
+    # gate = up = P (E4M3 code 0x38 = 1.0) with a different power of two in each
+    # 32 x 32 block row, down = P^T: the closed form needs the block of each row
+    H, I = 256, 128
+    one = 0x38
+    g = np.zeros((I, H), np.uint8)
+    g[np.arange(I), np.arange(I)] = one
+    d = np.zeros((H, I), np.uint8)
+    d[np.arange(I), np.arange(I)] = one
+    a = np.arange(I // 32) - 1                       # gate exponent per block row
+    gs = np.repeat((127 + a)[:, None], H // 32, axis=1).astype(np.uint8)
+    us = np.full((I // 32, H // 32), 127, np.uint8)
+    ds = np.full((H // 32, I // 32), 126, np.uint8)   # down x 1/2
+    shared = [{"fmt": 1, "gate_codes": g, "gate_scales": gs, "up_codes": g.copy(), "up_scales": us,
+               "down_codes": d, "down_scales": ds}]
+    rng = np.random.default_rng(29)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((5, H)).astype(np.float32) * 2)
+    idx = np.zeros((5, 0), np.int32)
+    w = np.zeros((5, 0))
+    _, y64 = oracle.moe_layer(x, idx, w, {}, shared, 4, I)
+    xq, xs = mx_ref.fp8_block_quant_torch(mx_ref.bf16_to_f64(x))
+    xh = mx_ref.fp8_block_dequant_torch(xq, xs)[:, :I]
+    ga = np.repeat(2.0 ** a, 32)[None, :] * xh
+    h = ga / (1 + np.exp(-ga)) * xh
+    ref = np.zeros((5, H))
+    ref[:, :I] = 0.5 * mx_ref.fp8_block_quant_f64(h)
+    assert np.allclose(y64, ref, rtol=1e-12, atol=0)
