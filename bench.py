@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--graph", type=int, default=1, help="1: launch each step as a captured CUDA graph, 0: stream launches")
     p.add_argument("--mma-rates", action="store_true",
                    help="build and run the tensor-core MMA issue-rate microbenchmark, then exit")
+    p.add_argument("--shared", default="mxfp4", choices=["mxfp4", "fp8"],
+                   help="shared experts' weights: mxfp4 (as the routed bank) or fp8 (E4M3, 32 x 32 blocks)")
     p.add_argument("--act", default="fp8", choices=["fp8", "fp4"],
                    help="activation format: fp8 (the layer) or fp4 (the FP4-activation variant)")
     return p.parse_args()
@@ -116,15 +118,17 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
-def layer_bytes(wl, n_experts_touched: int, T: int) -> dict:
+def layer_bytes(wl, n_experts_touched: int, T: int, shared_fp8: bool = False) -> dict:
     """Algorithmic HBM bytes of one layer step and of its two FFN kernels."""
     H, I, E, k, ns = wl.hidden, wl.inter, wl.n_experts, wl.top_k, wl.n_shared
     P = T * k + ns * T
     per_mat = H * I // 2 + H * I // 32
+    # a shared matrix: MXFP4 like the routed ones, or FP8 with one scale per 32 x 32 block
+    sh_mat = H * I + (H // 32) * (I // 32) if shared_fp8 else per_mat
     n = n_experts_touched + ns
-    up = n * 2 * per_mat + T * (H + H // 32) + P * (I + I // 32)
-    down = n * per_mat + P * (I + I // 32) + P * H * 4
-    layer = n * wl.expert_bytes + E * H * 4 + E * 4 + 2 * T * H * 2
+    up = n_experts_touched * 2 * per_mat + ns * 2 * sh_mat + T * (H + H // 32) + P * (I + I // 32)
+    down = n_experts_touched * per_mat + ns * sh_mat + P * (I + I // 32) + P * H * 4
+    layer = n_experts_touched * wl.expert_bytes + ns * 3 * sh_mat + E * H * 4 + E * 4 + 2 * T * H * 2
     return {"layer": layer, "ffn_up_simt": up, "ffn_down_simt": down,
             "ffn_up_mma": up, "ffn_down_mma": down}
 
@@ -238,9 +242,18 @@ def run_ours(args):
     T, H, E, k = wl.tokens, wl.hidden, wl.n_experts, wl.top_k
     nl = wl.layers
     W = [sg.device_layer(wl, l, dev) for l in range(nl)]
+    if args.shared == "fp8":  # the shared experts in the FP8 (32 x 32 block) format
+        for l in range(nl):
+            exs = [synth.host_expert_fp8(wl, l, E + s) for s in range(wl.n_shared)]
+            for mname in ("gate", "up", "down"):
+                for kind in ("codes", "scales"):
+                    a = np.ascontiguousarray(np.stack([e[f"{mname}_{kind}"] for e in exs]))
+                    W[l][f"s_{mname}_{kind}"] = torch.from_numpy(a).to(dev)
     Ls = [m.Layer(H, wl.inter, E, k, wl.n_shared, T, W[l]) for l in range(nl)]
     for L in Ls:
         L.set_option(m.MOE_OPT_PATH, args.path)
+        if args.shared == "fp8":
+            L.set_shared_format(m.MOE_SHARED_FP8_B32)
         if args.act == "fp4":
             L.set_act_format(m.MOE_ACT_FP4)
     n_in = args.steps + args.warmup
@@ -348,7 +361,7 @@ def run_ours(args):
     pk = peaks()
     roofline = None
     if mean_union is not None:
-        b = layer_bytes(wl, mean_union, T)
+        b = layer_bytes(wl, mean_union, T, shared_fp8=args.shared == "fp8")
         if dom in b:
             ach = b[dom] / (dom_ms / 1e3) / 1e9
             roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": pk["hbm_gbs"],
@@ -392,7 +405,8 @@ def run_ours(args):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "fp4xfp4->f32" if args.act == "fp4" else "fp4xfp8->f32", "data": "synthetic",
-                "config": {"workload": wl.name + ("_act_fp4" if args.act == "fp4" else ""), "tokens": T, "hidden": H, "inter": wl.inter,
+                "config": {"workload": wl.name + ("_act_fp4" if args.act == "fp4" else "") +
+                           ("_shared_fp8" if args.shared == "fp8" else ""), "tokens": T, "hidden": H, "inter": wl.inter,
                            "experts": E, "top_k": k, "shared": wl.n_shared, "layers": nl,
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                            "launch": "cuda_graph" if args.graph else "stream",

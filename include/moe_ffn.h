@@ -240,11 +240,26 @@ moe_status moe_sync(moe_layer* layer, void* stream);
  *                  only: MOE_ERR_UNSUPPORTED when H or I is not a multiple of
  *                  256 or the layer has no tensor-core path; MOE_OPT_PATH = 1
  *                  (SIMT) is refused while it is set.
+ *  MOE_OPT_SHARED_FORMAT  how the shared experts' weights (s_gate, s_up, s_down)
+ *                  are stored: MOE_SHARED_MXFP4 (default) as the routed bank;
+ *                  MOE_SHARED_FP8_B32: codes [n_shared][N][K] E4M3 (one byte per
+ *                  element, the two NaN codes not allowed) and scales
+ *                  [n_shared][N/32][K/32] UE8M0, one per block of 32 rows x 32
+ *                  inputs -- the checkpoint's scheme for its FP8 dense layers
+ *                  (FreeToken issue #444, "Is the quantization already
+ *                  supported": weight_block_size [32, 32], scale_fmt ue8m0; ai.rs,
+ *                  "The defect that never raised an error": the fp8 scale block
+ *                  is 32 x 32).  The pointers given at create are read in this
+ *                  format from the next call on (their sizes must match it).
+ *                  Tensor-core path with FP8 activations only: MOE_ERR_UNSUPPORTED
+ *                  without shared experts, with MOE_OPT_PATH = 1 or with FP4
+ *                  activations (and those are refused while it is set).
  * moe_route_static always uses softmax scoring with scale 1.             */
 enum { MOE_OPT_PATH = 1, MOE_OPT_TIMING = 2, MOE_OPT_SCORING = 3, MOE_OPT_ROUTED_SCALE = 4,
-       MOE_OPT_ACT_FORMAT = 5 };
+       MOE_OPT_ACT_FORMAT = 5, MOE_OPT_SHARED_FORMAT = 6 };
 enum { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 };
 enum { MOE_ACT_FP8 = 0, MOE_ACT_FP4 = 1 };
+enum { MOE_SHARED_MXFP4 = 0, MOE_SHARED_FP8_B32 = 1 };
 moe_status moe_set_option(moe_layer* layer, int32_t option, int64_t value);
 
 /* Per-kernel timing gathered while MOE_OPT_TIMING is on (synchronises the

@@ -16,6 +16,8 @@ LIB_PATH = os.path.join(_HERE, "libmoe_ffn.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_INTERNAL = 4, 5, 6
 MOE_OPT_PATH, MOE_OPT_TIMING, MOE_OPT_SCORING, MOE_OPT_ROUTED_SCALE, MOE_OPT_ACT_FORMAT = 1, 2, 3, 4, 5
+MOE_OPT_SHARED_FORMAT = 6
+MOE_SHARED_MXFP4, MOE_SHARED_FP8_B32 = 0, 1
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 MOE_ACT_FP8, MOE_ACT_FP4 = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_MMA = 0, 1, 2
@@ -241,6 +243,10 @@ class Layer:
     def set_act_format(self, fmt: int):
         """MOE_ACT_FP8 (the layer's definition) or MOE_ACT_FP4 (the variant)."""
         moe_set_option(self.handle, MOE_OPT_ACT_FORMAT, fmt)
+
+    def set_shared_format(self, fmt: int):
+        """MOE_SHARED_MXFP4 (default) or MOE_SHARED_FP8_B32 for the shared experts' weights."""
+        moe_set_option(self.handle, MOE_OPT_SHARED_FORMAT, fmt)
 
     def segments(self, idx, T, offsets, perm, stream=None):
         moe_segments(self.handle, idx, T, offsets, perm, stream)

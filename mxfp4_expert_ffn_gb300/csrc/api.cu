@@ -276,7 +276,8 @@ moe_status moe_set_option(moe_layer* L, int32_t option, int64_t value) {
   if (option == MOE_OPT_PATH) {
     if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
     if (value == 2 && !L->maps) return MOE_ERR_UNSUPPORTED;
-    if (value == 1 && L->act_format == MOE_ACT_FP4) return MOE_ERR_UNSUPPORTED;  // no SIMT FP4 path
+    if (value == 1 && (L->act_format == MOE_ACT_FP4 || L->shared_format == MOE_SHARED_FP8_B32))
+      return MOE_ERR_UNSUPPORTED;  // no SIMT path for either variant
     L->path = (int)value;
     return MOE_OK;
   }
@@ -294,10 +295,22 @@ moe_status moe_set_option(moe_layer* L, int32_t option, int64_t value) {
     L->routed_scale = f;
     return MOE_OK;
   }
+  if (option == MOE_OPT_SHARED_FORMAT) {
+    if (value != MOE_SHARED_MXFP4 && value != MOE_SHARED_FP8_B32) return MOE_ERR_INVALID_ARG;
+    // FP8 shared experts: tensor-core path with FP8 activations only
+    if (value == MOE_SHARED_FP8_B32 &&
+        (!L->maps || L->cfg.n_shared == 0 || L->path == 1 || L->act_format == MOE_ACT_FP4))
+      return MOE_ERR_UNSUPPORTED;
+    if (value == L->shared_format) return MOE_OK;
+    if (!mma_maps_set_shared_format(L->maps, L->cfg, L->w, value == MOE_SHARED_FP8_B32)) return MOE_ERR_UNSUPPORTED;
+    L->shared_format = (int)value;
+    return MOE_OK;
+  }
   if (option == MOE_OPT_ACT_FORMAT) {
     if (value != MOE_ACT_FP8 && value != MOE_ACT_FP4) return MOE_ERR_INVALID_ARG;
     // FP4 activations run on the tensor cores only, for H and I multiples of 256
     if (value == MOE_ACT_FP4 && (!L->maps || !mma_act4_supported(L->cfg))) return MOE_ERR_UNSUPPORTED;
+    if (value == MOE_ACT_FP4 && L->shared_format == MOE_SHARED_FP8_B32) return MOE_ERR_UNSUPPORTED;
     L->act_format = (int)value;
     return MOE_OK;
   }
@@ -420,10 +433,11 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool gather, const float* w
                     const void* residual, void* y, cudaStream_t st) {
   const moe_config& c = L->cfg;
   const ExpertBank bank = bank_of(L);
+  const int ns_tiles = c.n_shared * ((T + bn - 1) / bn);
   cudaError_t e;
   {
     TimedScope ts(L, st, "ffn_up_mma");
-    e = launch_ffn_mma(*L->maps, bank, 0, bn, gather, L->ws, L->num_sms, st, nullptr, act4_of(L));
+    e = launch_ffn_mma(*L->maps, bank, 0, bn, gather, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   if (gather && c.n_shared > 0) {
@@ -432,11 +446,11 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool gather, const float* w
     const CombineArgs cmb{T, c.top_k, c.n_shared, w, static_cast<const uint16_t*>(residual),
                           static_cast<uint16_t*>(y)};
     TimedScope ts(L, st, "ffn_down_mma");
-    return cuda_fail(launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, &cmb, act4_of(L)));
+    return cuda_fail(launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, &cmb, act4_of(L), ns_tiles));
   }
   {
     TimedScope ts(L, st, "ffn_down_mma");
-    e = launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, nullptr, act4_of(L));
+    e = launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   {
@@ -479,7 +493,8 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
     if (e != cudaSuccess) return cuda_fail(e);
     return ffn_tail(L, T, bn, false, w, residual, y, st);
   } else {
-    if (act4_of(L)) return MOE_ERR_UNSUPPORTED;  // FP4 activations: tensor cores only
+    // the FP4-activation and FP8-shared-expert variants run on the tensor cores only
+    if (act4_of(L) || L->shared_format == MOE_SHARED_FP8_B32) return MOE_ERR_UNSUPPORTED;
     {
       TimedScope ts(L, st, "quantize_act");
       e = launch_quantize_act(static_cast<const uint16_t*>(x), T, c.hidden, L->ws.xq, L->ws.xs, st);

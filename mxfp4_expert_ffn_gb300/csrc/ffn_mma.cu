@@ -56,21 +56,24 @@ int chunks_per_stage(int K, bool allow3) {
 // matrix}: the matrix stride is the distance between the two banks, so one
 // box {128, 128, ch, 2} loads the same rows of both.  Needs the distance to be
 // a multiple of 32 bytes; *swap tells that the up bank comes first.
-// packed: the bytes as they are (FP4-activation variant: 128-byte chunks of
-// 256 elements, for kind::mxf4) instead of the one-byte-per-element expansion.
+// fmt: how the banks' bytes are read -- kExpand: packed E2M1 expanded to a
+// byte per element (128-element chunks); kPacked: the packed bytes as they are
+// (FP4-activation variant: 128-byte chunks of 256 elements, for kind::mxf4);
+// kBytes: one byte per element already (FP8 shared expert).
+enum { kExpand = 0, kPacked = 1, kBytes = 2 };
 bool map_4d_pair(CUtensorMap* m, const void* gate, const void* up, uint64_t K, uint64_t rows,
-                 uint32_t ch, int* swap, bool packed = false) {
+                 uint32_t ch, int* swap, int fmt = kExpand) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !gate || !up) return false;
   const uintptr_t g = (uintptr_t)gate, u = (uintptr_t)up;
   const uintptr_t lo = g < u ? g : u, dist = g < u ? u - g : g - u;
   if (dist == 0 || dist % 32 != 0 || dist >= (1ull << 40)) return false;
   *swap = u < g;
-  cuuint64_t dims[4] = {128, rows, K / (packed ? 256 : 128), 2};
-  cuuint64_t strides[3] = {K / 2, packed ? 128u : 64u, (cuuint64_t)dist};
+  cuuint64_t dims[4] = {128, rows, K / (fmt == kPacked ? 256 : 128), 2};
+  cuuint64_t strides[3] = {fmt == kBytes ? K : K / 2, fmt == kExpand ? 64u : 128u, (cuuint64_t)dist};
   cuuint32_t box[4] = {128, 128, ch, 2};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, packed ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4,
+  return enc(m, fmt == kExpand ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
              reinterpret_cast<void*>(lo), dims, strides, box,
              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -88,6 +91,7 @@ struct FormatMaps {
   CUtensorMap xg_half, hq_half;  // CTA pairs: half a 112-token tile, one chunk per box
   int ch_up, ch_down;
   bool ok;
+  bool shared_fp8;  // the shared maps read FP8 (32 x 32 block) weights
 };
 
 struct MmaMaps {
@@ -108,6 +112,7 @@ int mma_tile_for_tokens(int T) { return T <= 64 ? 16 : (T < 512 ? 64 : 112); }
 static bool format_maps(FormatMaps* m, bool a4, const moe_config& c, const moe_weights& w, const Workspace& ws) {
   const uint64_t H = c.hidden, I = c.inter, E = c.n_experts, ns = c.n_shared;
   const uint64_t P = (uint64_t)c.max_tokens * (c.top_k + c.n_shared);
+  m->shared_fp8 = false;
   m->ch_up = a4 ? 1 : chunks_per_stage((int)H, false);
   m->ch_down = a4 ? 1 : chunks_per_stage((int)I, true);
   // weights: a4 views [rows][K/2] bytes as 128-byte chunks; else the 4-bit expansion
@@ -122,10 +127,11 @@ static bool format_maps(FormatMaps* m, bool a4, const moe_config& c, const moe_w
   m->merged[0] = m->merged[1] = 0;
   m->swap_gu[0] = m->swap_gu[1] = 0;
   if (ok) {
-    m->merged[0] = map_4d_pair(&m->gu_pair, w.gate.codes, w.up.codes, H, E * I, m->ch_up, &m->swap_gu[0], a4);
+    m->merged[0] = map_4d_pair(&m->gu_pair, w.gate.codes, w.up.codes, H, E * I, m->ch_up, &m->swap_gu[0],
+                               a4 ? kPacked : kExpand);
     if (ns > 0)
-      m->merged[1] =
-          map_4d_pair(&m->s_gu_pair, w.s_gate.codes, w.s_up.codes, H, ns * I, m->ch_up, &m->swap_gu[1], a4);
+      m->merged[1] = map_4d_pair(&m->s_gu_pair, w.s_gate.codes, w.s_up.codes, H, ns * I, m->ch_up,
+                                 &m->swap_gu[1], a4 ? kPacked : kExpand);
   }
   const uint32_t bns[3] = {16, 64, 112};
   const uint64_t xk = a4 ? H / 2 : H, hk = a4 ? I / 2 : I;  // activation row bytes
@@ -139,6 +145,22 @@ static bool format_maps(FormatMaps* m, bool a4, const moe_config& c, const moe_w
 }
 
 bool mma_act4_supported(const moe_config& c) { return c.hidden % 256 == 0 && c.inter % 256 == 0; }
+
+// The FP8-activation maps of the shared experts for their weight format: MXFP4
+// (expanded, as the routed bank) or FP8 with 32 x 32 blocks (codes read as bytes).
+bool mma_maps_set_shared_format(MmaMaps* mm, const moe_config& c, const moe_weights& w, bool fp8) {
+  FormatMaps* m = &mm->f[0];
+  const uint64_t H = c.hidden, I = c.inter, ns = c.n_shared;
+  if (ns == 0) return false;
+  bool ok = map_3d(&m->s_gate, !fp8, w.s_gate.codes, H, ns * I, 128, m->ch_up) &&
+            map_3d(&m->s_up, !fp8, w.s_up.codes, H, ns * I, 128, m->ch_up) &&
+            map_3d(&m->s_down, !fp8, w.s_down.codes, I, ns * H, 128, m->ch_down);
+  if (ok)
+    m->merged[1] = map_4d_pair(&m->s_gu_pair, w.s_gate.codes, w.s_up.codes, H, ns * I, m->ch_up, &m->swap_gu[1],
+                               fp8 ? kBytes : kExpand);
+  m->shared_fp8 = ok && fp8;
+  return ok;
+}
 
 MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Workspace& ws) {
   MmaMaps* m = new MmaMaps();
@@ -154,11 +176,14 @@ MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Worksp
 void mma_maps_destroy(MmaMaps* m) { delete m; }
 
 cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, int bn, bool gather,
-                           const Workspace& ws, int num_sms, cudaStream_t st, const CombineArgs* cmb, bool act4) {
+                           const Workspace& ws, int num_sms, cudaStream_t st, const CombineArgs* cmb, bool act4,
+                           int ns_tiles) {
   const FormatMaps& mm = maps.f[act4 ? 1 : 0];
   if (!mm.ok) return cudaErrorInvalidValue;
   MmaParams p;
   memset(&p, 0, sizeof(p));
+  p.shared_fp8 = mm.shared_fp8 ? 1 : 0;
+  p.ns_tiles = ns_tiles;
   const int bi = bn_index(bn);
   int ch;
   if (mode == kModeUp) {

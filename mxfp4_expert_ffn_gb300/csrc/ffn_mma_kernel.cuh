@@ -70,6 +70,8 @@ struct MmaParams {
   int32_t* comb_cnt;         // fuse_combine: writers finished per (token, 128-row tile, quadrant)
   const uint8_t* xq;         // gather: E4M3 codes of x by token, [T][K]
   const int32_t* pos_tok;    // gather: token of each position
+  int shared_fp8;            // shared experts in FP8 (E4M3, one scale per 32 x 32 block)
+  int ns_tiles;              // token tiles of the shared experts (the last ones of the table)
   int32_t* err;
 };
 
@@ -350,6 +352,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   const int rank = PAIR ? (int)cluster_ctarank() : -1;
   const int mt_units = PAIR ? mt_per_expert / 2 : mt_per_expert;
   const int total = p.n_active[1] * mt_units;
+  // FP8 shared experts: their tiles close the table, so a unit's format follows
+  // from its index (no tile-table load on the issuing thread)
+  const int shared_tile0 = (!A4 && p.shared_fp8) ? p.n_active[1] - p.ns_tiles : 0x7FFFFFFF;
   const Sched sc0(total, k_stages, BN <= 64 && p.split_ok, PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x,
                   PAIR ? (int)gridDim.x / 2 : (int)gridDim.x);
 
@@ -399,7 +404,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           }
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); ok = false; break; }
           uint8_t* sa = stage_base + slot * stage_bytes;
-          mbar_expect_tx(&full_bar[slot], tx_stage);
+          // FP8 shared weights arrive as bytes: twice the packed FP4 count
+          mbar_expect_tx(&full_bar[slot], tx_stage + (pc.u / mt_units >= shared_tile0 ? NA * 128 * 64 * CH : 0));
           if (NA == 2 && p.merged[sh]) {
             // gate and up rows of the stage in one op: {chunk elems, rows, chunks, matrix}
             tma_load_4d(sa, sh ? &p.a_shared[0] : &p.a_routed[0], 0, erow, s * CH, 0, &full_bar[slot]);
@@ -472,7 +478,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             NI = C::kSplitN ? (j == 0 ? min(C::kN0, nr) : nr - C::kN0) : nr;
           }
         }
-        const uint32_t idesc_base = A4 ? idesc_e2m1_e2m1(128, NI > 0 ? NI : 16, 0) : idesc_e2m1_e4m3(128, NI > 0 ? NI : 16, 0);
+        uint32_t idesc_base = A4 ? idesc_e2m1_e2m1(128, NI > 0 ? NI : 16, 0) : idesc_e2m1_e4m3(128, NI > 0 ? NI : 16, 0);
+        if (pc.u / mt_units >= shared_tile0) idesc_base &= ~(7u << 7);  // A = E4M3 (FP8 shared expert)
         bool ok = true;
         const int s_beg = pc.s0, s_end = pc.s1;
         for (int s = s_beg; s < s_end; ++s, ++g) {
@@ -551,7 +558,10 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       const size_t erow = (size_t)(sh ? un.e - p.E : un.e) * p.rows + un.row0 + 32 * q + lane;
       const uint8_t* sa_row[NA];
 #pragma unroll
-      for (int m = 0; m < NA; ++m) sa_row[m] = (sh ? p.sa_shared[m] : p.sa_routed[m]) + erow * (p.K / 32);
+      for (int m = 0; m < NA; ++m)
+        sa_row[m] = (sh ? p.sa_shared[m] : p.sa_routed[m]) +
+                    // FP8 shared: one scale per 32 x 32 block, shared by the warp's 32 rows
+                    (pc.u / mt_units >= shared_tile0 ? (erow >> 5) : erow) * (p.K / 32);
       const uint8_t* sb_row[NC];
 #pragma unroll
       for (int cb = 0; cb < NC; ++cb) {

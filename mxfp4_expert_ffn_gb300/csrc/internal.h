@@ -84,6 +84,7 @@ struct moe_layer {
   int scoring = 0;            // MOE_SCORING_SOFTMAX / MOE_SCORING_SIGMOID
   float routed_scale = 1.0f;  // routed weights are multiplied by it
   int act_format = 0;         // MOE_ACT_FP8 / MOE_ACT_FP4
+  int shared_format = 0;      // MOE_SHARED_MXFP4 / MOE_SHARED_FP8_B32
   bool timing = false;
   moe::Workspace ws;
   moe::MmaMaps* maps = nullptr;  // TMA descriptors of the tensor-core path
@@ -171,9 +172,12 @@ struct CombineArgs {
 // through pos_tok instead of from the slot-ordered copy xg/xgs.  cmb (down,
 // bn <= 64): the combine runs inside the down GEMM (needs T <= kPrepMaxTokens).
 // act4: the FP4-activation variant (xg/xq/hq hold packed E2M1 codes).
+// ns_tiles: token tiles of the shared experts (n_shared x ceil(T / bn)).
 cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn, bool gather,
                            const Workspace& ws, int num_sms, cudaStream_t st,
-                           const CombineArgs* cmb = nullptr, bool act4 = false);
+                           const CombineArgs* cmb = nullptr, bool act4 = false, int ns_tiles = 0);
+// Re-encodes the shared experts' maps for MXFP4 or FP8 (32 x 32 block) weights.
+bool mma_maps_set_shared_format(MmaMaps* m, const moe_config& c, const moe_weights& w, bool fp8);
 // FP4 activations need H and I multiples of 256 (whole 128-byte chunks).
 bool mma_act4_supported(const moe_config& c);
 // Small batches (T <= kPrepMaxTokens): router + top-k (route) or the given

@@ -23,6 +23,27 @@ def make_layer(wl, layer: int = 0, max_tokens: int | None = None, weights=None):
     return L, W
 
 
+def fp8_shared_weights(wl, layer: int = 0, device: str = DEV) -> dict:
+    """Device copies of the shared experts in the FP8 (32 x 32 block) format, keyed
+    like the layer's weight dict (s_gate_codes, ...), stacked over the shared experts."""
+    exs = [synth.host_expert_fp8(wl, layer, wl.n_experts + s) for s in range(wl.n_shared)]
+    out = {}
+    for mname in ("gate", "up", "down"):
+        for kind in ("codes", "scales"):
+            a = np.stack([e[f"{mname}_{kind}"] for e in exs])
+            out[f"s_{mname}_{kind}"] = torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return out
+
+
+def make_layer_fp8_shared(wl, layer: int = 0, max_tokens: int | None = None):
+    """A layer whose shared experts are FP8 with 32 x 32 block scales."""
+    W = sg.device_layer(wl, layer, DEV)
+    W.update(fp8_shared_weights(wl, layer))
+    L, W = make_layer(wl, layer, max_tokens, weights=W)
+    L.set_shared_format(m.MOE_SHARED_FP8_B32)
+    return L, W
+
+
 def bits_to_f64(bits) -> np.ndarray:
     if isinstance(bits, torch.Tensor):
         bits = bits.cpu().numpy()
@@ -63,11 +84,12 @@ def run_forward(L, x_bits, idx, w, residual_bits=None, H=None):
     return y.cpu().numpy().view(np.uint16)
 
 
-def oracle_layer(wl, layer, x_bits, idx, w, residual=None, act4=False):
+def oracle_layer(wl, layer, x_bits, idx, w, residual=None, act4=False, shared_fp8=False):
     ids = np.unique(idx)
     ids = ids[(ids >= 0) & (ids < wl.n_experts)]
     experts = sg.host_experts(wl, layer, ids)
-    shared = [synth.host_expert(wl, layer, wl.n_experts + s) for s in range(wl.n_shared)]
+    gen = synth.host_expert_fp8 if shared_fp8 else synth.host_expert
+    shared = [gen(wl, layer, wl.n_experts + s) for s in range(wl.n_shared)]
     y, _ = oracle.moe_layer(x_bits, idx, w, experts, shared, wl.n_experts, wl.inter,
                             residual=residual, act4=act4)
     return y

@@ -555,3 +555,51 @@ def test_fp4_activation_option_rules():
     L.set_act_format(m.MOE_ACT_FP8)
     L.set_option(m.MOE_OPT_PATH, m.PATH_SIMT)  # allowed again with FP8 activations
     L.close()
+
+
+# ---- FP8 shared expert (MOE_OPT_SHARED_FORMAT): E4M3 weights with one UE8M0
+# scale per 32 x 32 block, routed experts MXFP4
+
+FP8_SHARED = [
+    Workload("s8_h512_i256_e16_k6_t3", 512, 256, 16, 6, 1, 3, seed=51, scale_lo=-6, scale_hi=-2),
+    Workload("s8_h512_i256_e32_k4_s2_t80", 512, 256, 32, 4, 2, 80, seed=52, scale_lo=-6, scale_hi=-2),
+    Workload("s8_h512_i256_e16_k4_t600", 512, 256, 16, 4, 1, 600, seed=53, scale_lo=-8, scale_hi=-4),
+    SPLIT[2],
+]
+
+
+@pytest.mark.parametrize("wl", FP8_SHARED, ids=lambda w: w.name)
+def test_fp8_shared_expert_layer_matches_oracle(wl):
+    L, _ = gu.make_layer_fp8_shared(wl)
+    x = _x(wl)
+    T, k = wl.tokens, wl.top_k
+    xt = sg.bf16_tensor(x)
+    y = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=gu.DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=gu.DEV)
+    L.step(xt, T, y, idx=idx, w=w)
+    assert L.sync() == m.MOE_OK
+    y, idx, w = y.cpu().numpy().view(np.uint16), idx.cpu().numpy(), w.cpu().numpy()
+    assert np.array_equal(gu.run_forward(L, x, idx, w), y)
+    gu.assert_y_close(y, gu.oracle_layer(wl, 0, x, idx, w, shared_fp8=True))
+    # only the shared experts' contribution: zero routed weights
+    w0 = np.zeros_like(w)
+    gu.assert_y_close(gu.run_forward(L, x, idx, w0), gu.oracle_layer(wl, 0, x, idx, w0, shared_fp8=True))
+    L.close()
+
+
+def test_fp8_shared_expert_option_rules():
+    wl = FP8_SHARED[0]
+    L, _ = gu.make_layer_fp8_shared(wl)
+    for bad in ((m.MOE_OPT_PATH, m.PATH_SIMT), (m.MOE_OPT_ACT_FORMAT, m.MOE_ACT_FP4)):
+        with pytest.raises(m.MoeError) as e:
+            L.set_option(*bad)
+        assert e.value.status == m.MOE_ERR_UNSUPPORTED
+    with pytest.raises(m.MoeError):
+        L.set_shared_format(9)
+    L.close()
+    L, _ = gu.make_layer(SMALL[3])  # no shared expert
+    with pytest.raises(m.MoeError) as e:
+        L.set_shared_format(m.MOE_SHARED_FP8_B32)
+    assert e.value.status == m.MOE_ERR_UNSUPPORTED
+    L.close()
