@@ -118,6 +118,21 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(v: float, pg, device) -> float:
+    """The slowest rank's figure (every rank gets it); v itself on one process."""
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return t.item()
+
+
+def job_tokens_per_s(world: int, tokens: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput of N replicas: every rank's tokens over the slowest rank's time."""
+    return world * tokens * steps / (total_ms / 1e3)
+
+
 def layer_bytes(wl, n_experts_touched: int, T: int, shared_fp8: bool = False) -> dict:
     """Algorithmic HBM bytes of one layer step and of its two FFN kernels."""
     H, I, E, k, ns = wl.hidden, wl.inter, wl.n_experts, wl.top_k, wl.n_shared
@@ -324,13 +339,9 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         ms = timed_loop(run)
     clocks = clk.summary()
-    total_ms = sum(ms)
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = t.item()
+    total_ms = max_over_ranks(sum(ms), pg, dev)
     ms_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms / 1e3)
+    value = job_tokens_per_s(world, T, args.steps, total_ms)
 
     # union of experts per step (for byte accounting), outside the timed region
     unions = []
