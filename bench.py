@@ -152,9 +152,9 @@ def layer_bytes(wl, n_experts_touched: int, T: int, shared_fp8: bool = False) ->
 # summarised in profiles/ffn_mma_decode_e24_t1_full.md; valid only for the kernel source it was
 # taken on and for a decode token (7 experts streamed per launch, as in that capture).
 _TRAFFIC_SRC = ("mxfp4_expert_ffn_gb300/csrc/ffn_mma_kernel.cuh", "mxfp4_expert_ffn_gb300/csrc/ffn_mma.cu")
-_TRAFFIC_SHA256 = "c97268edcc356ae643b8d6dfc798cea6cd3af75d9f1454b7ebb02f6d81c9029b"
-_TRAFFIC = {("v41_layer_decode_t1", "ffn_up_mma"): (88.489472 + 2.591744) * 1e6,
-            ("v41_layer_decode_t1", "ffn_down_mma"): (43.978752 + 0.014336) * 1e6}
+_TRAFFIC_SHA256 = "f185e6426d2a2b32175b5cc18d6d184ffbeefa361b27dcbf448eadbe1502d222"
+_TRAFFIC = {("v41_layer_decode_t1", "ffn_up_mma"): (88.526336 + 2.677248) * 1e6,
+            ("v41_layer_decode_t1", "ffn_down_mma"): (43.978752 + 0.041728) * 1e6}
 
 
 def measured_traffic(workload: str, kernel: str):
@@ -350,6 +350,16 @@ def run_ours(args):
             Ls[0].route(xs[i % n_x], T, idx, wt)
             torch.cuda.synchronize()
             unions.append(len(np.unique(idx.cpu().numpy())))
+            continue
+        # a stack: every layer's routing of its own input (the same steps again)
+        cur, xn = xs[i % n_x], bufs[0]
+        for layer in range(nl):
+            nxt = bufs[1] if cur is not bufs[1] else bufs[2]
+            m.moe_rmsnorm(cur, T, H, 1e-6, xn)
+            Ls[layer].step(xn, T, nxt, residual=cur, idx=idx, w=wt)
+            torch.cuda.synchronize()
+            unions.append(len(np.unique(idx.cpu().numpy())))
+            cur = nxt
     mean_union = float(np.mean(unions)) if unions else None
 
     # per-kernel times: the same loop again with the library's event timing on
@@ -380,7 +390,7 @@ def run_ours(args):
                         "traffic": measured_traffic(wl.name, dom),
                         "algorithmic_bytes_per_launch": b[dom], "avg_launch_ms": dom_ms,
                         "peak_src": pk["src"]}
-        layer_gbs = b["layer"] / (ms_step / 1e3) / 1e9
+        layer_gbs = nl * b["layer"] / (ms_step / 1e3) / 1e9  # all layers' bytes over the step
     else:
         layer_gbs = None
 
