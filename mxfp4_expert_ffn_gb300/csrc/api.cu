@@ -484,11 +484,10 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
   }
   if (e != cudaSuccess) return cuda_fail(e);
   if (mma) {
-    const int P = T * (c.top_k + c.n_shared);
     {
-      TimedScope ts(L, st, "quantize_gather");
-      e = launch_quantize_gather(static_cast<const uint16_t*>(x), P, c.hidden, L->ws.pos_tok,
-                                 L->ws.xg, L->ws.xgs, act4_of(L), st);
+      TimedScope ts(L, st, "quantize_scatter");
+      e = launch_quantize_scatter(static_cast<const uint16_t*>(x), T, c.hidden, c.top_k, c.n_shared,
+                                  L->ws.slot_pos, L->ws.xg, L->ws.xgs, act4_of(L), st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return ffn_tail(L, T, bn, false, w, residual, y, st);

@@ -129,8 +129,10 @@ cudaError_t launch_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uin
                                 cudaStream_t st);
 cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared, int bn,
                             const Workspace& ws, cudaStream_t st);
-cudaError_t launch_quantize_gather(const uint16_t* x, int P, int H, const int32_t* pos_tok,
-                                   uint8_t* xg, uint8_t* xgs, bool act4, cudaStream_t st);
+// The codes of x at every position of each token (slot_pos for the routed
+// slots, S + s*T + t for the shared experts), computed once per token.
+cudaError_t launch_quantize_scatter(const uint16_t* x, int T, int H, int k, int ns, const int32_t* slot_pos,
+                                    uint8_t* xg, uint8_t* xgs, bool act4, cudaStream_t st);
 // The FP4-activation variant's quantiser of x by token: q [T][H/2], s [T][H/32].
 cudaError_t launch_quantize_act4(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s,
                                  cudaStream_t st);

@@ -13,6 +13,8 @@
 namespace moe {
 namespace {
 
+constexpr int kMaxPositions = 16;  // positions of one token: top-k (<= 8) + shared experts (<= 4)
+
 // One thread per 8 bf16 values; four consecutive threads form one 32-block.
 __global__ void quantize_act_kernel(const uint4* __restrict__ x, int n8, uint2* __restrict__ q,
                                     uint8_t* __restrict__ s) {
@@ -27,30 +29,7 @@ __global__ void quantize_act_kernel(const uint4* __restrict__ x, int n8, uint2* 
   }
 }
 
-// Same quantisation, written once per position (row p of xg is token
-// pos_tok[p]), so that each expert's activation rows are contiguous.  One CTA
-// per position row (grid-strided), threads over the row's 8-value groups.
-__global__ void quantize_gather_kernel(const uint16_t* __restrict__ x, int P, int H,
-                                       const int32_t* __restrict__ pos_tok, uint2* __restrict__ xg,
-                                       uint8_t* __restrict__ xgs) {
-  pdl_wait();
-  pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const unsigned quad = 0xFu << (lane & ~3);
-  const int per_row = H / 8;  // a multiple of 16: whole quads stay in or out
-  for (int p = blockIdx.x; p < P; p += gridDim.x) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)pos_tok[p] * H);
-    uint2* dst = xg + (size_t)p * per_row;
-    uint8_t* dsts = xgs + (size_t)p * (H / 32);
-    for (int j = threadIdx.x; j < per_row; j += blockDim.x) {
-      int e;
-      dst[j] = quant8(src[j], quad, &e);
-      if ((lane & 3) == 0) dsts[j >> 2] = (uint8_t)(e + 127);
-    }
-  }
-}
-
-// The FP4-activation variant of the two quantisers above: 8 values -> 4 bytes.
+// The FP4-activation variant of the quantiser above: 8 values -> 4 bytes.
 __global__ void quantize_act4_kernel(const uint4* __restrict__ x, int n8, uint32_t* __restrict__ q,
                                      uint8_t* __restrict__ s) {
   pdl_wait();
@@ -64,22 +43,49 @@ __global__ void quantize_act4_kernel(const uint4* __restrict__ x, int n8, uint32
   }
 }
 
-__global__ void quantize_gather4_kernel(const uint16_t* __restrict__ x, int P, int H,
-                                        const int32_t* __restrict__ pos_tok, uint32_t* __restrict__ xg,
+// The codes of x in slot order, token-major: one CTA per token quantises its
+// row once and stores the codes at each of the token's positions (its valid
+// routed slots, slot_pos[t*k + j], and its shared-expert positions
+// S + s*T + t), so each row is read and quantised once instead of once per
+// position.  Positions freed by invalid ids are not written (no tile reads
+// them).  A4: packed E2M1 (4 bytes per 8 values) instead of E4M3.
+template <bool A4>
+__global__ void quantize_scatter_kernel(const uint16_t* __restrict__ x, int T, int H, int k, int ns,
+                                        const int32_t* __restrict__ slot_pos, uint8_t* __restrict__ xg,
                                         uint8_t* __restrict__ xgs) {
   pdl_wait();
   pdl_trigger();
+  __shared__ int32_t pos[kMaxPositions];
   const int lane = threadIdx.x & 31;
   const unsigned quad = 0xFu << (lane & ~3);
-  const int per_row = H / 8;
-  for (int p = blockIdx.x; p < P; p += gridDim.x) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)pos_tok[p] * H);
-    uint32_t* dst = xg + (size_t)p * per_row;
-    uint8_t* dsts = xgs + (size_t)p * (H / 32);
+  const int per_row = H / 8;  // a multiple of 16: whole quads stay in or out
+  const size_t S = (size_t)T * k;
+  const size_t row_bytes = A4 ? H / 2 : H;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    __syncthreads();  // the previous token's positions are no longer read
+    const int np = k + ns;
+    if ((int)threadIdx.x < np)
+      pos[threadIdx.x] = (int)threadIdx.x < k ? slot_pos[(size_t)t * k + threadIdx.x]
+                                              : (int)(S + (size_t)((int)threadIdx.x - k) * T + t);
+    __syncthreads();
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     for (int j = threadIdx.x; j < per_row; j += blockDim.x) {
       int e;
-      dst[j] = quant4(src[j], quad, &e);
-      if ((lane & 3) == 0) dsts[j >> 2] = (uint8_t)(e + 127);
+      uint2 c8 = make_uint2(0u, 0u);
+      uint32_t c4 = 0u;
+      if (A4)
+        c4 = quant4(src[j], quad, &e);
+      else
+        c8 = quant8(src[j], quad, &e);
+      for (int q = 0; q < np; ++q) {
+        const int p = pos[q];
+        if (p < 0) continue;  // an invalid id: the slot has no position
+        if (A4)
+          reinterpret_cast<uint32_t*>(xg + (size_t)p * row_bytes)[j] = c4;
+        else
+          reinterpret_cast<uint2*>(xg + (size_t)p * row_bytes)[j] = c8;
+        if ((lane & 3) == 0) xgs[(size_t)p * (H / 32) + (j >> 2)] = (uint8_t)(e + 127);
+      }
     }
   }
 }
@@ -209,6 +215,19 @@ cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_share
   return cudaGetLastError();
 }
 
+cudaError_t launch_quantize_scatter(const uint16_t* x, int T, int H, int k, int ns, const int32_t* slot_pos,
+                                    uint8_t* xg, uint8_t* xgs, bool act4, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  if (k + ns > kMaxPositions) return cudaErrorInvalidValue;
+  const int blocks = T < 65536 ? T : 65536;
+  if (act4) {
+    { cudaError_t le_ = launch_pdl(quantize_scatter_kernel<true>, dim3(blocks), dim3(256), 0, st, x, T, H, k, ns, slot_pos, xg, xgs); if (le_ != cudaSuccess) return le_; }
+  } else {
+    { cudaError_t le_ = launch_pdl(quantize_scatter_kernel<false>, dim3(blocks), dim3(256), 0, st, x, T, H, k, ns, slot_pos, xg, xgs); if (le_ != cudaSuccess) return le_; }
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_act4(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s,
                                  cudaStream_t st) {
   const int n8 = T * (H / 8);
@@ -217,18 +236,6 @@ cudaError_t launch_quantize_act4(const uint16_t* x, int T, int H, uint8_t* q, ui
   if (blocks > 4096) blocks = 4096;
   { cudaError_t le_ = launch_pdl(quantize_act4_kernel, dim3(blocks), dim3(256), 0, st, reinterpret_cast<const uint4*>(x), n8,
                                  reinterpret_cast<uint32_t*>(q), s); if (le_ != cudaSuccess) return le_; }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_quantize_gather(const uint16_t* x, int P, int H, const int32_t* pos_tok,
-                                   uint8_t* xg, uint8_t* xgs, bool act4, cudaStream_t st) {
-  if (P == 0) return cudaSuccess;
-  const int blocks = P < 65536 ? P : 65536;
-  if (act4) {
-    { cudaError_t le_ = launch_pdl(quantize_gather4_kernel, dim3(blocks), dim3(256), 0, st, x, P, H, pos_tok, reinterpret_cast<uint32_t*>(xg), xgs); if (le_ != cudaSuccess) return le_; }
-    return cudaGetLastError();
-  }
-  { cudaError_t le_ = launch_pdl(quantize_gather_kernel, dim3(blocks), dim3(256), 0, st, x, P, H, pos_tok, reinterpret_cast<uint2*>(xg), xgs); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 

@@ -232,7 +232,6 @@ __device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx, in
 __device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ idx, int T, int k, int E,
                                                    int ns, int bn, const Workspace& ws, int32_t* sm) {
   const int NE = E + ns, S = T * k, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
   int32_t* cnt_s = sm;             // [E]     slots per expert
   int32_t* off_s = sm + E;         // [E]     first position per expert
   int32_t* act_s = sm + 2 * E;     // [NE]    active experts, routed then shared

@@ -603,3 +603,29 @@ def test_fp8_shared_expert_option_rules():
         L.set_shared_format(m.MOE_SHARED_FP8_B32)
     assert e.value.status == m.MOE_ERR_UNSUPPORTED
     L.close()
+
+
+def test_expert_id_out_of_range_above_64_tokens():
+    # the slot-ordered quantiser and the segments kernel (no preparation launch)
+    wl = STEP[-1]  # 80 tokens
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    idx, w = _oracle_routing(wl, x)
+    bad = idx.copy()
+    bad[3, 1] = -5
+    bad[70, 0] = wl.n_experts
+    xt = sg.bf16_tensor(x)
+    y = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    L.forward(xt, wl.tokens, torch.from_numpy(bad).to(gu.DEV),
+              torch.from_numpy(w.astype(np.float32)).to(gu.DEV), y)
+    assert L.sync() == m.MOE_ERR_INTERNAL
+    # the invalid slots contribute nothing: the oracle with their weights zeroed
+    w0 = w.copy()
+    w0[3, 1] = 0.0
+    w0[70, 0] = 0.0
+    ok = bad.copy()
+    ok[3, 1] = idx[3, 1]
+    ok[70, 0] = idx[70, 0]
+    gu.assert_y_close(y.cpu().numpy().view(np.uint16), gu.oracle_layer(wl, 0, x, ok, w0))
+    gu.assert_y_close(gu.run_forward(L, x, idx, w), gu.oracle_layer(wl, 0, x, idx, w))
+    L.close()
