@@ -85,6 +85,9 @@ size_t carve(const moe_config& c, int num_sms, char* base, Workspace& ws) {
   ws.prep_cnt = cv.take<int32_t>(16);
   ws.comb_cnt_n = kPrepMaxTokens * (int)(H / 128) * 4;
   ws.comb_cnt = cv.take<int32_t>((size_t)ws.comb_cnt_n);
+  ws.seg_cbase = cv.take<int32_t>((size_t)kSegCtas * E);
+  ws.seg_counter = cv.take<int32_t>(1);
+  ws.seg_routed = cv.take<int32_t>(1);
   ws.err = cv.take<int32_t>(1);
   return cv.off;
 }

@@ -59,6 +59,9 @@ struct Workspace {
   int32_t* prep_cnt = nullptr;// [16]       small-batch preparation counters (zero between launches)
   int32_t* comb_cnt = nullptr;// [64][H/128][4] fused-combine counters (zeroed by the segments)
   int comb_cnt_n = 0;
+  int32_t* seg_cbase = nullptr; // [kSegCtas][E] large-batch segments: per-CTA counts, then bases
+  int32_t* seg_counter = nullptr; // [1]    its last-arriver counter (zero between launches)
+  int32_t* seg_routed = nullptr;  // [1]    its routed slot total
   int32_t* err = nullptr;     // [1]        device error word
   int32_t* err_host = nullptr;// pinned copy of err
   void* base = nullptr;       // single allocation holding all of the above
@@ -66,6 +69,8 @@ struct Workspace {
 };
 
 struct MmaMaps;
+
+constexpr int kSegCtas = 32;  // CTAs of the large-batch segments
 
 struct Timer {
   const char* name = nullptr;

@@ -43,6 +43,23 @@ __global__ void quantize_act4_kernel(const uint4* __restrict__ x, int n8, uint32
   }
 }
 
+// Large batches: the segments in two launches over many CTAs (segments.cuh).
+__global__ void __launch_bounds__(1024) segments_count_kernel(const int32_t* __restrict__ idx, int T, int k,
+                                                              int E, int ns, int bn, Workspace ws) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ int32_t sm[];
+  segments_count_cta(idx, T, k, E, ns, bn, ws, sm);
+}
+
+__global__ void __launch_bounds__(1024) segments_place_kernel(const int32_t* __restrict__ idx, int T, int k,
+                                                              int E, int ns, Workspace ws) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ int32_t sm[];
+  segments_place_cta(idx, T, k, E, ns, ws, sm);
+}
+
 // The codes of x in slot order, token-major: one CTA per token quantises its
 // row once and stores the codes at each of the token's positions (its valid
 // routed slots, slot_pos[t*k + j], and its shared-expert positions
@@ -207,8 +224,21 @@ cudaError_t launch_quantize_act(const uint16_t* x, int T, int H, uint8_t* q, uin
 size_t segments_smem_bytes(int E) { return (size_t)(36 * E + 2 * 4 + 1) * sizeof(int32_t); }
 constexpr size_t kSegmentsSmemMax = 200 * 1024;  // room for the position table of up to ~30k slots
 
+// One CTA up to kSegSingleMax slots; above, two launches over up to kSegCtas CTAs.
+constexpr int kSegSingleMax = 4096;
+size_t segments_count_smem(int E, int ns) { return (size_t)(36 * E + 2 * ns + 2) * sizeof(int32_t); }
+size_t segments_place_smem(int E) { return (size_t)32 * E * sizeof(int32_t); }
+
 cudaError_t launch_segments(const int32_t* idx, int T, int k, int E, int n_shared, int bn,
                             const Workspace& ws, cudaStream_t st) {
+  const int S = T * k;
+  if (S > kSegSingleMax) {
+    int G = S / 768;
+    G = G < 2 ? 2 : (G > kSegCtas ? kSegCtas : G);
+    { cudaError_t le_ = launch_pdl(segments_count_kernel, dim3(G), dim3(1024), segments_count_smem(E, n_shared), st, idx, T, k, E, n_shared, bn, ws); if (le_ != cudaSuccess) return le_; }
+    { cudaError_t le_ = launch_pdl(segments_place_kernel, dim3(G), dim3(1024), segments_place_smem(E), st, idx, T, k, E, n_shared, ws); if (le_ != cudaSuccess) return le_; }
+    return cudaGetLastError();
+  }
   const size_t base = segments_smem_bytes(E), with_table = base + (size_t)T * k * sizeof(int32_t);
   const bool scatter = with_table <= kSegmentsSmemMax;  // position table in shared memory
   { cudaError_t le_ = launch_pdl(segments_kernel, dim3(1), dim3(1024), scatter ? with_table : base, st, idx, T, k, E, n_shared, bn, ws, scatter ? 1 : 0); if (le_ != cudaSuccess) return le_; }
@@ -241,8 +271,15 @@ cudaError_t launch_quantize_act4(const uint16_t* x, int T, int H, uint8_t* q, ui
 
 cudaError_t prepare_segments_kernel(int E) {
   const size_t b = segments_smem_bytes(E);
-  return cudaFuncSetAttribute(segments_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)(b > kSegmentsSmemMax ? b : kSegmentsSmemMax));
+  cudaError_t e = cudaFuncSetAttribute(segments_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(b > kSegmentsSmemMax ? b : kSegmentsSmemMax));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(segments_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)segments_count_smem(E, 4));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(segments_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)segments_place_smem(E));
+  return e;
 }
 
 cudaError_t launch_combine(const Workspace& ws, int T, int H, int k, int n_shared, const float* w,

@@ -355,4 +355,136 @@ __device__ __forceinline__ void segments_tiny(const int32_t* sid, int T, int k, 
   }
 }
 
+// ---- Large batches: the same stable counting sort over G CTAs in two
+// launches.  Slot ranges are contiguous per CTA and, inside a CTA, per warp,
+// in slot order, so positions come out exactly as from segments_cta.
+
+// Per-warp counts of this CTA's slots [c0, c1) into wcnt[32][E] (shared,
+// zeroed by the caller); invalid ids are reported (when report) and skipped.
+__device__ __forceinline__ void count_warp_slots(const int32_t* __restrict__ idx, int c0, int c1, int E,
+                                                 int32_t* wcnt, const Workspace& ws, bool report) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = (c1 - c0 + 31) / 32;
+  const int lo = min(c1, c0 + warp * per), hi = min(c1, lo + per);
+  for (int b0 = lo; b0 < hi; b0 += 32) {
+    const int s = b0 + lane;
+    int e = s < hi ? idx[s] : -1;
+    if (s < hi && (e < 0 || e >= E)) {
+      if (report) raise_error(ws.err, kErrExpertRange);
+      e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+  }
+}
+
+// Launch 1 of 2 (grid G, 1024 threads, 32 * E + 4 * E + 2 * ns + 2 ints of shared
+// memory): per-CTA counts into ws.seg_cbase[cta][E]; the last CTA to finish
+// turns them into absolute per-CTA bases, runs scan_experts and writes the
+// active list, tile table and shared positions.  Also zeroes the GEMM counters.
+__device__ __forceinline__ void segments_count_cta(const int32_t* __restrict__ idx, int T, int k, int E, int ns,
+                                                   int bn, const Workspace& ws, int32_t* sm) {
+  const int NE = E + ns, S = T * k, G = gridDim.x, cta = blockIdx.x;
+  int32_t* wcnt = sm;              // [32][E]
+  int32_t* stot = sm + 32 * E;     // [E]
+  int32_t* off_s = stot + E;       // [E]
+  int32_t* act_s = off_s + E;      // [NE]
+  int32_t* tp_s = act_s + NE;      // [NE+1]
+  __shared__ int n_act_s, routed_total_s, last;
+  for (int i = cta * blockDim.x + threadIdx.x; i < ws.split_cnt_n; i += G * blockDim.x) ws.split_cnt[i] = 0;
+  for (int i = cta * blockDim.x + threadIdx.x; i < ws.comb_cnt_n; i += G * blockDim.x) ws.comb_cnt[i] = 0;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int per = (S + G - 1) / G;
+  const int c0 = min(S, cta * per), c1 = min(S, c0 + per);
+  count_warp_slots(idx, c0, c1, E, wcnt, ws, true);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < 32; ++w) c += wcnt[w * E + e];
+    ws.seg_cbase[cta * E + e] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    last = atomic_add_acq_rel(ws.seg_counter, 1) == G - 1;
+    if (last) *ws.seg_counter = 0;
+  }
+  __syncthreads();
+  if (!last) return;
+  // the finisher: per expert, the running count over CTAs in order
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < G; ++c) {
+      const int n = __ldcg(ws.seg_cbase + c * E + e);
+      ws.seg_cbase[c * E + e] = run;
+      run += n;
+    }
+    stot[e] = run;
+  }
+  __syncthreads();
+  scan_experts(stot, E, T, S, ns, bn, ws, off_s, act_s, tp_s, &n_act_s, &routed_total_s);
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    for (int c = 0; c < G; ++c) ws.seg_cbase[c * E + e] += off_s[e];
+  const int na = n_act_s;
+  for (int a = threadIdx.x; a <= na; a += blockDim.x) {
+    ws.tile_prefix[a] = tp_s[a];
+    if (a < na) ws.active[a] = act_s[a];
+  }
+  if (bn > 0) {
+    for (int a = threadIdx.x; a < na; a += blockDim.x) {
+      const int x = act_s[a];
+      const int c = x < E ? stot[x] : T, p0 = x < E ? off_s[x] : S + (x - E) * T, t0 = tp_s[a];
+      for (int j = 0; j * bn < c; ++j) ws.tile_info[t0 + j] = make_int4(x, p0 + j * bn, min(bn, c - j * bn), 0);
+    }
+  }
+  if (threadIdx.x == 0) *ws.seg_routed = routed_total_s;
+}
+
+// Launch 2 of 2 (same grid, 32 * E ints of shared memory): per-warp counts
+// again, per-warp bases from this CTA's base, then every slot's position.
+__device__ __forceinline__ void segments_place_cta(const int32_t* __restrict__ idx, int T, int k, int E, int ns,
+                                                   const Workspace& ws, int32_t* sm) {
+  const int S = T * k, G = gridDim.x, cta = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int32_t* wcnt = sm;  // [32][E] counts, then bases
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int per = (S + G - 1) / G;
+  const int c0 = min(S, cta * per), c1 = min(S, c0 + per);
+  count_warp_slots(idx, c0, c1, E, wcnt, ws, false);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = __ldcg(ws.seg_cbase + cta * E + e);
+    for (int w = 0; w < 32; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const int wper = (c1 - c0 + 31) / 32;
+  const int lo = min(c1, c0 + warp * wper), hi = min(c1, lo + wper);
+  for (int b0 = lo; b0 < hi; b0 += 32) {
+    const int s = b0 + lane;
+    int e = s < hi ? idx[s] : -1;
+    if (s >= hi || e < 0 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (e >= 0) {
+      const int p = wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
+      ws.slot_pos[s] = p;
+      ws.perm[p] = s;
+      ws.pos_tok[p] = s / k;
+    } else if (s < hi) {
+      ws.slot_pos[s] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  // shared positions, and positions left free by invalid ids (a real token)
+  for (int i = cta * blockDim.x + threadIdx.x; i < ns * T; i += G * blockDim.x) ws.pos_tok[S + i] = i % T;
+  const int rt = __ldcg(ws.seg_routed);
+  for (int p = rt + cta * blockDim.x + threadIdx.x; p < S; p += G * blockDim.x) ws.pos_tok[p] = 0;
+}
+
 }  // namespace moe
