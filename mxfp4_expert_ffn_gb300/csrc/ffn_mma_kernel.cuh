@@ -99,12 +99,13 @@ struct Cfg {
   static constexpr int kATile = 128 * 128 * CH;           // one matrix, one stage
   static constexpr int kBTile = BN * 128 * CH;
   // MMA issue is split over two threads (see the kernel): gate/up one matrix
-  // each; down the token columns [0, kN0) and [kN0, BN) (BN >= 64; kN0 a
-  // multiple of 32 so each half's scale groups start a column group, both
-  // halves multiples of 16) or one half of each stage's K steps, into a second
-  // accumulator (BN = 16).
-  static constexpr bool kSplitN = MODE == kModeDown && BN >= 64;
-  static constexpr bool kSplitK = MODE == kModeDown && BN < 64;
+  // each; down at 64-token tiles the token columns [0, kN0) and [kN0, BN)
+  // (kN0 a multiple of 32 so each half's scale groups start a column group,
+  // both halves multiples of 16), and at 16- and 112-token tiles one half of
+  // each stage's K steps each, into a second accumulator (at 112 tokens this
+  // reads the weight tile once per K step instead of once per column half).
+  static constexpr bool kSplitN = MODE == kModeDown && BN == 64;
+  static constexpr bool kSplitK = MODE == kModeDown && (BN < 64 || BN == 112);
   static constexpr int kN0 = (BN / 2 + 31) / 32 * 32;
   // MMA width per tile from its token count (the 112-token tiles; narrower
   // tiles are mostly full or one instruction step wide)
