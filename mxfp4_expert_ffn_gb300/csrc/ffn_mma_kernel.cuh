@@ -99,14 +99,10 @@ struct Cfg {
   static constexpr int kATile = 128 * 128 * CH;           // one matrix, one stage
   static constexpr int kBTile = BN * 128 * CH;
   // MMA issue is split over two threads (see the kernel): gate/up one matrix
-  // each; down at 64-token tiles the token columns [0, kN0) and [kN0, BN)
-  // (kN0 a multiple of 32 so each half's scale groups start a column group,
-  // both halves multiples of 16), and at 16- and 112-token tiles one half of
-  // each stage's K steps each, into a second accumulator (at 112 tokens this
-  // reads the weight tile once per K step instead of once per column half).
-  static constexpr bool kSplitN = MODE == kModeDown && BN == 64;
-  static constexpr bool kSplitK = MODE == kModeDown && (BN < 64 || BN == 112);
-  static constexpr int kN0 = (BN / 2 + 31) / 32 * 32;
+  // each; down one half of each stage's K steps each, into a second
+  // accumulator that the epilogue adds in a fixed order (so every K step reads
+  // the weight tile once).
+  static constexpr bool kSplitK = MODE == kModeDown;
   // MMA width per tile from its token count (the 112-token tiles; narrower
   // tiles are mostly full or one instruction step wide)
   static constexpr bool kRagged = BN == 112;
@@ -119,12 +115,12 @@ struct Cfg {
   // then per chunk the token scales (group of 32 tokens g at column g); with
   // the column split each half starts a 4-column group of its own (the MMA
   // is handed a 4-column-aligned scale address).
-  static constexpr int kBCols = kSplitN ? 8 : 4;
+  static constexpr int kBCols = 4;  // token scale groups of 32 (BN <= 128)
   static constexpr int kSfCols = (kNA * 4 * CH + kBCols * CH) * kW;
   // A scales of (matrix m, chunk c, word w); B scales of (chunk c, word w, token group g)
   __host__ __device__ static constexpr int sfa_col(int m, int c, int w) { return ((m * CH + c) * kW + w) * 4; }
   __host__ __device__ static constexpr int sfb_col(int c, int w, int g) {
-    return kNA * 4 * CH * kW + (c * kW + w) * kBCols + (kSplitN ? (g < kN0 / 32 ? g : 4 + g - kN0 / 32) : g);
+    return kNA * 4 * CH * kW + (c * kW + w) * kBCols + g;
   }
   // ring depth: what the shared memory holds, and what TMEM holds next to the accumulators
   static constexpr int kStageCapT = (512 - kNAcc * kAccCols) / kSfCols;
@@ -455,9 +451,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // MMAs, so the empty and accumulator-full barriers count two arrivals.
     if (lane == 0) {
       const int j = warp == 1 ? 0 : 1;
-      // N of this thread's MMAs and the first of its token columns
-      const int NI0 = C::kSplitN ? (j == 0 ? C::kN0 : BN - C::kN0) : BN;
-      const int n0 = C::kSplitN ? j * C::kN0 : 0;
+      const int NI0 = BN;  // N of the MMAs (the tile's tokens for the ragged wide tiles)
       uint32_t g = 0, it = 0;
       Sched sc = sc0;
       for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
@@ -476,10 +470,10 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             // rounded up to the instruction's step of 16, so the MMAs cost
             // only the columns in use (the epilogue reads no column past them)
             const int nr = min(BN, (un.m_tile + 15) & ~15);
-            NI = C::kSplitN ? (j == 0 ? min(C::kN0, nr) : nr - C::kN0) : nr;
+            NI = nr;
           }
         }
-        uint32_t idesc_base = A4 ? idesc_e2m1_e2m1(128, NI > 0 ? NI : 16, 0) : idesc_e2m1_e4m3(128, NI > 0 ? NI : 16, 0);
+        uint32_t idesc_base = A4 ? idesc_e2m1_e2m1(128, NI, 0) : idesc_e2m1_e4m3(128, NI, 0);
         if (pc.u / mt_units >= shared_tile0) idesc_base &= ~(7u << 7);  // A = E4M3 (FP8 shared expert)
         bool ok = true;
         const int s_beg = pc.s0, s_end = pc.s1;
@@ -500,7 +494,6 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           for (int c = 0; c < CH; ++c)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              if (C::kRagged && NI <= 0) break;  // the second column half of a narrow tile is empty
               // 32 bytes of each operand row per instruction (K = 32 E4M3 / K = 64
               // packed E2M1); scale byte k of the chunk's word (A4: word k / 2,
               // bytes 2 (k % 2) and up)
@@ -519,10 +512,6 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
                 const int m = j, acc = swap ? 1 - m : m;  // gate -> accumulator 0, up -> 1
                 mma(d_tmem + acc * BN, a_desc0 + (uint64_t)((m * C::kATile + c * 16384 + 32 * k) >> 4), bdesc,
                     sf + C::sfa_col(acc, c, w), sfb, (s != s_beg || c || k) ? 1u : 0u);
-              } else if constexpr (C::kSplitN) {
-                // token columns [n0, n0 + NI): B rows and their scale groups
-                mma(d_tmem + n0, a_desc0 + (uint64_t)((c * 16384 + 32 * k) >> 4), bdesc + (uint64_t)((n0 * 128) >> 4),
-                    sf + C::sfa_col(0, c, w), sf + C::sfb_col(c, w, n0 / 32), (s != s_beg || c || k) ? 1u : 0u);
               } else {
                 // K steps i = 4c + k of the stage: the first half to accumulator 0
                 const int i = c * 4 + k, first = j * CH * 2;

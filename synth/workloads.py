@@ -43,6 +43,8 @@ DECODE_T1 = Workload("v41_layer_decode_t1", tokens=1, seed=1, **_V41)
 VERIFY_T5 = Workload("v41_layer_verify_t5_zipf", tokens=5, seed=2, zipf=1.1, **_V41)
 VERIFY_T32 = Workload("v41_layer_verify_t32_zipf", tokens=32, seed=3, zipf=1.1, **_V41)
 PREFILL_T4096 = Workload("v41_layer_prefill_t4096", tokens=4096, seed=4, **_V41)
+# a mid-size batch (64-token tiles, ~4 slots per expert): between decode and prefill
+MID_T256 = Workload("v41_layer_t256", tokens=256, seed=11, **_V41)
 # prefill sweep: tensor-pipe use as the tokens per expert grow (~64 at 4096)
 PREFILL_T16K = Workload("v41_layer_prefill_t16384", tokens=16384, seed=8, **_V41)
 PREFILL_T32K = Workload("v41_layer_prefill_t32768", tokens=32768, seed=9, **_V41)
@@ -55,6 +57,6 @@ STACK8_T64 = Workload("v41_stack8_decode_t64_zipf", tokens=64, seed=5, layers=8,
 NCU_DECODE_T1 = Workload("ncu_v41_e24_decode_t1", tokens=1, seed=6, **{**_V41, "n_experts": 24})
 NCU_PREFILL = Workload("ncu_v41_e24_prefill_t512", tokens=512, seed=7, **{**_V41, "n_experts": 24})
 
-WORKLOADS = {w.name: w for w in (TINY, DECODE_T1, VERIFY_T5, VERIFY_T32, PREFILL_T4096, PREFILL_T16K,
+WORKLOADS = {w.name: w for w in (TINY, DECODE_T1, VERIFY_T5, VERIFY_T32, MID_T256, PREFILL_T4096, PREFILL_T16K,
                                  PREFILL_T32K, PREFILL_T64K, STACK8_T64,
                                  NCU_DECODE_T1, NCU_PREFILL)}
