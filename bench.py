@@ -152,9 +152,9 @@ def layer_bytes(wl, n_experts_touched: int, T: int, shared_fp8: bool = False) ->
 # summarised in profiles/ffn_mma_decode_e24_t1_full.md; valid only for the kernel source it was
 # taken on and for a decode token (7 experts streamed per launch, as in that capture).
 _TRAFFIC_SRC = ("mxfp4_expert_ffn_gb300/csrc/ffn_mma_kernel.cuh", "mxfp4_expert_ffn_gb300/csrc/ffn_mma.cu")
-_TRAFFIC_SHA256 = "f185e6426d2a2b32175b5cc18d6d184ffbeefa361b27dcbf448eadbe1502d222"
-_TRAFFIC = {("v41_layer_decode_t1", "ffn_up_mma"): (88.526336 + 2.677248) * 1e6,
-            ("v41_layer_decode_t1", "ffn_down_mma"): (43.978752 + 0.041728) * 1e6}
+_TRAFFIC_SHA256 = "0c2a6c75173d05510332e178430977f7627548ffa4da6d2c291297c6411533ba"
+_TRAFFIC = {("v41_layer_decode_t1", "ffn_up_mma"): (88.507648 + 2.629888) * 1e6,
+            ("v41_layer_decode_t1", "ffn_down_mma"): (43.986176 + 0.043520) * 1e6}
 
 
 def measured_traffic(workload: str, kernel: str):
