@@ -75,6 +75,8 @@ size_t carve(const moe_config& c, int num_sms, char* base, Workspace& ws) {
   ws.idx = cv.take<int32_t>(T * k);
   ws.w = cv.take<float>(T * k);
   ws.x = cv.take<uint16_t>(T * H);
+  // the error word right before y (256 bytes apart): one copy brings back both
+  ws.err = cv.take<int32_t>(1);
   ws.y = cv.take<uint16_t>(T * H);
   // split partition of the tensor-core GEMM (few units, e.g. decode): two
   // partial slots per CTA and one counter per (unit, row quadrant), units < 4 * SMs
@@ -88,7 +90,6 @@ size_t carve(const moe_config& c, int num_sms, char* base, Workspace& ws) {
   ws.seg_cbase = cv.take<int32_t>((size_t)kSegCtas * E);
   ws.seg_counter = cv.take<int32_t>(1);
   ws.seg_routed = cv.take<int32_t>(1);
-  ws.err = cv.take<int32_t>(1);
   return cv.off;
 }
 
@@ -239,7 +240,13 @@ moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int dev
   L->ws.base = base;
   L->ws.bytes = bytes;
   cudaError_t e = cudaMemset(base, 0, bytes);
-  if (e == cudaSuccess) e = cudaMallocHost(&L->ws.err_host, sizeof(int32_t));
+  // pinned staging of the host entry point: the error word, then y of batches
+  // of up to 16 KB (one device-to-host copy for both; larger ones are copied
+  // straight to the caller, a second host copy would cost more than it saves)
+  L->out_rows = (int)(16384 / ((size_t)cfg->hidden * sizeof(uint16_t)));
+  if (L->out_rows > cfg->max_tokens) L->out_rows = cfg->max_tokens;
+  if (e == cudaSuccess)
+    e = cudaMallocHost(&L->ws.err_host, 256 + (size_t)L->out_rows * cfg->hidden * sizeof(uint16_t));
   if (e == cudaSuccess) e = prepare_segments_kernel(cfg->n_experts);
   if (e == cudaSuccess) e = prepare_ffn_simt(cfg->hidden, cfg->inter);
   if (e == cudaSuccess) e = prepare_prep_kernel(cfg->n_experts, cfg->hidden);
@@ -602,9 +609,24 @@ moe_status moe_forward_host(moe_layer* L, const void* x_host, int32_t T, void* y
   cudaError_t e = cudaMemcpyAsync(L->ws.x, x_host, bytes, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e);
   if ((s = step_impl(L, L->ws.x, T, nullptr, L->ws.y, nullptr, nullptr, nullptr, st)) != MOE_OK) return s;
-  e = cudaMemcpyAsync(y_host, L->ws.y, bytes, cudaMemcpyDeviceToHost, st);
+  if (T > L->out_rows || reinterpret_cast<char*>(L->ws.err) + 256 != reinterpret_cast<char*>(L->ws.y)) {
+    e = cudaMemcpyAsync(y_host, L->ws.y, bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return moe_sync(L, stream);
+  }
+  // small batches: the error word and y in one copy through the pinned staging
+  e = cudaMemcpyAsync(L->ws.err_host, L->ws.err, 256 + bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e);
-  return moe_sync(L, stream);
+  memcpy(y_host, reinterpret_cast<const char*>(L->ws.err_host) + 256, bytes);
+  const int32_t bits = *L->ws.err_host;
+  if (bits) {
+    e = cudaMemsetAsync(L->ws.err, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return (bits & kErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_INTERNAL;
+  }
+  return MOE_OK;
 }
 
 moe_status moe_quantize_act(moe_layer* L, const void* x, int32_t T, uint8_t* q, uint8_t* s,

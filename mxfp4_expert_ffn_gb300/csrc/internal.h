@@ -63,7 +63,7 @@ struct Workspace {
   int32_t* seg_counter = nullptr; // [1]    its last-arriver counter (zero between launches)
   int32_t* seg_routed = nullptr;  // [1]    its routed slot total
   int32_t* err = nullptr;     // [1]        device error word
-  int32_t* err_host = nullptr;// pinned copy of err
+  int32_t* err_host = nullptr;// pinned: the error word, then (host entry point) y of small batches
   void* base = nullptr;       // single allocation holding all of the above
   size_t bytes = 0;
 };
@@ -89,6 +89,7 @@ struct moe_layer {
   int scoring = 0;            // MOE_SCORING_SOFTMAX / MOE_SCORING_SIGMOID
   float routed_scale = 1.0f;  // routed weights are multiplied by it
   int act_format = 0;         // MOE_ACT_FP8 / MOE_ACT_FP4
+  int out_rows = 0;           // y rows the pinned staging (ws.err_host) holds after the error word
   int shared_format = 0;      // MOE_SHARED_MXFP4 / MOE_SHARED_FP8_B32
   bool timing = false;
   moe::Workspace ws;
