@@ -264,8 +264,10 @@ def test_fault_injection_launch_and_arg(monkeypatch):
     L.close()
 
 
-def test_forward_host_matches_device_path():
-    wl = SMALL[2]
+@pytest.mark.parametrize("wl", [SMALL[2], SMALL[1]], ids=lambda w: w.name)
+def test_forward_host_matches_device_path(wl):
+    # 13 tokens of 1 KB come back with the error word in one copy; 37 of 768 B
+    # exceed the 16 KB staging and are copied straight to the caller
     L, _ = gu.make_layer(wl)
     x = _x(wl)
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
