@@ -149,12 +149,12 @@ def layer_bytes(wl, n_experts_touched: int, T: int, shared_fp8: bool = False) ->
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu capture
-# summarised in profiles/ffn_mma_decode_e24_t1_full.md; valid only for the kernel source it was
+# summarised in profiles/ffn_mma_decode_e24_t1_traffic.md; valid only for the kernel source it was
 # taken on and for a decode token (7 experts streamed per launch, as in that capture).
 _TRAFFIC_SRC = ("mxfp4_expert_ffn_gb300/csrc/ffn_mma_kernel.cuh", "mxfp4_expert_ffn_gb300/csrc/ffn_mma.cu")
-_TRAFFIC_SHA256 = "0c2a6c75173d05510332e178430977f7627548ffa4da6d2c291297c6411533ba"
-_TRAFFIC = {("v41_layer_decode_t1", "ffn_up_mma"): (88.507648 + 2.629888) * 1e6,
-            ("v41_layer_decode_t1", "ffn_down_mma"): (43.986176 + 0.043520) * 1e6}
+_TRAFFIC_SHA256 = "abe7e20a8af16235b6cf84d9ce033c7459845c53fa261802b765210bb854bdfd"
+_TRAFFIC = {("v41_layer_decode_t1", "ffn_up_mma"): (88.527616 + 1.949696) * 1e6,
+            ("v41_layer_decode_t1", "ffn_down_mma"): (43.987712 + 0.002048) * 1e6}
 
 
 def measured_traffic(workload: str, kernel: str):

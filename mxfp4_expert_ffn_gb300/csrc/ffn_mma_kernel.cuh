@@ -579,6 +579,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
                              : make_uint4(0u, 0u, 0u, 0u);
         }
       };
+      // the weight scales first: their addresses do not wait for the token
+      // positions that the activation rows need
       auto load = [&](uint32_t (&w)[NB][NW], int s0) {
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
@@ -591,6 +593,17 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
 #pragma unroll
                 for (int m = 0; m < NA; ++m)
                   w[i][(m * CH + c) * KW + v] = __ldg(reinterpret_cast<const uint32_t*>(sa_row[m] + kb));
+              }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          if (s0 + i < s_end) {
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+#pragma unroll
+              for (int v = 0; v < KW; ++v) {
+                const int kb = 4 * (KW * ((s0 + i) * CH + c) + v);
 #pragma unroll
                 for (int cb = 0; cb < NC; ++cb)
                   w[i][(NA * CH + c * NC + cb) * KW + v] =

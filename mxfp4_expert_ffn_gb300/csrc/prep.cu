@@ -59,11 +59,15 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
   const bool tiny = p.T * p.k <= 32 && p.T <= p.bn && gridDim.y == 1;
 
   // ---- 1a. router partial sums: warp = expert, CTA = (expert group, token block, K chunk);
-  // the CTA's x chunk (8 tokens x H/ks) is staged in shared memory once
+  // the warp's first batch of W_r loads is in flight while the CTA's x chunk
+  // (8 tokens x H/ks) is staged in shared memory
   if (p.route) {
     const int e = blockIdx.x * kPrepWarps + warp;
     const int t0 = blockIdx.y * kPrepTT, nt = min(kPrepTT, p.T - t0);
     const int kc = p.H / p.ks, k0 = blockIdx.z * kc;
+    const float* wrow = p.W + (size_t)(e < p.E ? e : 0) * p.H + k0;
+    float4 wv[kRouterBatch];
+    if (e < p.E) router_load_batch(reinterpret_cast<const float4*>(wrow), kc / 4, lane, wv);
     uint32_t* xsm = reinterpret_cast<uint32_t*>(sm);  // [nt][kc / 2] bf16 pairs
     for (int i = threadIdx.x; i < nt * (kc / 8); i += blockDim.x) {
       const int t = i / (kc / 8), c = i - t * (kc / 8);
@@ -74,8 +78,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
       float acc[kPrepTT];
 #pragma unroll
       for (int i = 0; i < kPrepTT; ++i) acc[i] = 0.f;
-      router_dot<kPrepTT>(p.W + (size_t)e * p.H + k0, kc, nt, lane,
-                          [&](int i, int h) { return xsm[i * (kc / 2) + h / 2]; }, acc);
+      auto xf = [&](int i, int h) { return xsm[i * (kc / 2) + h / 2]; };
+      router_fma_batch<kPrepTT>(wv, kc / 4, lane, nt, xf, acc);
+      router_dot_rest<kPrepTT>(wrow, kc, nt, lane, xf, acc);
 #pragma unroll
       for (int i = 0; i < kPrepTT; ++i) {
         const float s = warp_sum(acc[i]);
@@ -114,25 +119,32 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
   __syncthreads();
   if (!last) return;
   if (p.route) {
-    float* lg = reinterpret_cast<float*>(sm);  // [nt][E]
+    // every thread: logits, then their selection codes and scores (so the
+    // selecting warp only compares)
     const int t0 = blockIdx.y * kPrepTT, nt = min(kPrepTT, p.T - t0);
+    uint32_t* okey = reinterpret_cast<uint32_t*>(sm);             // [nt][E]
+    float* osc = reinterpret_cast<float*>(sm) + kPrepTT * p.E;    // [nt][E]
     for (int i = threadIdx.x; i < nt * p.E; i += blockDim.x) {
       const int t = i / p.E, e = i - t * p.E;
       // the bias is part of the logit for softmax scoring, of the selection key for sigmoid
       const float f = router_sum_partials(p.part, p.ks, p.T, p.E, t0 + t, e, p.sg.sigmoid ? nullptr : p.b);
-      lg[i] = f;
       if (p.logits_out) p.logits_out[(size_t)(t0 + t) * p.E + e] = f;
+      float kv, sv;
+      topk_key_one(f, e, p.sg, kv, sv);
+      okey[i] = order_key(kv);
+      osc[i] = sv;
     }
     __syncthreads();
     if (warp < nt) {
-      float l[16], key[16], sc[16];
+      uint32_t ok[16];
+      float sc[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int e = lane + 32 * i;
-        l[i] = e < p.E ? lg[warp * p.E + e] : -INFINITY;
+        ok[i] = e < p.E ? okey[warp * p.E + e] : 0u;
+        sc[i] = e < p.E ? osc[warp * p.E + e] : 0.f;
       }
-      topk_keys(l, p.E, lane, p.sg, key, sc);
-      const int pick = select_topk(key, sc, t0 + warp, p.E, p.k, lane, p.sg, p.idx, p.w);
+      const int pick = select_topk_codes(ok, sc, t0 + warp, p.k, lane, p.sg, p.idx, p.w);
       if (tiny && lane < p.k) sid_s[(t0 + warp) * p.k + lane] = pick;
     }
   } else if (tiny && (int)threadIdx.x < p.T * p.k) {
@@ -158,7 +170,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
 }
 
 size_t prep_smem_bytes(int E, int H) {
-  const size_t seg = (size_t)(36 * E + 2 * 4 + 1) * sizeof(int32_t), lg = (size_t)kPrepTT * E * sizeof(float);
+  const size_t seg = (size_t)(36 * E + 2 * 4 + 1) * sizeof(int32_t), lg = (size_t)2 * kPrepTT * E * sizeof(float);
   const size_t xs = (size_t)kPrepTT * H * sizeof(uint16_t);  // bound for one K chunk of x
   const size_t small = (size_t)(4 * E + 2 * 4 + 1024 + 1) * sizeof(int32_t);  // segments_small_cta
   size_t m = seg > lg ? seg : lg;

@@ -42,35 +42,59 @@ __device__ __forceinline__ float sigmoid_f32(float l) {
 // acc[i] += sum over h in [k0, k0 + kc) of W[h] * x_i[h] for one W_r row (fp32)
 // and nt <= TT bf16 tokens; lane l takes the float4 groups l, l + 32, ... in
 // increasing order (so the sum order is fixed), and the row's float4 loads of a
-// lane are issued in batches of 8 before they are used.  x(i, h) returns the
-// two bf16 of token i at elements h, h+1 packed in a uint32 (low = h).
+// lane are issued in batches of kRouterBatch before they are used.  x(i, h)
+// returns the two bf16 of token i at elements h, h+1 packed in a uint32 (low = h).
+constexpr int kRouterBatch = 8;
+
+// The batch of float4 groups b, b + 32, ... of a row (zeros past kc4 groups).
+__device__ __forceinline__ void router_load_batch(const float4* __restrict__ wr, int kc4, int b,
+                                                  float4 (&wv)[kRouterBatch]) {
+#pragma unroll
+  for (int u = 0; u < kRouterBatch; ++u)
+    wv[u] = b + 32 * u < kc4 ? __ldg(wr + b + 32 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 template <int TT, typename XFn>
-__device__ __forceinline__ void router_dot(const float* __restrict__ wrow, int kc, int nt, int lane,
-                                           XFn x, float (&acc)[TT]) {
-  constexpr int U = 8;
-  const float4* wr = reinterpret_cast<const float4*>(wrow);
-  const int kc4 = kc / 4;
-  for (int b = lane; b < kc4; b += 32 * U) {
-    float4 wv[U];
+__device__ __forceinline__ void router_fma_batch(const float4 (&wv)[kRouterBatch], int kc4, int b, int nt, XFn x,
+                                                 float (&acc)[TT]) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) wv[u] = b + 32 * u < kc4 ? __ldg(wr + b + 32 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int u = 0; u < kRouterBatch; ++u) {
+    const int h4 = b + 32 * u;
+    if (h4 < kc4) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int h4 = b + 32 * u;
-      if (h4 < kc4) {
-#pragma unroll
-        for (int i = 0; i < TT; ++i) {
-          if (i < nt) {
-            const uint32_t x01 = x(i, 4 * h4), x23 = x(i, 4 * h4 + 2);
-            acc[i] = fmaf(wv[u].x, __uint_as_float(x01 << 16), acc[i]);
-            acc[i] = fmaf(wv[u].y, __uint_as_float(x01 & 0xFFFF0000u), acc[i]);
-            acc[i] = fmaf(wv[u].z, __uint_as_float(x23 << 16), acc[i]);
-            acc[i] = fmaf(wv[u].w, __uint_as_float(x23 & 0xFFFF0000u), acc[i]);
-          }
+      for (int i = 0; i < TT; ++i) {
+        if (i < nt) {
+          const uint32_t x01 = x(i, 4 * h4), x23 = x(i, 4 * h4 + 2);
+          acc[i] = fmaf(wv[u].x, __uint_as_float(x01 << 16), acc[i]);
+          acc[i] = fmaf(wv[u].y, __uint_as_float(x01 & 0xFFFF0000u), acc[i]);
+          acc[i] = fmaf(wv[u].z, __uint_as_float(x23 << 16), acc[i]);
+          acc[i] = fmaf(wv[u].w, __uint_as_float(x23 & 0xFFFF0000u), acc[i]);
         }
       }
     }
   }
+}
+
+// The batches after the first one (already loaded into wv and added by the caller).
+template <int TT, typename XFn>
+__device__ __forceinline__ void router_dot_rest(const float* __restrict__ wrow, int kc, int nt, int lane, XFn x,
+                                                float (&acc)[TT]) {
+  const float4* wr = reinterpret_cast<const float4*>(wrow);
+  const int kc4 = kc / 4;
+  for (int b = lane + 32 * kRouterBatch; b < kc4; b += 32 * kRouterBatch) {
+    float4 wv[kRouterBatch];
+    router_load_batch(wr, kc4, b, wv);
+    router_fma_batch<TT>(wv, kc4, b, nt, x, acc);
+  }
+}
+
+template <int TT, typename XFn>
+__device__ __forceinline__ void router_dot(const float* __restrict__ wrow, int kc, int nt, int lane,
+                                           XFn x, float (&acc)[TT]) {
+  float4 wv[kRouterBatch];
+  router_load_batch(reinterpret_cast<const float4*>(wrow), kc / 4, lane, wv);
+  router_fma_batch<TT>(wv, kc / 4, lane, nt, x, acc);
+  router_dot_rest<TT>(wrow, kc, nt, lane, x, acc);
 }
 
 // The logit of (token t, expert e) from ks <= 8 K-chunk partials
@@ -99,43 +123,48 @@ __device__ __forceinline__ float order_key_value(uint32_t u) {
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
+// Selection key and score of one logit l of expert e < E: softmax keys are l
+// (NaN as -infinity); sigmoid keys are sigmoid(l) + bias (NaN as -infinity),
+// scores sigmoid(l).
+__device__ __forceinline__ void topk_key_one(float l, int e, const Scoring& sg, float& kv, float& sv) {
+  kv = -INFINITY;
+  sv = 0.f;
+  if (!isnan(l)) {  // a NaN logit: key -infinity, score 0
+    if (sg.sigmoid) {
+      sv = sigmoid_f32(l);
+      kv = __fadd_rn(sv, sg.sel_bias ? sg.sel_bias[e] : 0.f);
+      if (isnan(kv)) kv = -INFINITY;
+    } else {
+      kv = sv = l;
+    }
+  }
+}
+
 // Per-lane selection keys and scores from the logits l[e] of one token held by
-// lane e % 32 (e = lane + 32 i): softmax keys are l (NaN as -infinity);
-// sigmoid keys are sigmoid(l) + bias (NaN as -infinity), scores sigmoid(l).
+// lane e % 32 (e = lane + 32 i); experts past E get key -infinity, score 0.
 __device__ __forceinline__ void topk_keys(const float (&l)[16], int E, int lane, const Scoring& sg,
                                           float (&key)[16], float (&sc)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int e = lane + 32 * i;
-    float kv = -INFINITY, sv = 0.f;
-    if (e < E && !isnan(l[i])) {  // a NaN logit: key -infinity, score 0
-      if (sg.sigmoid) {
-        sv = sigmoid_f32(l[i]);
-        kv = __fadd_rn(sv, sg.sel_bias ? sg.sel_bias[e] : 0.f);
-        if (isnan(kv)) kv = -INFINITY;
-      } else {
-        kv = sv = l[i];
-      }
-    }
-    key[i] = kv;
-    sc[i] = sv;
+    key[i] = -INFINITY;
+    sc[i] = 0.f;
+    if (e < E) topk_key_one(l[i], e, sg, key[i], sc[i]);
   }
 }
 
 // k rounds of a warp arg-max over (key desc, index asc) on the 16 keys per
-// lane (key[i] is expert lane + 32 i): the largest key by an integer warp
-// reduction of the order-preserving codes, then the lowest index holding it
-// by a second one.  Lane r < k ends with the r-th pick and writes idx[t][r]
-// and its weight: softmax w_r = exp(v_r - v_0) / sum_r' exp(v_r' - v_0) with
-// v the logits; sigmoid w_r = s_r / sum_r' s_r' with s the sigmoid scores;
-// both sums in rank order; then times the routed scale.  Returns the lane's
-// pick (-1 for lanes >= k).
-__device__ __forceinline__ int select_topk(const float (&key)[16], const float (&sc)[16], int t, int E, int k,
-                                           int lane, const Scoring& sg, int32_t* __restrict__ idx,
-                                           float* __restrict__ w) {
-  uint32_t ok[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) ok[i] = lane + 32 * i < E ? order_key(key[i]) : 0u;
+// lane (key[i] is expert lane + 32 i), given as order-preserving codes ok[i]
+// (order_key of the key; 0 for experts past E): the largest key by an integer
+// warp reduction of the codes, then the lowest index holding it by a second
+// one.  Lane r < k ends with the r-th pick and writes idx[t][r] and its
+// weight: softmax w_r = exp(v_r - v_0) / sum_r' exp(v_r' - v_0) with v the
+// logits; sigmoid w_r = s_r / sum_r' s_r' with s the sigmoid scores; both sums
+// in rank order; then times the routed scale.  Returns the lane's pick (-1 for
+// lanes >= k).
+__device__ __forceinline__ int select_topk_codes(uint32_t (&ok)[16], const float (&sc)[16], int t, int k,
+                                                 int lane, const Scoring& sg, int32_t* __restrict__ idx,
+                                                 float* __restrict__ w) {
   int my_i = -1;
   float my_v = 0.f, my_s = 0.f;
   for (int r = 0; r < k; ++r) {
@@ -180,6 +209,15 @@ __device__ __forceinline__ int select_topk(const float (&key)[16], const float (
     w[(size_t)t * k + lane] = wr;
   }
   return my_i;
+}
+
+__device__ __forceinline__ int select_topk(const float (&key)[16], const float (&sc)[16], int t, int E, int k,
+                                           int lane, const Scoring& sg, int32_t* __restrict__ idx,
+                                           float* __restrict__ w) {
+  uint32_t ok[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ok[i] = lane + 32 * i < E ? order_key(key[i]) : 0u;
+  return select_topk_codes(ok, sc, t, k, lane, sg, idx, w);
 }
 
 }  // namespace moe
