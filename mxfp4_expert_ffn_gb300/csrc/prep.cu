@@ -90,9 +90,14 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
   }
 
   // ---- 1b. FP8 codes of x by token, 8 values per thread, spread over all CTAs
+  // (and, for the one-warp segments, the zeroing of the GEMMs' arrival counters)
   {
     const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
     const int stride = gridDim.x * gridDim.y * gridDim.z * blockDim.x;
+    if (tiny) {
+      for (int i = cta * blockDim.x + threadIdx.x; i < p.ws.split_cnt_n; i += stride) p.ws.split_cnt[i] = 0;
+      for (int i = cta * blockDim.x + threadIdx.x; i < p.ws.comb_cnt_n; i += stride) p.ws.comb_cnt[i] = 0;
+    }
     const int n8 = p.T * (p.H / 8);  // a multiple of 4: whole quads stay in or out
     const unsigned quad = 0xFu << (lane & ~3);
     const uint4* x8 = reinterpret_cast<const uint4*>(p.x);

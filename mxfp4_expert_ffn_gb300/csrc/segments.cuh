@@ -288,11 +288,11 @@ __device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ i
 // places the slots (one lane each) with match and ballot operations -- the
 // same stable counting sort as segments_cta, so the same outputs.
 // sid: the S slot ids in shared memory, visible to every calling thread.
+// The caller zeroes ws.split_cnt and ws.comb_cnt (the preparation kernel does
+// it in its parallel phase, off this serial path).
 __device__ __forceinline__ void segments_tiny(const int32_t* sid, int T, int k, int E, int ns,
                                               const Workspace& ws) {
   const int S = T * k, NE = E + ns, tid = threadIdx.x, lane = tid & 31;
-  for (int i = tid; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
-  for (int i = tid; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
   for (int e = tid; e < E; e += blockDim.x) {
     int c = 0, off = 0;
     for (int j = 0; j < S; ++j) {
