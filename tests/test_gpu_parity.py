@@ -266,16 +266,25 @@ def test_fault_injection_launch_and_arg(monkeypatch):
 
 @pytest.mark.parametrize("wl", [SMALL[2], SMALL[1]], ids=lambda w: w.name)
 def test_forward_host_matches_device_path(wl):
-    # 13 tokens of 1 KB come back with the error word in one copy; 37 of 768 B
-    # exceed the 16 KB staging and are copied straight to the caller
+    # 13 tokens of 1 KB come back with the error word in one copy through the
+    # pinned staging; 37 tokens of 768 B exceed the 16 KB staging and are
+    # copied straight to the caller.  Repeated calls, a changed token count and
+    # a changed option (the routing changes with it) must each match the
+    # device path.
     L, _ = gu.make_layer(wl)
-    x = _x(wl)
-    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    L.forward_host(xh, wl.tokens, yh)
-    idx, w, _ = gu.run_route(L, x, wl.tokens, wl.n_experts, wl.top_k)
-    yd = gu.run_forward(L, x, idx, w)
-    assert np.array_equal(yh.numpy().view(np.uint16), yd)
+    T0 = wl.tokens
+    calls = [T0, T0, T0, T0 - 4, T0 - 4, T0 - 4, T0, "sigmoid", T0, T0, T0]
+    for i, T in enumerate(calls):
+        if T == "sigmoid":
+            L.set_scoring(m.MOE_SCORING_SIGMOID, 2.5)
+            continue
+        x = _x(wl, T=T, stream=i)
+        xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        L.forward_host(xh, T, yh)
+        idx, w, _ = gu.run_route(L, x, T, wl.n_experts, wl.top_k)
+        yd = gu.run_forward(L, x, idx, w)
+        assert np.array_equal(yh.numpy().view(np.uint16), yd), (i, T)
     L.close()
 
 
