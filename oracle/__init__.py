@@ -19,12 +19,21 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 
+def compile_library(src: str, out: str) -> None:
+    """gcc -O2 (OpenMP, no floating-point contraction, no -march flags) of one C source."""
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp",
+                           "-o", out, src, "-lm"])
+
+
 def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so with gcc (OpenMP, no -march flags)."""
+    """Compile oracle.c into liboracle.so.  ORACLE_LIB names another build of
+    the same exports to load instead (the tests' planted-mistake variants)."""
+    other = os.environ.get("ORACLE_LIB")
+    if other:
+        return other
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp",
-                               "-o", tmp, _SRC, "-lm"])
+        compile_library(_SRC, tmp)
         os.replace(tmp, _LIB)
     return _LIB
 
