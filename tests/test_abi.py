@@ -52,6 +52,12 @@ def _weights(fake=0x1000):
     (256, 128, 16, 2, 5, 4),      # too many shared experts
     (256, 128, 16, 2, 1, 0),      # no tokens
     (32768, 128, 16, 2, 1, 4),    # hidden too large
+    (256, 32768, 16, 2, 1, 4),    # inter too large
+    (256, 128, 0, 1, 1, 4),       # no experts
+    (256, 128, 16, 0, 1, 4),      # k = 0
+    (256, 128, 16, 2, -1, 4),     # negative shared count
+    (256, 128, 16, 2, 1, 65537),  # more tokens than the workspace limit
+    (-256, 128, 16, 2, 1, 4),     # negative hidden
 ])
 def test_create_rejects_unsupported_shapes(cfg):
     h = C.c_void_p()
