@@ -12,6 +12,14 @@ import mxfp4_expert_ffn_gb300 as m
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    # the checks load the compiled library: build it (nvcc cross-compiles for
+    # sm_103a without a GPU) if this checkout has not, a no-op when up to date
+    from mxfp4_expert_ffn_gb300 import build as b
+    b.build()
+
+
 def _declared():
     src = open(os.path.join(ROOT, "include", "moe_ffn.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
