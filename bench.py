@@ -1,16 +1,21 @@
-"""Benchmark of one MXFP4 MoE layer step on GB300.
+"""Benchmark of MXFP4 MoE layer steps on GB300.
 
 A step is one pass of the whole hot path over one batch: router logits,
 top-k, segments, FP8 activation quantisation, gate/up + SwiGLU + h
-quantisation, down, combine.  The default workload is one
-DeepSeek-V4.1-shaped layer at decode batch 1 (hidden 5120, intermediate 2304,
-384 routed experts top-6 + 1 shared, all experts resident); other workloads
-are selectable with --workload for profiling.
+quantisation, down, combine -- for every layer of the workload.  The default
+workload is the largest one a single GPU holds: a stack of 8
+DeepSeek-V4.1-shaped MoE layers (hidden 5120, intermediate 2304, 384 routed
+experts top-6 + 1 shared each, ~58 GB resident) run back to back on 64
+concurrent decode tokens with Zipf(1.1)-skewed routing and a bf16 residual
+add between layers (each layer's input RMS-normalised).  The single-layer
+decode, verification and prefill workloads are selectable with --workload.
 
-Prints ONE JSON line (rank 0).  `value` is layer tokens/s with inputs
-resident in HBM; each step gets a fresh token and the L2 is flushed between
-steps (outside the timed events).  `e2e` is the same metric through
-moe_forward_host with pinned host buffers (copies inside the timed region).
+Prints ONE JSON line (rank 0).  `value` is tokens/s through the workload
+(all its layers) with inputs resident in HBM; each step gets fresh tokens and
+the L2 is flushed between steps (outside the timed events).  `e2e` is the
+same metric through the library's host-buffer entry point
+(moe_stack_forward_host for a stack, moe_forward_host for one layer) with
+pinned host buffers, the copies inside the timed region.
 `--impl reference` times the fp64 CPU oracle instead.
 """
 from __future__ import annotations
@@ -31,7 +36,7 @@ import numpy as np  # noqa: E402
 
 from synth.workloads import WORKLOADS  # noqa: E402
 
-DEFAULT = "v41_layer_decode_t1"
+DEFAULT = "v41_stack8_decode_t64_zipf"
 METRIC = "MoE-layer tokens/s; decode HBM GB/s vs peak; prefill FP4 TFLOPS vs peak"
 
 
@@ -175,35 +180,47 @@ def layer_flops(wl, T: int) -> int:
     return (T * wl.top_k + wl.n_shared * T) * 3 * 2 * wl.hidden * wl.inter
 
 
-def oracle_tokens_per_s(wl, n_tokens: int, threads: int, stream: int = 50):
-    """Times the fp64 oracle (routing + layer) on n_tokens seeded tokens.
-    Expert bytes are regenerated before the clock starts (input generation)."""
+# Block-scaled tcgen05.mma throughput of one SM at M = 128, N >= 128, in FLOP per
+# SM clock cycle, as measured by the issue-rate microbenchmark (mma_rate.cu,
+# `bench.py --mma-rates`; profiles/mma_issue_rates.md): 128 x 256 x K x 2 FLOP in
+# 128.2 cycles, K = 32 for kind::mxf8f6f4 (FP4 weights x FP8 activations) and
+# K = 64 for kind::mxf4 (FP4 x FP4).
+MMA_FLOP_PER_CYCLE_SM = {"mxf8f6f4": 16362.0, "mxf4": 32724.0}
+
+
+def tensor_peak_tflops(kind: str, n_sms: int, sm_mhz: float) -> float:
+    """Dense peak of one block-scaled MMA kind at the given SM clock."""
+    return MMA_FLOP_PER_CYCLE_SM[kind] * n_sms * sm_mhz * 1e6 / 1e12
+
+
+def oracle_tokens_per_s(wl, n_tokens: int, threads: int, stream: int = 50, experts: dict | None = None):
+    """Times the fp64 oracle (input norm, routing and layer, for every layer of
+    the workload) on n_tokens seeded tokens.  The expert bytes the sample
+    touches are generated before the clock starts (input generation, on
+    parallel host threads); `experts` keeps them across calls."""
     import oracle
     import synth
-    nl = wl.layers
+    experts = {} if experts is None else experts
     x = synth.activations(wl, tokens=n_tokens, stream=stream)
-    # pre-generate the experts the sample touches, layer by layer
-    banks, t_total = [], 0.0
+    t_total = 0.0
     cur = x
-    for layer in range(nl):
-        xin = oracle.rmsnorm(cur, 1e-6) if wl.rmsnorm else cur
+    for layer in range(wl.layers):
         Wr, b = synth.router_weights(wl, layer), synth.router_bias(wl, layer)
         t0 = time.perf_counter()
+        xin = oracle.rmsnorm(cur, 1e-6) if wl.rmsnorm else cur
         lg = oracle.router_logits(xin, Wr, b, threads=threads)
         idx, w = oracle.topk(lg, wl.top_k)
         t_total += time.perf_counter() - t0
-        ex = {int(e): synth.host_expert(wl, layer, int(e)) for e in np.unique(idx)}
-        sh = [synth.host_expert(wl, layer, wl.n_experts + s) for s in range(wl.n_shared)]
+        ids = [int(e) for e in np.unique(idx)] + [wl.n_experts + s for s in range(wl.n_shared)]
+        missing = [e for e in ids if (layer, e) not in experts]
+        experts.update({(layer, e): v for e, v in synth.host_experts(wl, layer, missing).items()})
+        ex = {e: experts[(layer, e)] for e in ids[:len(ids) - wl.n_shared]}
+        sh = [experts[(layer, wl.n_experts + s)] for s in range(wl.n_shared)]
         t0 = time.perf_counter()
         y, _ = oracle.moe_layer(xin, idx, w, ex, sh, wl.n_experts, wl.inter,
                                 residual=cur if wl.rmsnorm else None, threads=threads)
         t_total += time.perf_counter() - t0
-        if wl.rmsnorm:
-            t0 = time.perf_counter()
-            oracle.rmsnorm(cur, 1e-6)
-            t_total += time.perf_counter() - t0
         cur = y
-        banks.append(len(ex))
     return n_tokens / t_total, t_total
 
 
@@ -215,23 +232,27 @@ def run_reference(args):
     wl = WORKLOADS[args.workload]
     cores = os.cpu_count() or 1
     threads = min(cores, oracle.max_threads())
-    n_tok = max(1, min(threads, 8 if wl.tokens < 512 else 16))
+    # one token per thread (the oracle runs tokens in parallel), the same
+    # seeded block every step so that its experts are generated once
+    n_tok = max(1, threads)
+    experts = {}
     for i in range(args.warmup):
-        oracle_tokens_per_s(wl, n_tok, threads, stream=200 + i)
+        oracle_tokens_per_s(wl, 1, 1, stream=300, experts=experts)
     total_t, total_n = 0.0, 0
     for i in range(args.steps):
-        _, t = oracle_tokens_per_s(wl, n_tok, threads, stream=300 + i)
+        _, t = oracle_tokens_per_s(wl, n_tok, threads, stream=300, experts=experts)
         total_t += t
         total_n += n_tok
     v = total_n / total_t
-    sample = f"{n_tok} seeded tokens per step of workload {wl.name} (routing + layer, fp64 oracle)"
+    sample = (f"{n_tok} seeded tokens per step (one per thread) of workload {wl.name}, through all "
+              f"{wl.layers} layer(s): input norm, routing and layer, fp64 oracle")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000 * total_t / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "tokens": wl.tokens, "layers": wl.layers},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": min(threads, n_tok),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -375,48 +396,78 @@ def run_ours(args):
             a[1] += n
         L.set_option(m.MOE_OPT_TIMING, 0)
     launches = sum(n for _, n in ktimes.values())
-    per_step_launches = launches // max(1, args.steps)
+    # plus one moe_rmsnorm launch per layer of a stack (not a layer call, so not in the layer timers)
+    per_step_launches = launches // max(1, args.steps) + (nl if nl > 1 else 0)
     dom = max(ktimes, key=lambda n: ktimes[n][0])
     dom_ms = ktimes[dom][0] / ktimes[dom][1]
 
     pk = peaks()
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0
+    mma_kind = "mxf4" if args.act == "fp4" else "mxf8f6f4"
+    mma_peak = tensor_peak_tflops(mma_kind, n_sms, sm_mhz)
     roofline = None
     if mean_union is not None:
         b = layer_bytes(wl, mean_union, T, shared_fp8=args.shared == "fp8")
         if dom in b:
-            ach = b[dom] / (dom_ms / 1e3) / 1e9
-            roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": pk["hbm_gbs"],
-                        "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
-                        "traffic": measured_traffic(wl.name, dom),
-                        "algorithmic_bytes_per_launch": b[dom], "avg_launch_ms": dom_ms,
-                        "peak_src": pk["src"]}
+            # the dominant kernel against the bound that takes longer at peak: HBM
+            # streaming of its algorithmic bytes, or its useful block-scaled MMA
+            # FLOPs (gate/up: 2 of the 3 matrices) at the measured MMA rate
+            kflops = layer_flops(wl, T) * (2 / 3 if "up" in dom else 1 / 3)
+            t_hbm = b[dom] / (pk["hbm_gbs"] * 1e9)
+            t_tensor = kflops / (mma_peak * 1e12)
+            if "mma" in dom and t_tensor > t_hbm:
+                ach = kflops / (dom_ms / 1e3) / 1e12
+                roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": mma_peak,
+                            "unit": "TFLOP/s", "frac": ach / mma_peak, "traffic": measured_traffic(wl.name, dom),
+                            "algorithmic_flops_per_launch": kflops, "avg_launch_ms": dom_ms,
+                            "peak_src": f"measured {mma_kind} issue rate x {n_sms} SMs x median SM clock "
+                                        f"{sm_mhz:.0f} MHz"}
+            else:
+                ach = b[dom] / (dom_ms / 1e3) / 1e9
+                roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": pk["hbm_gbs"],
+                            "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                            "traffic": measured_traffic(wl.name, dom),
+                            "algorithmic_bytes_per_launch": b[dom], "avg_launch_ms": dom_ms,
+                            "peak_src": pk["src"]}
         layer_gbs = nl * b["layer"] / (ms_step / 1e3) / 1e9  # all layers' bytes over the step
+        if roofline is not None:
+            # the whole step (every kernel of every layer) against HBM
+            roofline["step"] = {"achieved_gbs": layer_gbs, "frac": layer_gbs / pk["hbm_gbs"],
+                                "algorithmic_bytes_per_step": nl * b["layer"]}
     else:
         layer_gbs = None
 
-    # end to end through the host entry point (copies inside the timed region)
-    e2e = None
-    if nl == 1:
-        xh = torch.empty((n_x, T, H), dtype=torch.int16).pin_memory()
-        xh.copy_(xs.cpu())
-        yh = torch.empty((T, H), dtype=torch.int16).pin_memory()
-        for i in range(args.warmup):
+    # end to end through the host-buffer entry point (copies inside the timed
+    # region): one layer, or the whole stack in one call
+    xh = torch.empty((n_x, T, H), dtype=torch.int16).pin_memory()
+    xh.copy_(xs.cpu())
+    yh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+
+    def host_step(i):
+        if nl == 1:
             Ls[0].forward_host(xh[i % n_x], T, yh)
-        tt = 0.0
-        for i in range(args.warmup, n_in):
-            flush_l2(i)
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            Ls[0].forward_host(xh[i % n_x], T, yh)
-            tt += time.perf_counter() - t0
-        e2e = {"value": world * T * args.steps / tt, "unit": "tokens/s",
-               "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2}
+        else:
+            m.moe_stack_forward_host(Ls, xh[i % n_x], T, 1e-6 if wl.rmsnorm else -1.0, yh)
+    for i in range(args.warmup):
+        host_step(i)
+    tt = 0.0
+    for i in range(args.warmup, n_in):
+        flush_l2(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        host_step(i)
+        tt += time.perf_counter() - t0
+    tt = max_over_ranks(tt, pg, dev)
+    e2e = {"value": world * T * args.steps / tt, "unit": "tokens/s",
+           "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
+           "entry_point": "moe_forward_host" if nl == 1 else "moe_stack_forward_host"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         threads = min(os.cpu_count() or 1, oracle.max_threads())
-        n_tok = max(1, min(threads, 8))
+        n_tok = max(1, threads)  # one token per thread
         # batches of fresh seeded tokens until ~10 s of oracle time (at most 30 batches)
         tot_t, tot_n, nb = 0.0, 0, 0
         while tot_t < 10.0 and nb < 30:
@@ -425,8 +476,9 @@ def run_ours(args):
             tot_n += n_tok
             nb += 1
         cpu = {"value": tot_n / tot_t, "unit": "tokens/s", "cores": min(threads, n_tok), "kind": "oracle",
-               "sample": f"{nb} batches of {n_tok} seeded tokens of {wl.name} ({tot_n} tokens), routing + "
-                         f"layer, fp64 oracle, {tot_t:.1f} s of oracle time"}
+               "sample": f"{nb} batch(es) of {n_tok} seeded tokens of {wl.name} ({tot_n} tokens) through "
+                         f"all {nl} layer(s): input norm, routing and layer, fp64 oracle, "
+                         f"{tot_t:.1f} s of oracle time"}
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -440,7 +492,8 @@ def run_ours(args):
                            "l2": "flushed between steps (512 MB write + read), " +
                                  ("fresh tokens each step" if n_x == n_in else
                                   f"{n_x} distinct token block(s) of {T * H * 2 / 1e6:.0f} MB cycled"),
-                           "mean_expert_union": mean_union},
+                           "mean_expert_union": mean_union,
+                           "input_norm": "RMS norm of each layer's input, eps 1e-6, no gain" if nl > 1 else None},
                 "layer_gbs": layer_gbs,
                 "kernels": {n: {"ms_per_launch": a[0] / a[1], "launches": a[1]}
                             for n, a in ktimes.items()},
@@ -448,18 +501,21 @@ def run_ours(args):
                 "gpu_launches": per_step_launches * args.steps, "clocks": clocks}
         if wl.tokens >= 512:
             # useful MMA work (routed + shared slots, no tile padding) against the
-            # tensor peaks of the FP8-activation kind and of FP4, each the measured
-            # bf16 GEMM rate times the nominal ratio (2x, 6x)
+            # measured block-scaled MMA peaks (issue-rate microbenchmark x SMs x the
+            # median SM clock of the timed loop): the FP8-activation kind the layer
+            # uses, and the FP4 x FP4 kind
             tf = layer_flops(wl, T) / (ms_step / 1e3) / 1e12
             line["tflops"] = tf
-            fp8, fp4 = 2 * pk["bf16_tflops"], 6 * pk["bf16_tflops"]
+            fp8 = tensor_peak_tflops("mxf8f6f4", n_sms, sm_mhz)
+            fp4 = tensor_peak_tflops("mxf4", n_sms, sm_mhz)
             up_ms = ktimes.get("ffn_up_mma", [0.0, 1])
             up_tf = (2 / 3) * layer_flops(wl, T) / (up_ms[0] / up_ms[1] / 1e3) / 1e12 if up_ms[0] else None
             line["tensor"] = {"useful_tflops": tf, "peak_fp8_kind": fp8, "frac_fp8_kind": tf / fp8,
                               "peak_fp4": fp4, "frac_fp4": tf / fp4,
                               "gate_up_kernel_tflops": up_tf,
                               "gate_up_frac_fp8_kind": up_tf / fp8 if up_tf else None,
-                              "peak_src": pk["src"] + " bf16 GEMM x nominal ratio"}
+                              "gate_up_frac_fp4": up_tf / fp4 if up_tf else None,
+                              "peak_src": f"measured issue rates (mma_rate.cu) x {n_sms} SMs x {sm_mhz:.0f} MHz"}
         print(json.dumps(line), flush=True)
     for L in Ls:
         L.close()
@@ -473,7 +529,7 @@ def run_mma_rates() -> int:
     expert GEMM uses; prints the microbenchmark's table."""
     import subprocess
     import tempfile
-    src = os.path.join(ROOT, "mxfp4_expert_ffn_gb300", "mma_rate.cu")
+    src = os.path.join(ROOT, "mma_rate.cu")
     with tempfile.TemporaryDirectory() as d:
         exe = os.path.join(d, "mma_rate")
         subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe, src])

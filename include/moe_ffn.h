@@ -99,7 +99,11 @@ typedef struct moe_layer moe_layer;
 moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int device,
                             moe_layer** out);
 
-/* Synchronises the layer's device, frees its workspace and the handle. */
+/* Synchronises the layer's device, frees its workspace and the handle.
+ * NULL returns MOE_ERR_INVALID_ARG.  The handle must not be used afterwards. */
+moe_status moe_destroy(moe_layer* layer);
+
+/* The same call under the name that pairs with moe_layer_create. */
 moe_status moe_layer_destroy(moe_layer* layer);
 
 /* Router (ai.rs, "What remains is the reference rounding itself": the gate is
@@ -147,6 +151,22 @@ moe_status moe_step(moe_layer* layer, const void* x, int32_t T, const void* resi
 moe_status moe_forward_host(moe_layer* layer, const void* x_host, int32_t T, void* y_host,
                             void* stream);
 
+/* A stack of layers over one batch of T tokens, with x and y in HOST memory
+ * (the 8-layer decode stack of the pages' workloads: layers run back to
+ * back, a bf16 residual add between them).  Copies x to the device, then for
+ * l = 0 .. n_layers - 1
+ *     x_{l+1} = bf16( x_l + moe_step(layers[l], N(x_l)) )
+ * where N(v) = bf16( v / sqrt(mean(v^2) + norm_eps) ) per token (moe_rmsnorm)
+ * when norm_eps >= 0, and the identity when norm_eps < 0; then copies x_n to
+ * y_host.  Returns after y_host is written (the call synchronises the
+ * stream).  All layers must be on one device with one hidden size, and T at
+ * most each one's max_tokens (MOE_ERR_INVALID_ARG otherwise); 1 <= n_layers
+ * <= 64.  Runs entirely in the layers' own workspaces (no allocation); a
+ * device error any layer recorded is returned, and cleared, as by moe_sync.
+ * For full copy speed x_host and y_host should be page-locked. */
+moe_status moe_stack_forward_host(moe_layer* const* layers, int32_t n_layers, const void* x_host,
+                                  int32_t T, float norm_eps, void* y_host, void* stream);
+
 /* The activation quantiser alone: q [T][H] E4M3 codes and s [T][H/32] UE8M0
  * bytes, by the rule: per block of 32, e = the smallest integer with
  * max|x| <= 448 * 2^e (e = 0 for an all-zero block, limited to [-127, 127]),
@@ -184,19 +204,24 @@ moe_status moe_rmsnorm(const void* x, int32_t T, int32_t H, float eps, void* out
  * the device or fail for lack of memory.  The pages describe no such entry
  * point; it has no counterpart there.
  *
- * Same result as moe_route(layer, x, T, NULL, NULL, topk_idx, topk_w, stream)
- * on a layer with these shapes, but without a layer handle: the logits
- * scratch is a fixed array of MOE_ROUTE_STATIC_MAX_LOGITS floats (128 KB)
- * built into the library, which every GPU that loads the library holds until
- * the process exits.  T * E above that limit returns MOE_ERR_UNSUPPORTED;
- * H must be a multiple of 128 (at most 16384), E <= 512, 1 <= k <= min(8, E);
- * x and router_w 16-byte aligned.
+ * Same result, bit for bit, as moe_route(layer, x, T, NULL, NULL, topk_idx,
+ * topk_w, stream) on a layer with these shapes, router weights and the
+ * default scoring (softmax, scale 1): the same split-K kernels, partial sums
+ * added in the same fixed order.  No layer handle is needed: the partial
+ * sums go to a fixed array of 8 * MOE_ROUTE_STATIC_MAX_TOKENS * 512 floats
+ * (1 MiB) built into the library, which every GPU that loads the library
+ * holds until the process exits.  T above MOE_ROUTE_STATIC_MAX_TOKENS returns
+ * MOE_ERR_UNSUPPORTED; H must be a multiple of 128 (at most 16384),
+ * E <= 512, 1 <= k <= min(8, E) (MOE_ERR_INVALID_ARG otherwise); x and
+ * router_w 16-byte aligned; router_b fp32 [E] or NULL.
  * The first call on a device looks up the array's device address (set-up,
- * done once per device with that device current); make that first call
- * before any stream capture.  All calls share the one array: calls whose
- * work overlaps on the GPU (two streams, or two host threads) race on it and
- * must be serialised by the caller.  No call allocates or frees memory. */
-#define MOE_ROUTE_STATIC_MAX_LOGITS (64 * 512)
+ * done once per device with that device current, and again when the
+ * device's context has been replaced, e.g. after cudaDeviceReset); make that
+ * first call before any stream capture.  All calls share the one array:
+ * calls whose work overlaps on the GPU (two streams, or two host threads)
+ * race on it and must be serialised by the caller.  No call allocates or
+ * frees memory. */
+#define MOE_ROUTE_STATIC_MAX_TOKENS 64
 moe_status moe_route_static(const void* x, int32_t T, int32_t H, int32_t E, int32_t k,
                             const float* router_w, const float* router_b, int32_t* topk_idx,
                             float* topk_w, void* stream);
@@ -254,9 +279,18 @@ moe_status moe_sync(moe_layer* layer, void* stream);
  *                  Tensor-core path with FP8 activations only: MOE_ERR_UNSUPPORTED
  *                  without shared experts, with MOE_OPT_PATH = 1 or with FP4
  *                  activations (and those are refused while it is set).
+ *  MOE_OPT_WAIT_LIMIT  how many times a wait inside the tensor-core expert
+ *                  GEMMs polls its barrier before it gives up (default 2^24,
+ *                  far longer than any copy or MMA takes); 0..2^31-1.  A wait
+ *                  that gives up sets the layer's error word (moe_sync then
+ *                  returns MOE_ERR_TIMEOUT), lets the copies and MMAs it had
+ *                  issued finish, frees its tensor memory and ends the kernel;
+ *                  that call's y is undefined and the next call starts clean.
+ *                  0 makes every such wait give up at once: a test of that
+ *                  error path without hanging or faulting the GPU.
  * moe_route_static always uses softmax scoring with scale 1.             */
 enum { MOE_OPT_PATH = 1, MOE_OPT_TIMING = 2, MOE_OPT_SCORING = 3, MOE_OPT_ROUTED_SCALE = 4,
-       MOE_OPT_ACT_FORMAT = 5, MOE_OPT_SHARED_FORMAT = 6 };
+       MOE_OPT_ACT_FORMAT = 5, MOE_OPT_SHARED_FORMAT = 6, MOE_OPT_WAIT_LIMIT = 7 };
 enum { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 };
 enum { MOE_ACT_FP8 = 0, MOE_ACT_FP4 = 1 };
 enum { MOE_SHARED_MXFP4 = 0, MOE_SHARED_FP8_B32 = 1 };

@@ -5,7 +5,8 @@
 // kind) and kind::mxf4 (A and B packed E2M1, K = 64, scale_vec::2X; the
 // FP4-activation variant's kind), M = 128 and N from 16 to 256.  One CTA per
 // SM, one issuing thread; every wait is bounded.  Built and run by
-// `python bench.py --mma-rates`; a measurement tool, not part of the library.
+// `python bench.py --mma-rates`; a measurement tool beside the benchmark, not
+// part of the library.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>

@@ -16,18 +16,19 @@ LIB_PATH = os.path.join(_HERE, "libmoe_ffn.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_INTERNAL = 4, 5, 6
 MOE_OPT_PATH, MOE_OPT_TIMING, MOE_OPT_SCORING, MOE_OPT_ROUTED_SCALE, MOE_OPT_ACT_FORMAT = 1, 2, 3, 4, 5
-MOE_OPT_SHARED_FORMAT = 6
+MOE_OPT_SHARED_FORMAT, MOE_OPT_WAIT_LIMIT = 6, 7
+WAIT_LIMIT_DEFAULT = 1 << 24
 MOE_SHARED_MXFP4, MOE_SHARED_FP8_B32 = 0, 1
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 MOE_ACT_FP8, MOE_ACT_FP4 = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_MMA = 0, 1, 2
 
 # every symbol include/moe_ffn.h declares
-EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_route", "moe_forward", "moe_step",
+EXPORTS = ("moe_layer_create", "moe_destroy", "moe_layer_destroy", "moe_route", "moe_forward", "moe_step",
            "moe_forward_host", "moe_quantize_act", "moe_quantize_act4", "moe_segments", "moe_rmsnorm", "moe_sync",
            "moe_set_option", "moe_get_kernel_times", "moe_status_string", "moe_abi_version",
-           "moe_route_static")
-ROUTE_STATIC_MAX_LOGITS = 64 * 512
+           "moe_route_static", "moe_stack_forward_host")
+ROUTE_STATIC_MAX_TOKENS = 64
 
 
 class MoeError(RuntimeError):
@@ -66,6 +67,7 @@ def lib():
         L = C.CDLL(LIB_PATH)
         L.moe_layer_create.argtypes = [C.POINTER(MoeConfig), C.POINTER(MoeWeights), C.c_int,
                                        C.POINTER(P)]
+        L.moe_destroy.argtypes = [P]
         L.moe_layer_destroy.argtypes = [P]
         L.moe_route.argtypes = [P, P, I32, P, P, P, P, P]
         L.moe_forward.argtypes = [P, P, I32, P, P, P, P, P]
@@ -80,6 +82,7 @@ def lib():
         L.moe_get_kernel_times.argtypes = [P, C.POINTER(C.c_char_p), C.POINTER(C.c_double),
                                            C.POINTER(C.c_int64), I32, C.POINTER(I32)]
         L.moe_route_static.argtypes = [P, I32, I32, I32, I32, P, P, P, P, P]
+        L.moe_stack_forward_host.argtypes = [P, I32, P, I32, C.c_float, P, P]
         L.moe_status_string.argtypes = [C.c_int]
         L.moe_status_string.restype = C.c_char_p
         L.moe_abi_version.restype = I32
@@ -133,6 +136,10 @@ def moe_layer_create(cfg: MoeConfig, weights: MoeWeights, device: int = 0) -> in
     return h.value
 
 
+def moe_destroy(h: int) -> None:
+    _check(lib().moe_destroy(h), "moe_destroy")
+
+
 def moe_layer_destroy(h: int) -> None:
     _check(lib().moe_layer_destroy(h), "moe_layer_destroy")
 
@@ -178,9 +185,19 @@ def moe_rmsnorm(x, T, H, eps, out, stream=None) -> None:
 
 
 def moe_route_static(x, T, H, E, k, router_w, router_b, topk_idx, topk_w, stream=None) -> None:
-    """Router that allocates nothing (logits scratch built into the library)."""
+    """Router that allocates nothing (its scratch is built into the library);
+    the same results as moe_route for up to ROUTE_STATIC_MAX_TOKENS tokens."""
     _check(lib().moe_route_static(ptr(x), T, H, E, k, ptr(router_w), ptr(router_b), ptr(topk_idx),
                                   ptr(topk_w), stream_handle(stream)), "moe_route_static")
+
+
+def moe_stack_forward_host(handles, x_host, T, norm_eps, y_host, stream=None) -> None:
+    """A stack of layers (handles, or Layer objects) from host x to host y:
+    per layer x = x + step(rmsnorm(x)) (norm_eps >= 0) or x + step(x) (norm_eps < 0)."""
+    hs = [h.handle if isinstance(h, Layer) else h for h in handles]
+    arr = (P * len(hs))(*hs)
+    _check(lib().moe_stack_forward_host(arr, len(hs), ptr(x_host), T, norm_eps, ptr(y_host),
+                                        stream_handle(stream)), "moe_stack_forward_host")
 
 
 def moe_sync(h, stream=None) -> int:
@@ -269,7 +286,7 @@ class Layer:
 
     def close(self):
         if self.handle:
-            moe_layer_destroy(self.handle)
+            moe_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -268,7 +268,7 @@ moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int dev
   return MOE_OK;
 }
 
-moe_status moe_layer_destroy(moe_layer* L) {
+moe_status moe_destroy(moe_layer* L) {
   if (!L) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(L->device);
   cudaError_t e = cudaDeviceSynchronize();
@@ -280,6 +280,8 @@ moe_status moe_layer_destroy(moe_layer* L) {
   delete L;
   return cuda_fail(e);
 }
+
+moe_status moe_layer_destroy(moe_layer* L) { return moe_destroy(L); }
 
 moe_status moe_set_option(moe_layer* L, int32_t option, int64_t value) {
   if (!L) return MOE_ERR_INVALID_ARG;
@@ -322,6 +324,11 @@ moe_status moe_set_option(moe_layer* L, int32_t option, int64_t value) {
     if (value == MOE_ACT_FP4 && (!L->maps || !mma_act4_supported(L->cfg))) return MOE_ERR_UNSUPPORTED;
     if (value == MOE_ACT_FP4 && L->shared_format == MOE_SHARED_FP8_B32) return MOE_ERR_UNSUPPORTED;
     L->act_format = (int)value;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_WAIT_LIMIT) {
+    if (value < 0 || value > 0x7FFFFFFFll) return MOE_ERR_INVALID_ARG;
+    L->wait_limit = (uint32_t)value;
     return MOE_OK;
   }
   if (option == MOE_OPT_TIMING) {
@@ -447,7 +454,8 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool gather, const float* w
   cudaError_t e;
   {
     TimedScope ts(L, st, "ffn_up_mma");
-    e = launch_ffn_mma(*L->maps, bank, 0, bn, gather, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles);
+    e = launch_ffn_mma(*L->maps, bank, 0, bn, gather, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles,
+                       L->wait_limit);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   if (gather && c.n_shared > 0) {
@@ -456,11 +464,13 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool gather, const float* w
     const CombineArgs cmb{T, c.top_k, c.n_shared, w, static_cast<const uint16_t*>(residual),
                           static_cast<uint16_t*>(y)};
     TimedScope ts(L, st, "ffn_down_mma");
-    return cuda_fail(launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, &cmb, act4_of(L), ns_tiles));
+    return cuda_fail(launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, &cmb, act4_of(L), ns_tiles,
+                                    L->wait_limit));
   }
   {
     TimedScope ts(L, st, "ffn_down_mma");
-    e = launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles);
+    e = launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles,
+                       L->wait_limit);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   {
@@ -623,6 +633,64 @@ moe_status moe_forward_host(moe_layer* L, const void* x_host, int32_t T, void* y
   if (bits) {
     e = cudaMemsetAsync(L->ws.err, 0, sizeof(int32_t), st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return (bits & kErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_INTERNAL;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_stack_forward_host(moe_layer* const* Ls, int32_t n, const void* x_host, int32_t T,
+                                  float norm_eps, void* y_host, void* stream) {
+  if (!Ls || n < 1 || n > 64 || !x_host || !y_host || norm_eps != norm_eps) return MOE_ERR_INVALID_ARG;
+  for (int l = 0; l < n; ++l) {
+    moe_status s = check_tokens(Ls[l], T);
+    if (s != MOE_OK) return s;
+    if (Ls[l]->device != Ls[0]->device || Ls[l]->cfg.hidden != Ls[0]->cfg.hidden) return MOE_ERR_INVALID_ARG;
+  }
+  if (T == 0) return MOE_OK;
+  if (fault("launch")) return MOE_ERR_CUDA;
+  DeviceGuard g(Ls[0]->device);
+  if (g.status != cudaSuccess) return cuda_fail(g.status);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int H = Ls[0]->cfg.hidden;
+  const bool norm = norm_eps >= 0.f;
+  const size_t bytes = (size_t)T * H * sizeof(uint16_t);
+  // The residual stream: the input in layer 0's y (normalised: x_0 is only
+  // read as the residual) or x (not normalised: x_0 is the layer's input),
+  // then each layer's output in its own y.  A layer's y may alias its
+  // residual but never its input.
+  uint16_t* cur = norm ? Ls[0]->ws.y : Ls[0]->ws.x;
+  cudaError_t e = cudaMemcpyAsync(cur, x_host, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  for (int l = 0; l < n; ++l) {
+    moe_layer* L = Ls[l];
+    const uint16_t* in = cur;
+    if (norm) {
+      e = launch_rmsnorm(cur, T, H, norm_eps, L->ws.x, st);
+      if (e != cudaSuccess) return cuda_fail(e);
+      in = L->ws.x;
+    }
+    uint16_t* out = (!norm && cur == L->ws.y) ? L->ws.x : L->ws.y;
+    moe_status s = step_impl(L, in, T, cur, out, nullptr, nullptr, nullptr, st);
+    if (s != MOE_OK) return s;
+    cur = out;
+  }
+  e = cudaMemcpyAsync(y_host, cur, bytes, cudaMemcpyDeviceToHost, st);
+  for (int l = 0; e == cudaSuccess && l < n; ++l)
+    e = cudaMemcpyAsync(Ls[l]->ws.err_host, Ls[l]->ws.err, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int32_t bits = 0;
+  for (int l = 0; l < n; ++l) {
+    const int32_t b = *Ls[l]->ws.err_host;
+    if (b) {
+      bits |= b;
+      e = cudaMemsetAsync(Ls[l]->ws.err, 0, sizeof(int32_t), st);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+  }
+  if (bits) {
+    e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e);
     return (bits & kErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_INTERNAL;
   }

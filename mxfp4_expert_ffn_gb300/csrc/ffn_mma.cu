@@ -88,7 +88,6 @@ struct FormatMaps {
   CUtensorMap gu_pair, s_gu_pair;  // gate + up as one 4-D tensor (when possible)
   int merged[2], swap_gu[2];
   CUtensorMap xg[3], hq[3];  // per token tile width: 16, 64, 112
-  CUtensorMap xg_half, hq_half;  // CTA pairs: half a 112-token tile, one chunk per box
   int ch_up, ch_down;
   bool ok;
   bool shared_fp8;  // the shared maps read FP8 (32 x 32 block) weights
@@ -138,8 +137,6 @@ static bool format_maps(FormatMaps* m, bool a4, const moe_config& c, const moe_w
   for (int i = 0; ok && i < 3; ++i)
     ok = map_3d(&m->xg[i], false, ws.xg, xk, P, bns[i], m->ch_up) &&
          map_3d(&m->hq[i], false, ws.hq, hk, P, bns[i], m->ch_down);
-  if (ok)
-    ok = map_3d(&m->xg_half, false, ws.xg, xk, P, 112 / 2, 1) && map_3d(&m->hq_half, false, ws.hq, hk, P, 112 / 2, 1);
   m->ok = ok;
   return ok;
 }
@@ -177,13 +174,14 @@ void mma_maps_destroy(MmaMaps* m) { delete m; }
 
 cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, int bn, bool gather,
                            const Workspace& ws, int num_sms, cudaStream_t st, const CombineArgs* cmb, bool act4,
-                           int ns_tiles) {
+                           int ns_tiles, uint32_t wait_limit) {
   const FormatMaps& mm = maps.f[act4 ? 1 : 0];
   if (!mm.ok) return cudaErrorInvalidValue;
   MmaParams p;
   memset(&p, 0, sizeof(p));
   p.shared_fp8 = mm.shared_fp8 ? 1 : 0;
   p.ns_tiles = ns_tiles;
+  p.wait_limit = wait_limit;
   const int bi = bn_index(bn);
   int ch;
   if (mode == kModeUp) {
@@ -247,11 +245,8 @@ cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, 
     p.y = cmb->y;
     p.comb_cnt = ws.comb_cnt;
   }
-  // CTA pairs for the widest tiles: both row-tile counts even, an even grid
-  const bool pair = bn == 112 && (p.rows / 128) % 2 == 0 && num_sms >= 2;
-  if (pair) p.b_half = mode == kModeUp ? mm.xg_half : mm.hq_half;
-  return act4 ? launch_ffn_mma_fp4(p, mode, bn, ch, pair, num_sms, st)
-              : launch_ffn_mma_fp8(p, mode, bn, ch, pair, num_sms, st);
+  return act4 ? launch_ffn_mma_fp4(p, mode, bn, ch, num_sms, st)
+              : launch_ffn_mma_fp8(p, mode, bn, ch, num_sms, st);
 }
 
 }  // namespace moe

@@ -41,7 +41,6 @@ struct MmaParams {
   CUtensorMap a_routed[2];   // up mode: gate, up banks; down mode: down bank in [0]
   CUtensorMap a_shared[2];
   CUtensorMap b;             // activations by position, 3-D view of [P][K] E4M3
-  CUtensorMap b_half;        // CTA pairs: the same view, half a token tile, one chunk per box
   const uint8_t* sa_routed[2];
   const uint8_t* sa_shared[2];
   const uint8_t* sb;         // activation scales by position, [P][K/32]
@@ -71,6 +70,7 @@ struct MmaParams {
   const uint8_t* xq;         // gather: E4M3 codes of x by token, [T][K]
   const int32_t* pos_tok;    // gather: token of each position
   int shared_fp8;            // shared experts in FP8 (E4M3, one scale per 32 x 32 block)
+  uint32_t wait_limit;       // polls after which a pipeline wait gives up (then the error word)
   int ns_tiles;              // token tiles of the shared experts (the last ones of the table)
   int32_t* err;
 };
@@ -81,7 +81,9 @@ using namespace sm100;
 
 constexpr int kThreadsMma = 352;  // 11 warps: TMA, MMA, 4 epilogue, 4 scale-factor, 2nd MMA
 constexpr int kIssuer2Warp = 10;
-constexpr uint32_t kWaitLimit = 1u << 24;
+// Polls for the waits that let copies and MMAs already issued complete before
+// the CTA leaves (they always end: the hardware finishes what was issued).
+constexpr uint32_t kDrainLimit = 1u << 24;
 constexpr int kSmemBudget = 227 * 1024 - 2048;
 
 constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
@@ -147,13 +149,12 @@ struct Unit {
 };
 
 // Unit u -> (token tile v, 128-row tile); row tiles innermost so consecutive
-// units share the activation tile.  For a CTA pair, u counts pairs of row
-// tiles (mt_units = row tiles / 2) and rank picks the pair's member.
-__device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_units, int rank = -1) {
+// units share the activation tile.
+__device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_units) {
   const int v = u / mt_units;
   const int4 t = __ldg(p.tile_info + v);
   const int r = u - v * mt_units;
-  return Unit{t.x, t.y, t.z, (rank < 0 ? r : 2 * r + rank) * 128};
+  return Unit{t.x, t.y, t.z, r * 128};
 }
 
 // Work partition.  Plain: whole units strided over the CTAs.  Split: when
@@ -174,7 +175,7 @@ constexpr int kMaxTopK = 8, kMaxShared = 4;  // layer limits (moe_config)
 struct Sched {
   int ti, g, end;  // split: stage iterations in all, cursor, end of this CTA's range
   int total, ks, u;
-  int cta, G;      // this worker and the number of workers (CTAs, or CTA pairs)
+  int cta, G;      // this CTA and the number of CTAs
   bool split;
   __device__ Sched(int total_, int ks_, int split_ok, int cta_, int G_)
       : total(total_), ks(ks_), cta(cta_), G(G_) {
@@ -233,37 +234,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// Multicast load into the same shared-memory offset of every CTA in mask (the
-// mbarrier at bar's offset in each of them receives the bytes).
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
-                                               int32_t c2, uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
-      "[%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
-// tcgen05.commit whose arrival goes to the mbarrier at bar's offset in every
-// CTA of mask.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // h = silu(g) * u = g / (1 + e^-g) * u with the SFU exponential and the fast
 // divide: a few ulp from the correctly rounded form, far inside the FP8
 // rounding of h that follows (one E4M3 step is 2^-3 relative).
@@ -280,10 +250,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// PAIR: the grid is clusters of two CTAs that process the two row tiles of a
-// pair for the same token tile: each CTA loads half of the activation tile
-// and multicasts it to both, so each SM moves half the activation bytes.
-template <int MODE, int BN, int CH, bool PAIR, bool A4>
+template <int MODE, int BN, int CH, bool A4>
 __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_constant__ MmaParams p) {
   using C = Cfg<MODE, BN, CH, A4>;
   constexpr int NA = C::kNA;
@@ -291,7 +258,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full_bar[kMaxStages], sf_bar[kMaxStages], empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
+  __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -319,15 +286,16 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       prefetch_tensormap(&p.a_routed[m]);
       prefetch_tensormap(&p.a_shared[m]);
     }
-    prefetch_tensormap(PAIR ? &p.b_half : &p.b);
+    prefetch_tensormap(&p.b);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&sf_bar[s], 4);
-      mbar_init(&empty_bar[s], PAIR ? 4 : 2);  // one commit per MMA-issuing thread (of both CTAs)
+      mbar_init(&empty_bar[s], 2);  // one commit per MMA-issuing thread
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf_bar[b], 2);
       mbar_init(&acce_bar[b], 4);
+      mbar_init(&drain_bar[b], 1);
     }
     abort_flag = 0;
     fence_barrier_init();
@@ -335,8 +303,6 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   if (warp == 1) tmem_alloc(&tmem_slot, C::kTmemAlloc);
   fence_before();
   __syncthreads();
-  // a pair's barriers must be initialised before the peer multicasts into them
-  if constexpr (PAIR) cluster_sync_all();
   fence_after();
   const uint32_t tmem = tmem_slot;
   // Programmatic dependent launch.  Usually the tile table and the weights
@@ -346,14 +312,12 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   // kernel the tile table is that kernel's own output, so everything waits.
   if (p.wait_tiles) pdl_wait();
   pdl_trigger();
-  const int rank = PAIR ? (int)cluster_ctarank() : -1;
-  const int mt_units = PAIR ? mt_per_expert / 2 : mt_per_expert;
+  const int mt_units = mt_per_expert;
   const int total = p.n_active[1] * mt_units;
   // FP8 shared experts: their tiles close the table, so a unit's format follows
   // from its index (no tile-table load on the issuing thread)
   const int shared_tile0 = (!A4 && p.shared_fp8) ? p.n_active[1] - p.ns_tiles : 0x7FFFFFFF;
-  const Sched sc0(total, k_stages, BN <= 64 && p.split_ok, PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x,
-                  PAIR ? (int)gridDim.x / 2 : (int)gridDim.x);
+  const Sched sc0(total, k_stages, BN <= 64 && p.split_ok, (int)blockIdx.x, (int)gridDim.x);
 
   auto give_up = [&]() {
     atomicOr(p.err, kErrTimeout);
@@ -368,24 +332,15 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       int last_parity[kMaxStages];
       int deferred_pos[kMaxStages], deferred_s[kMaxStages], n_deferred = 0;
       bool waited = gather;  // gather mode: the TMA warp loads weights only
-      // the activation tile of a stage: whole (one op), or for a CTA pair this
-      // CTA's half of every chunk, multicast into both CTAs' slots
+      // the activation tile of a stage, one op
       auto load_b = [&](int slot, int pos0, int st) {
-        uint8_t* sb = stage_base + slot * stage_bytes + NA * C::kATile;
-        if constexpr (PAIR) {
-#pragma unroll
-          for (int c = 0; c < CH; ++c)
-            tma_load_3d_mc(sb + (c * BN + rank * (BN / 2)) * 128, &p.b_half, 0, pos0 + rank * (BN / 2), st * CH + c,
-                           &full_bar[slot], 0x3);
-        } else {
-          tma_load_3d(sb, &p.b, 0, pos0, st * CH, &full_bar[slot]);
-        }
+        tma_load_3d(stage_base + slot * stage_bytes + NA * C::kATile, &p.b, 0, pos0, st * CH, &full_bar[slot]);
       };
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
       Sched sc = sc0;
       for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next()) {
-        const Unit un = decode_unit(p, pc.u, mt_units, rank);
+        const Unit un = decode_unit(p, pc.u, mt_units);
         const bool sh = un.e >= p.E;
         const int erow = (sh ? un.e - p.E : un.e) * p.rows + un.row0;
         bool ok = true;
@@ -399,7 +354,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             waited = true;
             for (int i = 0; i < n_deferred; ++i) load_b(i, deferred_pos[i], deferred_s[i]);
           }
-          if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); ok = false; break; }
+          if (!mbar_wait(&empty_bar[slot], ph ^ 1, p.wait_limit)) { give_up(); ok = false; break; }
           uint8_t* sa = stage_base + slot * stage_bytes;
           // FP8 shared weights arrive as bytes: twice the packed FP4 count
           mbar_expect_tx(&full_bar[slot], tx_stage + (pc.u / mt_units >= shared_tile0 ? NA * 128 * 64 * CH : 0));
@@ -433,14 +388,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       // never leave with copies in flight: wait for the last load into each slot
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s)
-        if (last_parity[s] >= 0) mbar_wait(&full_bar[s], (uint32_t)last_parity[s], kWaitLimit);
-      if constexpr (PAIR) {
-        // nor with the pair's releases still on their way: wait until both CTAs
-        // have released the last fill of every slot
-#pragma unroll
-        for (int s = 0; s < kMaxStages; ++s)
-          if (last_parity[s] >= 0) mbar_wait(&empty_bar[s], (uint32_t)last_parity[s], kWaitLimit);
-      }
+        if (last_parity[s] >= 0) mbar_wait(&full_bar[s], (uint32_t)last_parity[s], kDrainLimit);
     }
   } else if (warp == 1 || warp == kIssuer2Warp) {
     // ---------------------------------------------------------------- MMA
@@ -457,12 +405,12 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
         const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
         const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
-        if (!mbar_wait(&acce_bar[buf], ph_acc ^ 1, kWaitLimit)) { give_up(); break; }
+        if (!mbar_wait(&acce_bar[buf], ph_acc ^ 1, p.wait_limit)) { give_up(); break; }
         fence_after();
         const uint32_t d_tmem = tmem + buf * C::kAccCols;
         int swap = 0, NI = NI0;
         if (NA == 2 || C::kRagged) {
-          const Unit un = decode_unit(p, pc.u, mt_units, rank);
+          const Unit un = decode_unit(p, pc.u, mt_units);
           const int sh = un.e >= p.E;
           if (NA == 2) swap = p.merged[sh] && p.swap_gu[sh];
           if (C::kRagged) {
@@ -480,7 +428,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         for (int s = s_beg; s < s_end; ++s, ++g) {
           const int slot = g % NS;
           const uint32_t ph = (g / NS) & 1;
-          if (!mbar_wait(&full_bar[slot], ph, kWaitLimit) || !mbar_wait(&sf_bar[slot], ph, kWaitLimit)) {
+          if (!mbar_wait(&full_bar[slot], ph, p.wait_limit) || !mbar_wait(&sf_bar[slot], ph, p.wait_limit)) {
             give_up();
             ok = false;
             break;
@@ -520,14 +468,17 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
                       sfb, (s != s_beg || i != first) ? 1u : 0u);
               }
             }
-          if constexpr (PAIR)
-            mma_commit_mc(&empty_bar[slot], 0x3);  // the slot is refilled in both CTAs at once
-          else
-            mma_commit(&empty_bar[slot]);
+          mma_commit(&empty_bar[slot]);
         }
         if (!ok) break;
         mma_commit(&accf_bar[buf]);
       }
+      // Leave only when every MMA this thread issued has completed: after a
+      // wait elsewhere gave up, nothing else waits for them, and the TMEM they
+      // write is freed below.  (With no MMA outstanding the commit arrives at
+      // once.)
+      mma_commit(&drain_bar[j]);
+      mbar_wait(&drain_bar[j], 0, kDrainLimit);
     }
   } else if (warp >= 6) {
     // ------------------------------------------------------- scale factors
@@ -542,7 +493,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     bool ok = true;
     Sched sc = sc0;
     for (Piece pc = sc.next(); ok && pc.u >= 0 && !aborted(); pc = sc.next()) {
-      const Unit un = decode_unit(p, pc.u, mt_units, rank);
+      const Unit un = decode_unit(p, pc.u, mt_units);
       const int s_end = pc.s1;
       const bool sh = un.e >= p.E;
       const size_t erow = (size_t)(sh ? un.e - p.E : un.e) * p.rows + un.row0 + 32 * q + lane;
@@ -618,7 +569,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           if (s0 + i >= s_end) break;
           const int slot = g % NS;
           const uint32_t ph = (g / NS) & 1;
-          if (!mbar_wait(&empty_bar[slot], ph ^ 1, kWaitLimit)) { give_up(); return false; }
+          if (!mbar_wait(&empty_bar[slot], ph ^ 1, p.wait_limit)) { give_up(); return false; }
           fence_after();
           if constexpr (kGatherCapable) {
             if (gather) {
@@ -795,10 +746,10 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     uint32_t it = 0;
     Sched sc = sc0;
     for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
-      const Unit un = decode_unit(p, pc.u, mt_units, rank);
+      const Unit un = decode_unit(p, pc.u, mt_units);
       const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
       const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
-      if (!mbar_wait(&accf_bar[buf], ph_acc, kWaitLimit)) { give_up(); break; }
+      if (!mbar_wait(&accf_bar[buf], ph_acc, p.wait_limit)) { give_up(); break; }
       fence_after();
       const uint32_t t_base = tmem + ((uint32_t)(32 * q) << 16) + buf * C::kAccCols;
       int first, n;
@@ -886,21 +837,19 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   }
   fence_before();
   __syncthreads();
-  // a CTA of a pair leaves only when the peer no longer writes into it
-  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     fence_after();
     tmem_dealloc(tmem, C::kTmemAlloc);
   }
 }
 
-template <int MODE, int BN, int CH, bool PAIR, bool A4>
+template <int MODE, int BN, int CH, bool A4>
 cudaError_t launch_one(MmaParams& p, int num_sms, cudaStream_t st) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_mma_kernel<MODE, BN, CH, PAIR, A4>,
+    cudaError_t e = cudaFuncSetAttribute(ffn_mma_kernel<MODE, BN, CH, A4>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -908,36 +857,16 @@ cudaError_t launch_one(MmaParams& p, int num_sms, cudaStream_t st) {
   int smem = 0;
   geometry<MODE, BN, CH, A4>(p.K, &p.n_stages, &smem);
   if (p.n_stages < 2) return cudaErrorInvalidConfiguration;
-  if (!PAIR) {
-    { cudaError_t le_ = launch_pdl(ffn_mma_kernel<MODE, BN, CH, false, A4>, dim3(num_sms), dim3(kThreadsMma), smem, st, p); if (le_ != cudaSuccess) return le_; }
-    return cudaGetLastError();
-  }
-  // clusters of two CTAs, as a programmatic dependent launch
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_sms & ~1);
-  cfg.blockDim = dim3(kThreadsMma);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, ffn_mma_kernel<MODE, BN, CH, PAIR, A4>, p);
+  cudaError_t e = launch_pdl(ffn_mma_kernel<MODE, BN, CH, A4>, dim3(num_sms), dim3(kThreadsMma), smem, st, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <int MODE, int CH, bool A4>
-cudaError_t launch_bn(MmaParams& p, int bn, bool pair, int num_sms, cudaStream_t st) {
-  if (bn == 16) return launch_one<MODE, 16, CH, false, A4>(p, num_sms, st);
-  if (bn == 64) return launch_one<MODE, 64, CH, false, A4>(p, num_sms, st);
-  if (pair) return launch_one<MODE, 112, CH, true, A4>(p, num_sms, st);
-  return launch_one<MODE, 112, CH, false, A4>(p, num_sms, st);
+cudaError_t launch_bn(MmaParams& p, int bn, int num_sms, cudaStream_t st) {
+  if (bn == 16) return launch_one<MODE, 16, CH, A4>(p, num_sms, st);
+  if (bn == 64) return launch_one<MODE, 64, CH, A4>(p, num_sms, st);
+  return launch_one<MODE, 112, CH, A4>(p, num_sms, st);
 }
 
 }  // namespace
@@ -945,26 +874,25 @@ cudaError_t launch_bn(MmaParams& p, int bn, bool pair, int num_sms, cudaStream_t
 // Launches of the kernel for one activation format (one translation unit each,
 // so that the two sets of instantiations compile in parallel).  ch: chunks per
 // stage, 1..3.
-cudaError_t launch_ffn_mma_fp8(MmaParams& p, int mode, int bn, int ch, bool pair, int num_sms, cudaStream_t st);
-cudaError_t launch_ffn_mma_fp4(MmaParams& p, int mode, int bn, int ch, bool pair, int num_sms, cudaStream_t st);
+cudaError_t launch_ffn_mma_fp8(MmaParams& p, int mode, int bn, int ch, int num_sms, cudaStream_t st);
+cudaError_t launch_ffn_mma_fp4(MmaParams& p, int mode, int bn, int ch, int num_sms, cudaStream_t st);
 
 #ifdef MOE_FFN_MMA_INSTANTIATE
-cudaError_t MOE_FFN_MMA_INSTANTIATE(MmaParams& p, int mode, int bn, int ch, bool pair, int num_sms,
-                                    cudaStream_t st) {
+cudaError_t MOE_FFN_MMA_INSTANTIATE(MmaParams& p, int mode, int bn, int ch, int num_sms, cudaStream_t st) {
 #if MOE_FFN_MMA_A4
   // FP4 activations: one 256-element chunk per stage (the TMEM left next to
   // the widest tile's double-buffered accumulators holds two stages' scales)
   if (ch != 1) return cudaErrorInvalidValue;
-  return mode == kModeUp ? launch_bn<kModeUp, 1, true>(p, bn, pair, num_sms, st)
-                         : launch_bn<kModeDown, 1, true>(p, bn, pair, num_sms, st);
+  return mode == kModeUp ? launch_bn<kModeUp, 1, true>(p, bn, num_sms, st)
+                         : launch_bn<kModeDown, 1, true>(p, bn, num_sms, st);
 #else
   // ch 3 only where it divides down's K chunks (I / 384)
   if (mode == kModeUp)
-    return ch == 2 ? launch_bn<kModeUp, 2, false>(p, bn, pair, num_sms, st)
-                   : launch_bn<kModeUp, 1, false>(p, bn, pair, num_sms, st);
-  if (ch == 3) return launch_bn<kModeDown, 3, false>(p, bn, pair, num_sms, st);
-  return ch == 2 ? launch_bn<kModeDown, 2, false>(p, bn, pair, num_sms, st)
-                 : launch_bn<kModeDown, 1, false>(p, bn, pair, num_sms, st);
+    return ch == 2 ? launch_bn<kModeUp, 2, false>(p, bn, num_sms, st)
+                   : launch_bn<kModeUp, 1, false>(p, bn, num_sms, st);
+  if (ch == 3) return launch_bn<kModeDown, 3, false>(p, bn, num_sms, st);
+  return ch == 2 ? launch_bn<kModeDown, 2, false>(p, bn, num_sms, st)
+                 : launch_bn<kModeDown, 1, false>(p, bn, num_sms, st);
 #endif
 }
 #endif

@@ -91,6 +91,7 @@ struct moe_layer {
   int act_format = 0;         // MOE_ACT_FP8 / MOE_ACT_FP4
   int out_rows = 0;           // y rows the pinned staging (ws.err_host) holds after the error word
   int shared_format = 0;      // MOE_SHARED_MXFP4 / MOE_SHARED_FP8_B32
+  uint32_t wait_limit = 1u << 24;  // polls per bounded wait in the tensor-core GEMMs
   bool timing = false;
   moe::Workspace ws;
   moe::MmaMaps* maps = nullptr;  // TMA descriptors of the tensor-core path
@@ -181,9 +182,11 @@ struct CombineArgs {
 // bn <= 64): the combine runs inside the down GEMM (needs T <= kPrepMaxTokens).
 // act4: the FP4-activation variant (xg/xq/hq hold packed E2M1 codes).
 // ns_tiles: token tiles of the shared experts (n_shared x ceil(T / bn)).
+// wait_limit: polls after which a pipeline wait gives up (MOE_OPT_WAIT_LIMIT).
 cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn, bool gather,
                            const Workspace& ws, int num_sms, cudaStream_t st,
-                           const CombineArgs* cmb = nullptr, bool act4 = false, int ns_tiles = 0);
+                           const CombineArgs* cmb = nullptr, bool act4 = false, int ns_tiles = 0,
+                           uint32_t wait_limit = 1u << 24);
 // Re-encodes the shared experts' maps for MXFP4 or FP8 (32 x 32 block) weights.
 bool mma_maps_set_shared_format(MmaMaps* m, const moe_config& c, const moe_weights& w, bool fp8);
 // FP4 activations need H and I multiples of 256 (whole 128-byte chunks).

@@ -14,8 +14,9 @@
 
 namespace moe {
 
-// e^x in fp32 from IEEE operations only (Cody-Waite reduction by ln 2, a
-// degree-7 Taylor polynomial on |r| <= ln2/2, exact scaling by 2^n), so that any
+// e^x in fp32 from IEEE operations only (Cody-Waite reduction by ln 2, split
+// in two parts as the SLEEF vector math library publishes for single precision,
+// a degree-7 Taylor polynomial on |r| <= ln2/2, exact scaling by 2^n), so that any
 // implementation doing the same operations gets the same bits.  x is clamped
 // to [-87, 88]; error a few ulp.
 __device__ __forceinline__ float exp_poly_f32(float x) {

@@ -278,7 +278,9 @@ void orc_topk(const float* logits, int T, int E, int k, int32_t* idx, double* w)
  * fp32, the precision the layer computes it in, so sigmoid here is a fixed
  * sequence of correctly rounded fp32 operations: e^x by Cody and Waite's
  * reduction x = n ln2 + r (n = round-half-even(x log2 e), ln 2 split into
- * 0.693145752 + 1.42860677e-6 so that n * 0.693145752 is exact), e^r by its
+ * 0.693145752 + 1.42860677e-6 so that n * 0.693145752 is exact -- the same
+ * two-part split of ln 2 that the SLEEF vector math library publishes for
+ * single precision), e^r by its
  * degree-7 Taylor polynomial in Horner form with fused multiply-adds
  * (truncation below 6e-9 relative on |r| <= ln2/2), then times 2^n; x is first
  * clamped to [-87, 88].  Compiled without floating-point contraction. */

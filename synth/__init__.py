@@ -135,6 +135,17 @@ def host_expert(wl: "Workload", layer: int, expert: int) -> dict:
     }
 
 
+def host_experts(wl: "Workload", layer: int, ids) -> dict:
+    """host_expert for several ids, generated on parallel host threads (the
+    generator is C called through ctypes, which releases the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+    ids = [int(e) for e in ids]
+    if len(ids) <= 1:
+        return {e: host_expert(wl, layer, e) for e in ids}
+    with ThreadPoolExecutor(max_workers=min(len(ids), os.cpu_count() or 1)) as ex:
+        return dict(zip(ids, ex.map(lambda e: host_expert(wl, layer, e), ids)))
+
+
 # The shared-expert FP8 variant: E4M3 codes with one UE8M0 scale per 32 x 32
 # block, drawn from streams of their own (matrix ids 4..6).  Scale exponents
 # sit 6 below the MXFP4 range, since E4M3 reaches 448 where E2M1 reaches 6.

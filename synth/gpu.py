@@ -62,7 +62,7 @@ def device_layer(wl, layer: int = 0, device: str = "cuda") -> dict:
 
 def host_experts(wl, layer: int, ids) -> dict:
     """Host copies (regenerated, not read back) of the given expert ids."""
-    return {int(e): synth.host_expert(wl, layer, int(e)) for e in ids}
+    return synth.host_experts(wl, layer, ids)
 
 
 def bf16_tensor(bits: np.ndarray, device: str = "cuda") -> torch.Tensor:

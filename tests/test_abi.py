@@ -97,5 +97,11 @@ def test_null_handle_is_rejected():
     assert L.moe_route(None, None, 1, None, None, None, None, None) == m.MOE_ERR_INVALID_ARG
     assert L.moe_forward(None, None, 1, None, None, None, None, None) == m.MOE_ERR_INVALID_ARG
     assert L.moe_sync(None, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_destroy(None) == m.MOE_ERR_INVALID_ARG
     assert L.moe_layer_destroy(None) == m.MOE_ERR_INVALID_ARG
+    buf = (C.c_uint16 * 8)()
+    assert L.moe_stack_forward_host(None, 1, buf, 1, C.c_float(1e-6), buf, None) == m.MOE_ERR_INVALID_ARG
+    arr = (C.c_void_p * 1)(None)
+    assert L.moe_stack_forward_host(arr, 1, buf, 1, C.c_float(1e-6), buf, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_stack_forward_host(arr, 0, buf, 1, C.c_float(1e-6), buf, None) == m.MOE_ERR_INVALID_ARG
     assert L.moe_rmsnorm(None, 1, 100, 1e-6, None, None) == m.MOE_ERR_INVALID_ARG  # H % 8

@@ -246,6 +246,85 @@ def test_expert_id_out_of_range_is_reported_and_recovers(path):
     L.close()
 
 
+@pytest.mark.parametrize("T", [37, 130])
+def test_wait_that_gives_up_is_reported_and_recovers(T):
+    """MOE_OPT_WAIT_LIMIT = 0: every pipeline wait of the tensor-core GEMMs gives
+    up at once.  The call ends (each kernel lets its issued copies and MMAs
+    finish, frees its tensor memory and returns), moe_sync reports
+    MOE_ERR_TIMEOUT, and the next call with the default limit matches the
+    oracle.  37 tokens: gathered 16-token tiles with the combine in the down
+    GEMM; 130 tokens: 64-token tiles and the separate combine."""
+    wl = SMALL[1].with_tokens(T)
+    L, _ = gu.make_layer(wl)
+    L.set_option(m.MOE_OPT_PATH, m.PATH_MMA)
+    x = _x(wl)
+    idx, w = _oracle_routing(wl, x)
+    xt = sg.bf16_tensor(x)
+    it = torch.from_numpy(idx).to(gu.DEV)
+    wt = torch.from_numpy(w.astype(np.float32)).to(gu.DEV)
+    y = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    for call in ("forward", "step"):
+        L.set_option(m.MOE_OPT_WAIT_LIMIT, 0)
+        if call == "forward":
+            L.forward(xt, T, it, wt, y)
+        else:
+            L.step(xt, T, y)
+        assert L.sync() == m.MOE_ERR_TIMEOUT, call
+        assert L.sync() == m.MOE_OK, call  # the error word is cleared
+        L.set_option(m.MOE_OPT_WAIT_LIMIT, m.WAIT_LIMIT_DEFAULT)
+        gu.assert_y_close(gu.run_forward(L, x, idx, w), gu.oracle_layer(wl, 0, x, idx, w), what=call)
+    for bad in (-1, 1 << 31):
+        with pytest.raises(m.MoeError) as e:
+            L.set_option(m.MOE_OPT_WAIT_LIMIT, bad)
+        assert e.value.status == m.MOE_ERR_INVALID_ARG
+    L.close()
+
+
+@pytest.mark.parametrize("norm_eps", [1e-6, -1.0])
+def test_stack_forward_host_matches_device_loop_and_oracle(norm_eps):
+    """moe_stack_forward_host over three layers (host x in, host y out) gives
+    the same bits as the device loop of moe_rmsnorm + moe_step (or moe_step
+    alone without normalisation), and each layer of that loop matches the
+    oracle given its input (teacher forcing)."""
+    base = SMALL[1]
+    wls = [Workload(f"stack_l{i}", base.hidden, base.inter, base.n_experts, base.top_k, base.n_shared,
+                    base.tokens, seed=30 + i, scale_lo=-6, scale_hi=-2) for i in range(3)]
+    T, H = base.tokens, base.hidden
+    Ls = [gu.make_layer(wl)[0] for wl in wls]
+    x0 = _x(base, stream=7)
+    cur = x0
+    for wl, L in zip(wls, Ls):
+        if norm_eps >= 0:
+            xn_t = torch.empty((T, H), dtype=torch.int16, device=gu.DEV)
+            m.moe_rmsnorm(sg.bf16_tensor(cur), T, H, norm_eps, xn_t)
+            torch.cuda.synchronize()
+            xin = xn_t.cpu().numpy().view(np.uint16)
+        else:
+            xin = cur
+        y = torch.empty((T, H), dtype=torch.int16, device=gu.DEV)
+        lo = torch.empty((T, wl.n_experts), dtype=torch.float32, device=gu.DEV)
+        L.step(sg.bf16_tensor(xin), T, y, residual=sg.bf16_tensor(cur), logits_out=lo)
+        assert L.sync() == m.MOE_OK
+        ridx, rw = oracle.topk(lo.cpu().numpy(), wl.top_k)
+        yb = y.cpu().numpy().view(np.uint16)
+        gu.assert_y_close(yb, gu.oracle_layer(wl, 0, xin, ridx, rw, residual=cur), what=wl.name)
+        cur = yb
+    xh = torch.from_numpy(x0.view(np.int16).copy()).pin_memory()
+    yh = torch.empty(xh.shape, dtype=torch.int16).pin_memory()
+    for _ in range(2):
+        yh.fill_(0)
+        m.moe_stack_forward_host(Ls, xh, T, norm_eps, yh)
+        assert np.array_equal(yh.numpy().view(np.uint16), cur)
+    # a layer whose hidden size differs is refused before anything runs
+    other, _ = gu.make_layer(TINY)
+    with pytest.raises(m.MoeError) as e:
+        m.moe_stack_forward_host([Ls[0], other], xh, T, norm_eps, yh)
+    assert e.value.status == m.MOE_ERR_INVALID_ARG
+    other.close()
+    for L in Ls:
+        L.close()
+
+
 def test_fault_injection_launch_and_arg(monkeypatch):
     wl = TINY
     L, _ = gu.make_layer(wl)
