@@ -445,8 +445,11 @@ bool use_mma(const moe_layer* L, int T) {
 bool act4_of(const moe_layer* L) { return L->act_format == MOE_ACT_FP4; }
 
 // gate/up, down and combine on the tensor cores, once the segments and the
-// activation codes are in the workspace.
-moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool gather, const float* w,
+// activation codes are in the workspace.  small: up to kPrepMaxTokens tokens
+// after the preparation kernel (token-major codes, every expert in one tile):
+// gate/up reads all tokens' codes (dense) and, with shared experts, the down
+// GEMM does the combine.
+moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool small, const float* w,
                     const void* residual, void* y, cudaStream_t st) {
   const moe_config& c = L->cfg;
   const ExpertBank bank = bank_of(L);
@@ -454,22 +457,25 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool gather, const float* w
   cudaError_t e;
   {
     TimedScope ts(L, st, "ffn_up_mma");
-    e = launch_ffn_mma(*L->maps, bank, 0, bn, gather, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles,
+    e = launch_ffn_mma(*L->maps, bank, 0, bn, small ? T : 0, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles,
                        L->wait_limit);
   }
   if (e != cudaSuccess) return cuda_fail(e);
-  if (gather && c.n_shared > 0) {
-    // small batch: the combine runs inside the down GEMM (every token has a
-    // shared-expert position, so every y row has a last writer)
+  if (small && bn == 16 && c.n_shared > 0) {
+    // up to 16 tokens: the combine runs inside the down GEMM (every token has a
+    // shared-expert position, so every y row has a last writer).  With wider
+    // tiles a unit is the last writer of up to 64 tokens, whose combines one
+    // warp would do one after the other; the combine kernel does them in
+    // parallel instead.
     const CombineArgs cmb{T, c.top_k, c.n_shared, w, static_cast<const uint16_t*>(residual),
                           static_cast<uint16_t*>(y)};
     TimedScope ts(L, st, "ffn_down_mma");
-    return cuda_fail(launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, &cmb, act4_of(L), ns_tiles,
+    return cuda_fail(launch_ffn_mma(*L->maps, bank, 1, bn, 0, L->ws, L->num_sms, st, &cmb, act4_of(L), ns_tiles,
                                     L->wait_limit));
   }
   {
     TimedScope ts(L, st, "ffn_down_mma");
-    e = launch_ffn_mma(*L->maps, bank, 1, bn, false, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles,
+    e = launch_ffn_mma(*L->maps, bank, 1, bn, 0, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles,
                        L->wait_limit);
   }
   if (e != cudaSuccess) return cuda_fail(e);

@@ -88,6 +88,7 @@ struct FormatMaps {
   CUtensorMap gu_pair, s_gu_pair;  // gate + up as one 4-D tensor (when possible)
   int merged[2], swap_gu[2];
   CUtensorMap xg[3], hq[3];  // per token tile width: 16, 64, 112
+  CUtensorMap xq[4];         // dense gate/up: the token-major codes, 16, 32, 48 or 64 rows per copy
   int ch_up, ch_down;
   bool ok;
   bool shared_fp8;  // the shared maps read FP8 (32 x 32 block) weights
@@ -99,11 +100,12 @@ struct MmaMaps {
 
 static int bn_index(int bn) { return bn == 16 ? 0 : (bn == 64 ? 1 : 2); }
 
-// Token tile width: 16 for decode, 64 below 512 tokens, else 112 — the widest
-// N for which the gate/up kernel's two accumulators fit TMEM twice (2 x 2 x
-// 112 columns + the stages' scale factors <= 512), so the epilogue of one unit
-// overlaps the MMAs of the next.
-int mma_tile_for_tokens(int T) { return T <= 64 ? 16 : (T < 512 ? 64 : 112); }
+// Token tile width: 16 up to 16 tokens, 64 below 512 tokens (up to 64 tokens
+// every expert's slots fit one tile, so its weights stream once), else 112 —
+// the widest N for which the gate/up kernel's two accumulators fit TMEM twice
+// (2 x 2 x 112 columns + the stages' scale factors <= 512), so the epilogue of
+// one unit overlaps the MMAs of the next.
+int mma_tile_for_tokens(int T) { return T <= 16 ? 16 : (T < 512 ? 64 : 112); }
 
 // a4: packed operands (the FP4-activation variant): a chunk is 128 bytes of
 // a row, 256 elements, one per stage; rows of K elements are K/2 bytes for
@@ -137,6 +139,8 @@ static bool format_maps(FormatMaps* m, bool a4, const moe_config& c, const moe_w
   for (int i = 0; ok && i < 3; ++i)
     ok = map_3d(&m->xg[i], false, ws.xg, xk, P, bns[i], m->ch_up) &&
          map_3d(&m->hq[i], false, ws.hq, hk, P, bns[i], m->ch_down);
+  const uint64_t T = (uint64_t)c.max_tokens;
+  for (int i = 0; ok && i < 4; ++i) ok = map_3d(&m->xq[i], false, ws.xq, xk, T, 16 * (i + 1), m->ch_up);
   m->ok = ok;
   return ok;
 }
@@ -172,7 +176,7 @@ MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Worksp
 
 void mma_maps_destroy(MmaMaps* m) { delete m; }
 
-cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, int bn, bool gather,
+cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, int bn, int dense_T,
                            const Workspace& ws, int num_sms, cudaStream_t st, const CombineArgs* cmb, bool act4,
                            int ns_tiles, uint32_t wait_limit) {
   const FormatMaps& mm = maps.f[act4 ? 1 : 0];
@@ -194,15 +198,21 @@ cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, 
       p.swap_gu[i] = mm.swap_gu[i];
     }
     p.b = mm.xg[bi];
+    p.b_rows = bn;
     p.sa_routed[0] = bk.gs;
     p.sa_routed[1] = bk.us;
     p.sa_shared[0] = bk.sgs;
     p.sa_shared[1] = bk.sus;
     p.sb = ws.xgs;
-    if (gather && bn == 16) {  // activations by token: codes xq, scales xs
-      p.gather = 1;
+    if (dense_T > 0) {
+      // every token's codes (token-major xq / xs), T rounded up to 16 rows per copy
+      const int r16 = (dense_T + 15) / 16;
+      if (r16 > 4 || 16 * r16 > bn) return cudaErrorInvalidValue;
+      p.dense = 1;
+      p.T = dense_T;
+      p.b = mm.xq[r16 - 1];
+      p.b_rows = 16 * r16;
       p.wait_tiles = 1;  // launched right after the preparation kernel
-      p.xq = ws.xq;
       p.pos_tok = ws.pos_tok;
       p.sb = ws.xs;
     }
@@ -214,6 +224,7 @@ cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, 
     p.a_routed[0] = mm.down;
     p.a_shared[0] = mm.s_down;
     p.b = mm.hq[bi];
+    p.b_rows = bn;
     p.sa_routed[0] = bk.ds;
     p.sa_shared[0] = bk.sds;
     p.sb = ws.hs;
@@ -235,6 +246,7 @@ cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, 
   p.err = ws.err;
   if (mode == kModeDown && cmb && bn <= 64) {
     p.fuse_combine = 1;
+    p.shared_first = 1;
     p.T = cmb->T;
     p.k = cmb->k;
     p.ns = cmb->ns;

@@ -59,19 +59,20 @@ struct MmaParams {
   float* part;               // split partition: fp32 partial tiles, 2 slots per CTA
   int32_t* cnt;              // split partition: pieces finished per (unit, row quadrant)
   int split_ok;              // part/cnt are large enough for this launch
-  int gather;                // up mode, BN 16: activation rows gathered by token from xq
+  int dense;                 // up mode, T <= 64: B = the codes of all tokens (token-major), read by TMA
+  int b_rows;                // activation rows one B copy brings (dense: T rounded up to 16; else BN)
   int fuse_combine;          // down mode, BN <= 64: the last writer of a token's rows combines them
-  int T, k, ns;              // fuse_combine: tokens, top-k, shared experts
+  int T, k, ns;              // tokens (dense, fuse_combine), top-k, shared experts (fuse_combine)
   const int32_t* slot_pos;   // fuse_combine: position of slot t*k + j (-1: invalid id)
   const float* w;            // fuse_combine: combine weights [T][k]
   const uint16_t* res;       // fuse_combine: bf16 residual [T][H] or null
   uint16_t* y;               // fuse_combine: bf16 output [T][H]
   int32_t* comb_cnt;         // fuse_combine: writers finished per (token, 128-row tile, quadrant)
-  const uint8_t* xq;         // gather: E4M3 codes of x by token, [T][K]
-  const int32_t* pos_tok;    // gather: token of each position
+  const int32_t* pos_tok;    // dense, fuse_combine: token of each position
   int shared_fp8;            // shared experts in FP8 (E4M3, one scale per 32 x 32 block)
   uint32_t wait_limit;       // polls after which a pipeline wait gives up (then the error word)
   int ns_tiles;              // token tiles of the shared experts (the last ones of the table)
+  int shared_first;          // process the shared experts' tiles first (fuse_combine: see the kernel)
   int32_t* err;
 };
 
@@ -110,8 +111,13 @@ struct Cfg {
   static constexpr bool kRagged = BN == 112;
   static constexpr int kAccCols = (MODE == kModeUp || kSplitK ? 2 : 1) * BN;  // g, u (up); o (down)
   static constexpr int kNAcc = (MODE == kModeUp && BN >= 128) ? 1 : 2;
-  static constexpr int kStage = kNA * kATile + kBTile;  // shared memory of one ring stage
-  static constexpr int kStageCap0 = (kSmemBudget - 1024) / kStage;
+  // 64-token gate/up: the activation tiles get a ring of their own (two
+  // slots), so that three 64 KB weight stages still fit next to them; the
+  // weight bytes in flight, not the activations (read from L2), set the pace.
+  static constexpr bool kSepB = MODE == kModeUp && BN == 64 && !A4 && CH == 2;
+  static constexpr int kBRing = kSepB ? 2 : 0;
+  static constexpr int kStage = kNA * kATile + (kSepB ? 0 : kBTile);  // shared memory of one ring stage
+  static constexpr int kStageCap0 = (kSmemBudget - 1024 - kBRing * kBTile) / kStage;
   static constexpr int kStageCap = kStageCap0 < kMaxStages ? kStageCap0 : kMaxStages;
   // Scale factors in TMEM, per stage: 4 columns per (weight matrix, chunk),
   // then per chunk the token scales (group of 32 tokens g at column g); with
@@ -141,7 +147,7 @@ void geometry(int K, int* n_stages, int* smem) {
   using C = Cfg<MODE, BN, CH, A4>;
   (void)K;
   *n_stages = C::kStages;
-  *smem = 1024 + C::kStages * C::kStage;
+  *smem = 1024 + C::kStages * C::kStage + C::kBRing * C::kBTile;
 }
 
 struct Unit {
@@ -149,11 +155,16 @@ struct Unit {
 };
 
 // Unit u -> (token tile v, 128-row tile); row tiles innermost so consecutive
-// units share the activation tile.
-__device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_units) {
-  const int v = u / mt_units;
+// units share the activation tile.  rot: the units start at tile rot of the
+// table and wrap around (n_tiles tiles in all).
+__device__ __forceinline__ int tile_of(int u, int mt_units, int rot, int n_tiles) {
+  const int v = u / mt_units + rot;
+  return v >= n_tiles ? v - n_tiles : v;
+}
+__device__ __forceinline__ Unit decode_unit(const MmaParams& p, int u, int mt_units, int rot, int n_tiles) {
+  const int v = tile_of(u, mt_units, rot, n_tiles);
   const int4 t = __ldg(p.tile_info + v);
-  const int r = u - v * mt_units;
+  const int r = u - (u / mt_units) * mt_units;
   return Unit{t.x, t.y, t.z, r * 128};
 }
 
@@ -259,6 +270,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full_bar[kMaxStages], sf_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar[2];
+  __shared__ __align__(8) uint64_t bfull_bar[2], bempty_bar[2];  // the separate B ring (kSepB)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -267,15 +279,23 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   const int k_stages = p.K / (C::kKC * CH);
   const int NS = p.n_stages;
   uint8_t* stage_base = smem;
-  const int stage_bytes = NA * C::kATile + C::kBTile;
-  // Gather mode (gate/up at 16-token tiles, i.e. decode): the scale-factor
-  // warps copy each position's activation row from the per-token codes into
-  // the stage (swizzled like a TMA tile), so no slot-ordered copy of x exists.
-  constexpr bool kGatherCapable = MODE == kModeUp && BN == 16;
-  const bool gather = kGatherCapable && p.gather;
+  constexpr bool kSepB = C::kSepB;
+  const int stage_bytes = C::kStage;
+  uint8_t* bring_base = smem + NS * stage_bytes;  // kSepB: the B ring after the weight stages
+  // Dense mode (gate/up for up to 64 tokens): B is the codes of all T tokens,
+  // token-major as the preparation kernel wrote them, b_rows = T rounded up to
+  // 16 rows by one TMA copy per stage; every expert's unit multiplies them all
+  // (an MMA costs about the same at N = 16 and N = 64) and the epilogue reads
+  // the accumulator columns of the unit's own tokens.  No copy of x per slot
+  // is made and the expert's weights stream once.
+  const bool dense = MODE == kModeUp && p.dense;
+  const int BR = p.b_rows;  // activation rows per B tile (the MMA's N, except ragged tiles)
   // bytes a stage's copies bring: the weights packed (FP4: 64 bytes per
-  // 128-element chunk row, unpacked into 128; A4: 128 bytes, stored as is)
-  const uint32_t tx_stage = NA * 128 * (A4 ? 128 : 64) * CH + (gather ? 0 : BN * 128 * CH);
+  // 128-element chunk row, unpacked into 128; A4: 128 bytes, stored as is),
+  // and the activation rows
+  const uint32_t tx_a = NA * 128 * (A4 ? 128 : 64) * CH;
+  const uint32_t tx_b = (uint32_t)BR * 128 * CH;
+  const uint32_t tx_stage = tx_a + (kSepB ? 0 : tx_b);
   const uint32_t sf_col0 = C::kNAcc * C::kAccCols;
 
   if (threadIdx.x == 0) {
@@ -296,6 +316,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       mbar_init(&accf_bar[b], 2);
       mbar_init(&acce_bar[b], 4);
       mbar_init(&drain_bar[b], 1);
+      mbar_init(&bfull_bar[b], 1);
+      mbar_init(&bempty_bar[b], 2);
     }
     abort_flag = 0;
     fence_barrier_init();
@@ -316,7 +338,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   const int total = p.n_active[1] * mt_units;
   // FP8 shared experts: their tiles close the table, so a unit's format follows
   // from its index (no tile-table load on the issuing thread)
-  const int shared_tile0 = (!A4 && p.shared_fp8) ? p.n_active[1] - p.ns_tiles : 0x7FFFFFFF;
+  const int n_tiles = p.n_active[1];
+  const int shared_tile0 = (!A4 && p.shared_fp8) ? n_tiles - p.ns_tiles : 0x7FFFFFFF;
+  // With the combine fused into the down GEMM, whichever unit writes a token's
+  // last output row does that token's combine.  The shared experts' tiles hold
+  // every token, so they go first: the last writers are then routed units
+  // spread over the launch, not the last few units holding all the tokens.
+  const int rot = p.shared_first ? n_tiles - p.ns_tiles : 0;
+  auto shared_fp8_unit = [&](int u) { return tile_of(u, mt_units, rot, n_tiles) >= shared_tile0; };
   const Sched sc0(total, k_stages, BN <= 64 && p.split_ok, (int)blockIdx.x, (int)gridDim.x);
 
   auto give_up = [&]() {
@@ -329,18 +358,29 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       uint32_t g = 0;
-      int last_parity[kMaxStages];
+      int last_parity[kMaxStages], last_bparity[2] = {-1, -1};
       int deferred_pos[kMaxStages], deferred_s[kMaxStages], n_deferred = 0;
-      bool waited = gather;  // gather mode: the TMA warp loads weights only
-      // the activation tile of a stage, one op
-      auto load_b = [&](int slot, int pos0, int st) {
-        tma_load_3d(stage_base + slot * stage_bytes + NA * C::kATile, &p.b, 0, pos0, st * CH, &full_bar[slot]);
+      // dense mode runs after the preparation kernel and waited for it above
+      bool waited = dense;
+      // B copies issued before the previous kernel is waited for: as many as
+      // there are slots to hold them
+      const uint32_t defer_cap = kSepB ? 2u : (uint32_t)NS;
+      // the activation tile of stage g (slot i: the stage's own area, or the
+      // B ring's slot), one op; dense: rows 0.. of the token-major codes
+      auto load_b = [&](int i, int pos0, int st) {
+        const int row = dense ? 0 : pos0;
+        if constexpr (kSepB) {
+          mbar_expect_tx(&bfull_bar[i], tx_b);
+          tma_load_3d(bring_base + i * C::kBTile, &p.b, 0, row, st * CH, &bfull_bar[i]);
+        } else {
+          tma_load_3d(stage_base + i * stage_bytes + NA * C::kATile, &p.b, 0, row, st * CH, &full_bar[i]);
+        }
       };
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
       Sched sc = sc0;
       for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next()) {
-        const Unit un = decode_unit(p, pc.u, mt_units);
+        const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
         const bool sh = un.e >= p.E;
         const int erow = (sh ? un.e - p.E : un.e) * p.rows + un.row0;
         bool ok = true;
@@ -348,7 +388,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         for (int s = pc.s0; s < s_end; ++s, ++g) {
           const int slot = g % NS;
           const uint32_t ph = (g / NS) & 1;
-          if (!waited && g >= (uint32_t)NS) {
+          if (!waited && g >= defer_cap) {
             // ring full: wait for the previous kernel, then load the deferred activations
             pdl_wait();
             waited = true;
@@ -357,7 +397,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, p.wait_limit)) { give_up(); ok = false; break; }
           uint8_t* sa = stage_base + slot * stage_bytes;
           // FP8 shared weights arrive as bytes: twice the packed FP4 count
-          mbar_expect_tx(&full_bar[slot], tx_stage + (pc.u / mt_units >= shared_tile0 ? NA * 128 * 64 * CH : 0));
+          mbar_expect_tx(&full_bar[slot], tx_stage + (shared_fp8_unit(pc.u) ? NA * 128 * 64 * CH : 0));
           if (NA == 2 && p.merged[sh]) {
             // gate and up rows of the stage in one op: {chunk elems, rows, chunks, matrix}
             tma_load_4d(sa, sh ? &p.a_shared[0] : &p.a_routed[0], 0, erow, s * CH, 0, &full_bar[slot]);
@@ -367,13 +407,19 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
               tma_load_3d(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
                           &full_bar[slot]);
           }
-          if (gather) {
-            // activations come from the scale-factor warps
-          } else if (waited) {
-            load_b(slot, un.pos0, s);
+          if (waited) {
+            if constexpr (kSepB) {
+              const int bs = (int)(g & 1u);
+              if (!mbar_wait(&bempty_bar[bs], ((g >> 1) & 1u) ^ 1u, p.wait_limit)) { give_up(); ok = false; break; }
+              load_b(bs, un.pos0, s);
+              last_bparity[bs] = (int)((g >> 1) & 1u);
+            } else {
+              load_b(slot, un.pos0, s);
+            }
           } else {
-            deferred_pos[n_deferred] = un.pos0;  // slot == n_deferred while g < NS
+            deferred_pos[n_deferred] = un.pos0;  // the B slot is n_deferred while g < defer_cap
             deferred_s[n_deferred++] = s;
+            if constexpr (kSepB) last_bparity[n_deferred - 1] = 0;
           }
 #pragma unroll
           for (int i = 0; i < kMaxStages; ++i)
@@ -389,6 +435,10 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s)
         if (last_parity[s] >= 0) mbar_wait(&full_bar[s], (uint32_t)last_parity[s], kDrainLimit);
+      if constexpr (kSepB) {
+        for (int i = 0; i < 2; ++i)
+          if (last_bparity[i] >= 0) mbar_wait(&bfull_bar[i], (uint32_t)last_bparity[i], kDrainLimit);
+      }
     }
   } else if (warp == 1 || warp == kIssuer2Warp) {
     // ---------------------------------------------------------------- MMA
@@ -399,7 +449,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // MMAs, so the empty and accumulator-full barriers count two arrivals.
     if (lane == 0) {
       const int j = warp == 1 ? 0 : 1;
-      const int NI0 = BN;  // N of the MMAs (the tile's tokens for the ragged wide tiles)
+      // N of the MMAs: the B rows (dense: all tokens), or per unit the tile's
+      // tokens for the ragged wide tiles
+      const int NI0 = BR;
       uint32_t g = 0, it = 0;
       Sched sc = sc0;
       for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
@@ -410,7 +462,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         const uint32_t d_tmem = tmem + buf * C::kAccCols;
         int swap = 0, NI = NI0;
         if (NA == 2 || C::kRagged) {
-          const Unit un = decode_unit(p, pc.u, mt_units);
+          const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
           const int sh = un.e >= p.E;
           if (NA == 2) swap = p.merged[sh] && p.swap_gu[sh];
           if (C::kRagged) {
@@ -422,21 +474,23 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           }
         }
         uint32_t idesc_base = A4 ? idesc_e2m1_e2m1(128, NI, 0) : idesc_e2m1_e4m3(128, NI, 0);
-        if (pc.u / mt_units >= shared_tile0) idesc_base &= ~(7u << 7);  // A = E4M3 (FP8 shared expert)
+        if (shared_fp8_unit(pc.u)) idesc_base &= ~(7u << 7);  // A = E4M3 (FP8 shared expert)
         bool ok = true;
         const int s_beg = pc.s0, s_end = pc.s1;
         for (int s = s_beg; s < s_end; ++s, ++g) {
           const int slot = g % NS;
           const uint32_t ph = (g / NS) & 1;
-          if (!mbar_wait(&full_bar[slot], ph, p.wait_limit) || !mbar_wait(&sf_bar[slot], ph, p.wait_limit)) {
+          if (!mbar_wait(&full_bar[slot], ph, p.wait_limit) || !mbar_wait(&sf_bar[slot], ph, p.wait_limit) ||
+              (kSepB && !mbar_wait(&bfull_bar[g & 1u], (g >> 1) & 1u, p.wait_limit))) {
             give_up();
             ok = false;
             break;
           }
           fence_after();
           const uint32_t sa = smem_u32(stage_base + slot * stage_bytes);
+          const uint32_t sb_addr = kSepB ? smem_u32(bring_base + (g & 1u) * C::kBTile) : sa + NA * C::kATile;
           // descriptors differ only in the start-address field (bits 0..13, address / 16)
-          const uint64_t a_desc0 = sw128_desc(sa), b_desc0 = sw128_desc(sa + NA * C::kATile);
+          const uint64_t a_desc0 = sw128_desc(sa), b_desc0 = sw128_desc(sb_addr);
           const uint32_t sf = tmem + sf_col0 + slot * C::kSfCols;
 #pragma unroll
           for (int c = 0; c < CH; ++c)
@@ -448,7 +502,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
               const int w = A4 ? k >> 1 : 0;
               const uint32_t sfid = A4 ? (uint32_t)(k & 1) * 2u : (uint32_t)k;
               const uint32_t idesc = idesc_base | (sfid << 4) | (sfid << 29);
-              const uint64_t bdesc = b_desc0 + (uint64_t)((c * BN * 128 + 32 * k) >> 4);
+              // chunk c of the B tile starts after c chunks of BR rows of 128 bytes
+              const uint64_t bdesc = b_desc0 + (uint64_t)((c * BR * 128 + 32 * k) >> 4);
               const uint32_t sfb = sf + C::sfb_col(c, w, 0);
               auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfbb, uint32_t accumulate) {
                 if constexpr (A4)
@@ -469,6 +524,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
               }
             }
           mma_commit(&empty_bar[slot]);
+          if constexpr (kSepB) mma_commit(&bempty_bar[g & 1u]);
         }
         if (!ok) break;
         mma_commit(&accf_bar[buf]);
@@ -486,14 +542,13 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // registers), so a global-load latency is paid per NB stages.
     constexpr int KW = C::kW;                                    // scale words per row and chunk
     constexpr int NB = 4, NW = (NA * CH + NC * CH) * KW;  // words per stage
-    constexpr int BCH = kGatherCapable ? CH : 1;   // gathered 16-byte granules per stage
     const int q = warp & 3;
     pdl_wait();  // the activation scales come from the previous kernel
     uint32_t g = 0;
     bool ok = true;
     Sched sc = sc0;
     for (Piece pc = sc.next(); ok && pc.u >= 0 && !aborted(); pc = sc.next()) {
-      const Unit un = decode_unit(p, pc.u, mt_units);
+      const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
       const int s_end = pc.s1;
       const bool sh = un.e >= p.E;
       const size_t erow = (size_t)(sh ? un.e - p.E : un.e) * p.rows + un.row0 + 32 * q + lane;
@@ -502,36 +557,17 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       for (int m = 0; m < NA; ++m)
         sa_row[m] = (sh ? p.sa_shared[m] : p.sa_routed[m]) +
                     // FP8 shared: one scale per 32 x 32 block, shared by the warp's 32 rows
-                    (pc.u / mt_units >= shared_tile0 ? (erow >> 5) : erow) * (p.K / 32);
+                    (shared_fp8_unit(pc.u) ? (erow >> 5) : erow) * (p.K / 32);
+      // the scale row of B column n: dense, token n (all T tokens); else the
+      // unit's position pos0 + n.  Columns without one get 2^0.
       const uint8_t* sb_row[NC];
 #pragma unroll
       for (int cb = 0; cb < NC; ++cb) {
         const int n = lane + 32 * cb;
         sb_row[cb] = nullptr;
-        if (n < un.m_tile) {
-          const size_t row = gather ? (size_t)p.pos_tok[un.pos0 + n] : (size_t)(un.pos0 + n);
-          sb_row[cb] = p.sb + row * (p.K / 32);
-        }
+        if (dense ? n < p.T : n < un.m_tile) sb_row[cb] = p.sb + (size_t)(dense ? n : un.pos0 + n) * (p.K / 32);
       }
-      // gather: this thread copies 16-byte granule bg of activation row br of
-      // every chunk (128 threads x 2 chunks = the 16 x 256-byte B stage)
-      const int br = (32 * q + lane) >> 3, bg = lane & 7;
-      const uint8_t* xrow = nullptr;
-      if (gather && br < un.m_tile) xrow = p.xq + (size_t)p.pos_tok[un.pos0 + br] * (p.K / (A4 ? 2 : 1)) + bg * 16;
-      const int b_off = NA * C::kATile + br * 128 + ((bg ^ (br & 7)) << 4);  // 128-byte swizzle
-      auto load_b = [&](uint4 (&bw)[NB][BCH], int s0) {
-        if constexpr (kGatherCapable) {
-#pragma unroll
-          for (int i = 0; i < NB; ++i)
-#pragma unroll
-            for (int c = 0; c < BCH; ++c)
-              bw[i][c] = (xrow && s0 + i < s_end)
-                             ? __ldg(reinterpret_cast<const uint4*>(xrow + ((s0 + i) * CH + c) * 128))
-                             : make_uint4(0u, 0u, 0u, 0u);
-        }
-      };
-      // the weight scales first: their addresses do not wait for the token
-      // positions that the activation rows need
+      // the weight scales first: their addresses are known before the token ones
       auto load = [&](uint32_t (&w)[NB][NW], int s0) {
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
@@ -563,7 +599,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           }
         }
       };
-      auto store = [&](const uint32_t (&w)[NB][NW], const uint4 (&bw)[NB][BCH], int s0) -> bool {
+      auto store = [&](const uint32_t (&w)[NB][NW], int s0) -> bool {
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
           if (s0 + i >= s_end) break;
@@ -571,14 +607,6 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           const uint32_t ph = (g / NS) & 1;
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, p.wait_limit)) { give_up(); return false; }
           fence_after();
-          if constexpr (kGatherCapable) {
-            if (gather) {
-              uint8_t* dst = stage_base + slot * stage_bytes + b_off;
-#pragma unroll
-              for (int c = 0; c < BCH; ++c) *reinterpret_cast<uint4*>(dst + c * BN * 128) = bw[i][c];
-              fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
-            }
-          }
           const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + sf_col0 + slot * C::kSfCols;
 #pragma unroll
           for (int c = 0; c < CH; ++c)
@@ -599,21 +627,13 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         return true;
       };
       uint32_t w0[NB][NW], w1[NB][NW];
-      uint4 b0[NB][BCH], b1[NB][BCH];
       load(w0, pc.s0);
-      load_b(b0, pc.s0);
       for (int s0 = pc.s0; s0 < s_end; s0 += 2 * NB) {
-        if (s0 + NB < s_end) {
-          load(w1, s0 + NB);
-          load_b(b1, s0 + NB);
-        }
-        if (!(ok = store(w0, b0, s0))) break;
+        if (s0 + NB < s_end) load(w1, s0 + NB);
+        if (!(ok = store(w0, s0))) break;
         if (s0 + NB >= s_end) break;
-        if (s0 + 2 * NB < s_end) {
-          load(w0, s0 + 2 * NB);
-          load_b(b0, s0 + 2 * NB);
-        }
-        if (!(ok = store(w1, b1, s0 + NB))) break;
+        if (s0 + 2 * NB < s_end) load(w0, s0 + 2 * NB);
+        if (!(ok = store(w1, s0 + NB))) break;
       }
     }
   } else {
@@ -694,59 +714,82 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         __threadfence();
         __syncwarp();
         const int n_rt = p.out_cols / 128, rt = un.row0 / 128;
-        int done = -1;
-        if (lane < un.m_tile) {
-          const int t = p.pos_tok[un.pos0 + lane];
-          int sp[kMaxTopK];
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) sp[j] = j < p.k ? p.slot_pos[t * p.k + j] : -1;
-          int need = p.ns;
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) need += sp[j] >= 0;
-          if (atomicAdd(&p.comb_cnt[(t * n_rt + rt) * 4 + q], 1) == need - 1) done = t;
-        }
-        unsigned todo = __ballot_sync(0xFFFFFFFFu, done >= 0);
-        if (todo) __threadfence();
         const int row = un.row0 + rl;
         const size_t S = (size_t)p.T * p.k, H = (size_t)p.out_cols;
-        while (todo) {
-          const int t = __shfl_sync(0xFFFFFFFFu, done, __ffs(todo) - 1);
-          todo &= todo - 1;
-          // lane j < k holds slot j's position and weight; then every o load is in flight at once
-          const int my_pp = lane < p.k ? p.slot_pos[t * p.k + lane] : -1;
-          const float my_w = lane < p.k ? p.w[t * p.k + lane] : 0.f;
-          float osh[kMaxShared], ov[kMaxTopK];
+        // the unit's positions 32 at a time, lane i0 + lane counting its token
+        for (int i0 = 0; i0 < un.m_tile; i0 += 32) {
+          int done = -1;
+          if (i0 + lane < un.m_tile) {
+            const int t = p.pos_tok[un.pos0 + i0 + lane];
+            int sp[kMaxTopK];
 #pragma unroll
-          for (int j = 0; j < kMaxShared; ++j)
-            osh[j] = j < p.ns ? __ldcg(p.o + (S + (size_t)j * p.T + t) * H + row) : 0.f;
+            for (int j = 0; j < kMaxTopK; ++j) sp[j] = j < p.k ? p.slot_pos[t * p.k + j] : -1;
+            int need = p.ns;
 #pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) {
-            const int pp = __shfl_sync(0xFFFFFFFFu, my_pp, j);
-            ov[j] = pp >= 0 ? __ldcg(p.o + (size_t)pp * H + row) : 0.f;
+            for (int j = 0; j < kMaxTopK; ++j) need += sp[j] >= 0;
+            if (atomicAdd(&p.comb_cnt[(t * n_rt + rt) * 4 + q], 1) == need - 1) done = t;
           }
-          // the combine's fixed order: shared experts, then slots j = 0..k-1
-          float acc = 0.f;
+          unsigned todo = __ballot_sync(0xFFFFFFFFu, done >= 0);
+          if (todo) __threadfence();
+          while (todo) {
+            const int t = __shfl_sync(0xFFFFFFFFu, done, __ffs(todo) - 1);
+            todo &= todo - 1;
+            // lane j < k holds slot j's position and weight; then every o load is in flight at once
+            const int my_pp = lane < p.k ? p.slot_pos[t * p.k + lane] : -1;
+            const float my_w = lane < p.k ? p.w[t * p.k + lane] : 0.f;
+            float osh[kMaxShared], ov[kMaxTopK];
 #pragma unroll
-          for (int j = 0; j < kMaxShared; ++j)
-            if (j < p.ns) acc += osh[j];
+            for (int j = 0; j < kMaxShared; ++j)
+              osh[j] = j < p.ns ? __ldcg(p.o + (S + (size_t)j * p.T + t) * H + row) : 0.f;
 #pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) {
-            const float wj = __shfl_sync(0xFFFFFFFFu, my_w, j);
-            if (__shfl_sync(0xFFFFFFFFu, my_pp, j) >= 0) acc = fmaf(wj, ov[j], acc);
+            for (int j = 0; j < kMaxTopK; ++j) {
+              const int pp = __shfl_sync(0xFFFFFFFFu, my_pp, j);
+              ov[j] = pp >= 0 ? __ldcg(p.o + (size_t)pp * H + row) : 0.f;
+            }
+            // the combine's fixed order: shared experts, then slots j = 0..k-1
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxShared; ++j)
+              if (j < p.ns) acc += osh[j];
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+              const float wj = __shfl_sync(0xFFFFFFFFu, my_w, j);
+              if (__shfl_sync(0xFFFFFFFFu, my_pp, j) >= 0) acc = fmaf(wj, ov[j], acc);
+            }
+            uint16_t yb = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+            if (p.res)
+              yb = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits_to_float(p.res[(size_t)t * H + row]) +
+                                                            bf16_bits_to_float(yb)));
+            p.y[(size_t)t * H + row] = yb;
           }
-          uint16_t yb = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-          if (p.res)
-            yb = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits_to_float(p.res[(size_t)t * H + row]) +
-                                                          bf16_bits_to_float(yb)));
-          p.y[(size_t)t * H + row] = yb;
         }
       }
     };
-    constexpr int kSlot = NA * BN * 128;  // floats per partial slot: [matrix][column][row]
+    constexpr int kSlot = NA * BN * 128;  // floats per partial slot: [matrix][position][row]
+    // The accumulator values of the unit's positions i0 .. i0 + 15 (matrix 0
+    // / the first K half in v, matrix 1 / the second K half in vu): in dense
+    // mode the column of each position's token, one column per load; else the
+    // positions are the columns.
+    auto load_cols = [&](const Unit& un, uint32_t t_base, int i0, uint32_t (&v)[16], uint32_t (&vu)[16]) {
+      constexpr bool kTwo = MODE == kModeUp || C::kSplitK;
+      if (dense) {
+        const int tok = (lane < 16 && i0 + lane < un.m_tile) ? p.pos_tok[un.pos0 + i0 + lane] : 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t col = (uint32_t)__shfl_sync(0xFFFFFFFFu, tok, j);
+          tmem_ld1(t_base + col, v[j]);
+          if (kTwo) tmem_ld1(t_base + BN + col, vu[j]);
+        }
+      } else {
+        tmem_ld16(t_base + i0, v);
+        if (kTwo) tmem_ld16(t_base + BN + i0, vu);
+      }
+      tmem_ld_wait();
+    };
     uint32_t it = 0;
     Sched sc = sc0;
     for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
-      const Unit un = decode_unit(p, pc.u, mt_units);
+      const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
       const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
       const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
       if (!mbar_wait(&accf_bar[buf], ph_acc, p.wait_limit)) { give_up(); break; }
@@ -754,22 +797,20 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       const uint32_t t_base = tmem + ((uint32_t)(32 * q) << 16) + buf * C::kAccCols;
       int first, n;
       sc.pieces(pc.u, first, n);
+      // positions of the unit, in groups of 16
+      const int i_end = (un.m_tile + 15) & ~15;
       if (n == 1) {
-        // the whole unit: straight from TMEM to the outputs (the columns the
-        // MMAs wrote)
-        const int c_end = C::kRagged ? min(BN, (un.m_tile + 15) & ~15) : BN;
+        // the whole unit: straight from TMEM to the outputs
 #pragma unroll 1
-        for (int c = 0; c < c_end; c += 16) {
+        for (int i0 = 0; i0 < i_end; i0 += 16) {
           uint32_t v[16], vu[16];
-          tmem_ld16(t_base + c, v);
-          if (MODE == kModeUp || C::kSplitK) tmem_ld16(t_base + BN + c, vu);
-          tmem_ld_wait();
-          if (c + 16 >= c_end) {
+          load_cols(un, t_base, i0, v, vu);
+          if (i0 + 16 >= i_end) {
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce_bar[buf]);
           }
-          if (c < un.m_tile) emit16(un, c, v, vu);  // down split-K: the two K halves, in fixed order
+          emit16(un, i0, v, vu);  // down split-K: the two K halves, in fixed order
         }
         combine_tail(un);
         continue;
@@ -781,24 +822,22 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         // and quadrant) and no warp ever waits for another.
         float* mine = p.part + (size_t)sc.slot(pc.u, first, sc.cta - first) * kSlot;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
+        for (int i0 = 0; i0 < i_end; i0 += 16) {
           uint32_t v[16], vu[16];
-          tmem_ld16(t_base + c, v);
-          if (MODE == kModeUp || C::kSplitK) tmem_ld16(t_base + BN + c, vu);
-          tmem_ld_wait();
-          if (c + 16 >= BN) {
+          load_cols(un, t_base, i0, v, vu);
+          if (i0 + 16 >= i_end) {
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce_bar[buf]);
           }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (c + j >= un.m_tile) break;  // warp-uniform
+            if (i0 + j >= un.m_tile) break;  // warp-uniform
             if constexpr (C::kSplitK)
-              mine[(c + j) * 128 + rl] = __uint_as_float(v[j]) + __uint_as_float(vu[j]);
+              mine[(i0 + j) * 128 + rl] = __uint_as_float(v[j]) + __uint_as_float(vu[j]);
             else
-              mine[(c + j) * 128 + rl] = __uint_as_float(v[j]);
-            if (MODE == kModeUp) mine[(BN + c + j) * 128 + rl] = __uint_as_float(vu[j]);
+              mine[(i0 + j) * 128 + rl] = __uint_as_float(v[j]);
+            if (MODE == kModeUp) mine[(BN + i0 + j) * 128 + rl] = __uint_as_float(vu[j]);
           }
         }
         __threadfence();

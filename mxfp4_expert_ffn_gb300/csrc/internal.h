@@ -177,13 +177,14 @@ struct CombineArgs {
   const uint16_t* residual; // [T][H] or null
   uint16_t* y;              // [T][H]
 };
-// gather (gate/up at bn 16 only): activation rows are read by token from xq/xs
-// through pos_tok instead of from the slot-ordered copy xg/xgs.  cmb (down,
+// dense_T (gate/up, T <= 64 tokens, bn >= T): the activations are the codes of
+// all dense_T tokens, token-major (xq/xs), and each unit's epilogue reads its
+// own tokens' columns; 0: the slot-ordered copy xg/xgs by position.  cmb (down,
 // bn <= 64): the combine runs inside the down GEMM (needs T <= kPrepMaxTokens).
 // act4: the FP4-activation variant (xg/xq/hq hold packed E2M1 codes).
 // ns_tiles: token tiles of the shared experts (n_shared x ceil(T / bn)).
 // wait_limit: polls after which a pipeline wait gives up (MOE_OPT_WAIT_LIMIT).
-cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn, bool gather,
+cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn, int dense_T,
                            const Workspace& ws, int num_sms, cudaStream_t st,
                            const CombineArgs* cmb = nullptr, bool act4 = false, int ns_tiles = 0,
                            uint32_t wait_limit = 1u << 24);

@@ -56,7 +56,11 @@ STACK8_T64 = Workload("v41_stack8_decode_t64_zipf", tokens=64, seed=5, layers=8,
 # enough for an ncu capture with memory save/restore; not a benchmark line.
 NCU_DECODE_T1 = Workload("ncu_v41_e24_decode_t1", tokens=1, seed=6, **{**_V41, "n_experts": 24})
 NCU_PREFILL = Workload("ncu_v41_e24_prefill_t512", tokens=512, seed=7, **{**_V41, "n_experts": 24})
+# one layer of the decode stack's shape (64 tokens, Zipf(1.1) routing) with a 128-expert bank
+# (~2.4 GB): small enough for a full ncu capture; not a benchmark line.
+NCU_STACK_T64 = Workload("ncu_v41_e128_decode_t64_zipf", tokens=64, seed=12, zipf=1.1,
+                         **{**_V41, "n_experts": 128})
 
 WORKLOADS = {w.name: w for w in (TINY, DECODE_T1, VERIFY_T5, VERIFY_T32, MID_T256, PREFILL_T4096, PREFILL_T16K,
                                  PREFILL_T32K, PREFILL_T64K, STACK8_T64,
-                                 NCU_DECODE_T1, NCU_PREFILL)}
+                                 NCU_DECODE_T1, NCU_PREFILL, NCU_STACK_T64)}

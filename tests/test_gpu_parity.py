@@ -148,6 +148,8 @@ SPLIT = [
     Workload("split_up_h5120_i256_e8_k2_t3", 5120, 256, 8, 2, 1, 3, seed=21, scale_lo=-8, scale_hi=-4),
     Workload("split_down_h1024_i2304_e8_k2_t3", 1024, 2304, 8, 2, 1, 3, seed=22, scale_lo=-8, scale_hi=-4),
     Workload("split_both_h5120_i2304_e6_k1_t2", 5120, 2304, 6, 1, 1, 2, seed=23, scale_lo=-8, scale_hi=-4),
+    # 64-token tiles read by every token (40 tokens): pieces of units whose tile holds more than 32 slots
+    Workload("split_dense_h5120_i256_e4_k2_t40", 5120, 256, 4, 2, 1, 40, seed=27, scale_lo=-8, scale_hi=-4),
 ]
 
 
@@ -386,6 +388,8 @@ def test_prefill_tiles_match_oracle():
 
 STEP = SMALL + [
     Workload("step_h1024_i256_e64_k6_t64", 1024, 256, 64, 6, 1, 64, seed=24, scale_lo=-8, scale_hi=-4),
+    # up to 64 tokens with experts of more than 32 slots (one 64-token tile each) and two shared experts
+    Workload("step_h512_i256_e8_k4_s2_t60", 512, 256, 8, 4, 2, 60, seed=28, scale_lo=-8, scale_hi=-4),
     Workload("step_h512_i256_e32_k4_t80", 512, 256, 32, 4, 1, 80, seed=25, scale_lo=-8, scale_hi=-4),
 ]
 
@@ -602,6 +606,7 @@ ACT4 = [
     Workload("a4_h512_i256_e16_k6_t3", 512, 256, 16, 6, 1, 3, seed=41, scale_lo=-6, scale_hi=-2),
     Workload("a4_h512_i256_e32_k4_s2_t80", 512, 256, 32, 4, 2, 80, seed=42, scale_lo=-6, scale_hi=-2),
     Workload("a4_h512_i256_e16_k4_t600", 512, 256, 16, 4, 1, 600, seed=43, scale_lo=-8, scale_hi=-4),
+    Workload("a4_h512_i256_e8_k4_t48", 512, 256, 8, 4, 1, 48, seed=44, scale_lo=-6, scale_hi=-2),
     SPLIT[2],  # 5120 x 2304: the split partition on both GEMMs
 ]
 
@@ -654,6 +659,7 @@ FP8_SHARED = [
     Workload("s8_h512_i256_e16_k6_t3", 512, 256, 16, 6, 1, 3, seed=51, scale_lo=-6, scale_hi=-2),
     Workload("s8_h512_i256_e32_k4_s2_t80", 512, 256, 32, 4, 2, 80, seed=52, scale_lo=-6, scale_hi=-2),
     Workload("s8_h512_i256_e16_k4_t600", 512, 256, 16, 4, 1, 600, seed=53, scale_lo=-8, scale_hi=-4),
+    Workload("s8_h512_i256_e8_k4_t48", 512, 256, 8, 4, 1, 48, seed=54, scale_lo=-6, scale_hi=-2),
     SPLIT[2],
 ]
 
