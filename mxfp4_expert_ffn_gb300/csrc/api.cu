@@ -82,7 +82,7 @@ size_t carve(const moe_config& c, int num_sms, char* base, Workspace& ws) {
   // partial slots per CTA and one counter per (unit, row quadrant), units < 4 * SMs
   ws.part_bn = mma_tile_for_tokens(c.max_tokens) < 64 ? mma_tile_for_tokens(c.max_tokens) : 64;
   ws.part = cv.take<float>((size_t)2 * num_sms * 2 * ws.part_bn * 128);
-  ws.split_cnt_n = 2 * 16 * num_sms;
+  ws.split_cnt_n = 2 * 4 * kSplitUnitsPerCta * num_sms;
   ws.split_cnt = cv.take<int32_t>((size_t)ws.split_cnt_n);
   ws.prep_cnt = cv.take<int32_t>(16);
   ws.comb_cnt_n = kPrepMaxTokens * (int)(H / 128) * 4;
@@ -553,12 +553,23 @@ moe_status step_impl(moe_layer* L, const void* x, int32_t T, const void* residua
   if (!w) w = L->ws.w;
   if (use_mma(L, T) && T <= kPrepMaxTokens) {
     const int bn = mma_tile_for_tokens(T);
-    cudaError_t e;
+    cudaError_t e = cudaSuccess;
+    // above 8 tokens the router's partial sums and the codes of x come from a
+    // register-tiled launch, then selection and segments from the preparation
+    // launch; up to 8 tokens (one token block) the preparation launch does it
+    // all (one launch less on the decode path)
+    const bool tile = T > 8 && router_tile_quantises(c.hidden);
+    if (tile) {
+      TimedScope ts(L, st, "router_tile");
+      e = launch_router_tile(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts, L->w.router_w, L->ws.rpart,
+                             L->ws.xq, L->ws.xs, act4_of(L), st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
     {
       TimedScope ts(L, st, "prep");
       e = launch_prep(static_cast<const uint16_t*>(x), T, c.hidden, c.n_experts, c.top_k, c.n_shared,
                       bn, L->w.router_w, L->w.router_b, scoring_of(L), logits_out, idx, w, true, act4_of(L),
-                      L->ws, st);
+                      L->ws, st, tile);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return ffn_tail(L, T, bn, true, w, residual, y, st);

@@ -242,7 +242,7 @@ cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, 
   p.o = ws.o;
   p.part = ws.part;
   p.cnt = ws.split_cnt + (mode == kModeUp ? 0 : ws.split_cnt_n / 2);
-  p.split_ok = bn <= ws.part_bn && ws.split_cnt_n >= 2 * 16 * num_sms;
+  p.split_ok = bn <= ws.part_bn && ws.split_cnt_n >= 2 * 4 * kSplitUnitsPerCta * num_sms;
   p.err = ws.err;
   if (mode == kModeDown && cmb && bn <= 64) {
     p.fuse_combine = 1;

@@ -181,8 +181,9 @@ struct Piece {
 constexpr int kMaxPieces = 16;  // pieces per unit in the split partition
 constexpr int kMaxTopK = 8, kMaxShared = 4;  // layer limits (moe_config)
 
-// All arithmetic in 32 bits: split mode needs total < 4 * gridDim.x, so the
-// stage iterations stay below 2^20.
+// All arithmetic in 32 bits: split mode needs total < kSplitUnitsPerCta *
+// gridDim.x (at most 64 stages a unit), so stage iterations times CTAs stay
+// far below 2^32.
 struct Sched {
   int ti, g, end;  // split: stage iterations in all, cursor, end of this CTA's range
   int total, ks, u;
@@ -191,7 +192,7 @@ struct Sched {
   __device__ Sched(int total_, int ks_, int split_ok, int cta_, int G_)
       : total(total_), ks(ks_), cta(cta_), G(G_) {
     split = false;
-    if (split_ok && total < 4 * G) {
+    if (split_ok && total < kSplitUnitsPerCta * G) {
       ti = total * ks;
       const int split_max = (ti + G - 1) / G;
       const int plain_max = ((total + G - 1) / G) * ks;

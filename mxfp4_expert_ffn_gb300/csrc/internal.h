@@ -71,6 +71,11 @@ struct Workspace {
 struct MmaMaps;
 
 constexpr int kSegCtas = 32;  // CTAs of the large-batch segments
+// The tensor-core GEMM's split partition takes launches of fewer than this
+// many units per CTA (one arrival counter per unit and row quadrant).  With
+// more units the plain partition is as even, and cutting units costs more
+// (partial tiles through L2): measured slower at 7 and 16 units per CTA.
+constexpr int kSplitUnitsPerCta = 4;
 
 struct Timer {
   const char* name = nullptr;
@@ -147,6 +152,13 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const f
                                  const float* b, float* logits, int num_sms, cudaStream_t st);
 int router_ksplit(int H);
 constexpr int kRouterSplitMaxT = 64;
+// Split-K partial sums part[ks][T][E] (ks = router_ksplit(H)) of the router
+// logits for T <= kRouterSplitMaxT tokens, and, with xq non-null, the codes
+// of x (xq [T][H] E4M3, or packed E2M1 when act4; xs [T][H/32]).
+cudaError_t launch_router_tile(const uint16_t* x, int T, int H, int E, const float* W, float* part,
+                               uint8_t* xq, uint8_t* xs, bool act4, cudaStream_t st);
+// Whether launch_router_tile can also write the codes of x for this hidden size.
+bool router_tile_quantises(int H);
 cudaError_t launch_router_split(const uint16_t* x, int T, int H, int E, int k, const float* W,
                                 const float* b, const Scoring& sg, float* part, float* logits_out,
                                 int32_t* idx, float* w, cudaStream_t st);
@@ -194,12 +206,15 @@ bool mma_maps_set_shared_format(MmaMaps* m, const moe_config& c, const moe_weigh
 bool mma_act4_supported(const moe_config& c);
 // Small batches (T <= kPrepMaxTokens): router + top-k (route) or the given
 // routing, FP8 codes of x by token (xq/xs) and the segments, in one launch.
+// parts_ready (route): launch_router_tile has already written the router's
+// partial sums (ws.rpart) and the codes of x; this launch adds the partials,
+// selects and builds the segments.
 constexpr int kPrepMaxTokens = 64;
 cudaError_t prepare_prep_kernel(int E, int H);
 cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, int bn,
                         const float* W, const float* b, const Scoring& sg, float* logits_out,
                         int32_t* idx, float* w, bool route, bool act4, const Workspace& ws,
-                        cudaStream_t st);
+                        cudaStream_t st, bool parts_ready = false);
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out,
                            cudaStream_t st);
 

@@ -35,6 +35,7 @@ struct PrepParams {
   const uint16_t* x;
   int T, H, E, k, ns, bn;
   int route;             // 1: compute logits and top-k; 0: idx and w are given
+  int parts_ready;       // route: the partial sums and the codes of x come from router_tile_kernel
   const float* W;        // [E][H] router weights (route)
   const float* b;        // [E] bias or null
   int ks;                // K chunks of the router
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
   // ---- 1a. router partial sums: warp = expert, CTA = (expert group, token block, K chunk);
   // the warp's first batch of W_r loads is in flight while the CTA's x chunk
   // (8 tokens x H/ks) is staged in shared memory
-  if (p.route) {
+  if (p.route && !p.parts_ready) {
     const int e = blockIdx.x * kPrepWarps + warp;
     const int t0 = blockIdx.y * kPrepTT, nt = min(kPrepTT, p.T - t0);
     const int kc = p.H / p.ks, k0 = blockIdx.z * kc;
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
       for (int i = cta * blockDim.x + threadIdx.x; i < p.ws.split_cnt_n; i += stride) p.ws.split_cnt[i] = 0;
       for (int i = cta * blockDim.x + threadIdx.x; i < p.ws.comb_cnt_n; i += stride) p.ws.comb_cnt[i] = 0;
     }
-    const int n8 = p.T * (p.H / 8);  // a multiple of 4: whole quads stay in or out
+    const int n8 = p.parts_ready ? 0 : p.T * (p.H / 8);  // a multiple of 4: whole quads stay in or out
     const unsigned quad = 0xFu << (lane & ~3);
     const uint4* x8 = reinterpret_cast<const uint4*>(p.x);
     uint2* q8 = reinterpret_cast<uint2*>(p.ws.xq);
@@ -193,7 +194,7 @@ cudaError_t prepare_prep_kernel(int E, int H) {
 cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, int bn,
                         const float* W, const float* b, const Scoring& sg, float* logits_out,
                         int32_t* idx, float* w, bool route, bool act4, const Workspace& ws,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool parts_ready) {
   if (T <= 0 || T > kPrepMaxTokens) return cudaErrorInvalidValue;
   PrepParams p;
   p.x = x;
@@ -204,6 +205,7 @@ cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, i
   p.ns = ns;
   p.bn = bn;
   p.route = route ? 1 : 0;
+  p.parts_ready = route && parts_ready ? 1 : 0;
   p.W = W;
   p.b = b;
   p.ks = router_ksplit(H);
@@ -216,7 +218,9 @@ cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, i
   p.act4 = act4 ? 1 : 0;
   p.ws = ws;
   dim3 grid;
-  if (route) {
+  if (p.parts_ready) {
+    grid = dim3(1, (T + kPrepTT - 1) / kPrepTT, 1);
+  } else if (route) {
     grid = dim3((E + kPrepWarps - 1) / kPrepWarps, (T + kPrepTT - 1) / kPrepTT, p.ks);
   } else {
     const int n8 = T * (H / 8);
