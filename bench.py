@@ -153,16 +153,19 @@ def layer_bytes(wl, n_experts_touched: int, T: int, shared_fp8: bool = False) ->
             "ffn_up_mma": up, "ffn_down_mma": down}
 
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu capture
-# summarised in profiles/ffn_mma_decode_e24_t1_traffic.md; valid only for the kernel source it was
-# taken on and for a decode token (7 experts streamed per launch, as in that capture).
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) as a multiple of the
+# launch's algorithmic bytes, from the ncu capture summarised in
+# profiles/ffn_mma_t64_e128_full.md (one layer of the 8-layer stack's shape: 64 tokens, Zipf
+# routing, a 128-expert bank, 64-token tiles).  The stack's launches stream their experts the
+# same way (one 64-token tile per active expert), so the traffic scales with the experts touched:
+# traffic = ratio x algorithmic bytes.  Valid only for the kernel source the capture was taken on.
 _TRAFFIC_SRC = ("mxfp4_expert_ffn_gb300/csrc/ffn_mma_kernel.cuh", "mxfp4_expert_ffn_gb300/csrc/ffn_mma.cu")
-_TRAFFIC_SHA256 = "abe7e20a8af16235b6cf84d9ce033c7459845c53fa261802b765210bb854bdfd"
-_TRAFFIC = {("v41_layer_decode_t1", "ffn_up_mma"): (88.527616 + 1.949696) * 1e6,
-            ("v41_layer_decode_t1", "ffn_down_mma"): (43.987712 + 0.002048) * 1e6}
+_TRAFFIC_SHA256 = "6d260135d5a0cb9a9fec8c1fc345a738f922e6d249aa184e081251d52c681bc6"
+_TRAFFIC_RATIO = {("v41_stack8_decode_t64_zipf", "ffn_up_mma"): (703.216128 + 4.781568) / 715.826688,
+                  ("ncu_v41_e128_decode_t64_zipf", "ffn_up_mma"): (703.216128 + 4.781568) / 715.826688}
 
 
-def measured_traffic(workload: str, kernel: str):
+def measured_traffic(workload: str, kernel: str, algorithmic_bytes: float):
     import hashlib
     try:
         h = hashlib.sha256()
@@ -173,7 +176,8 @@ def measured_traffic(workload: str, kernel: str):
             return None  # the kernel changed since the counters were taken
     except OSError:
         return None
-    return _TRAFFIC.get((workload, kernel))
+    r = _TRAFFIC_RATIO.get((workload, kernel))
+    return None if r is None else r * algorithmic_bytes
 
 
 def layer_flops(wl, T: int) -> int:
@@ -387,6 +391,10 @@ def run_ours(args):
     for L in Ls:
         L.set_option(m.MOE_OPT_TIMING, 1)
         L.kernel_times()
+    # this library's launches in one step (every layer call records each of its launches)
+    step(0)
+    per_step_launches = sum(n for L in Ls for _, _, n in L.kernel_times())
+    per_step_launches += nl if nl > 1 else 0  # one moe_rmsnorm launch per layer of a stack
     timed_loop(step)  # stream launches: the library's events bracket each kernel
     ktimes = {}
     for L in Ls:
@@ -395,9 +403,6 @@ def run_ours(args):
             a[0] += kms
             a[1] += n
         L.set_option(m.MOE_OPT_TIMING, 0)
-    launches = sum(n for _, n in ktimes.values())
-    # plus one moe_rmsnorm launch per layer of a stack (not a layer call, so not in the layer timers)
-    per_step_launches = launches // max(1, args.steps) + (nl if nl > 1 else 0)
     dom = max(ktimes, key=lambda n: ktimes[n][0])
     dom_ms = ktimes[dom][0] / ktimes[dom][1]
 
@@ -419,7 +424,7 @@ def run_ours(args):
             if "mma" in dom and t_tensor > t_hbm:
                 ach = kflops / (dom_ms / 1e3) / 1e12
                 roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": mma_peak,
-                            "unit": "TFLOP/s", "frac": ach / mma_peak, "traffic": measured_traffic(wl.name, dom),
+                            "unit": "TFLOP/s", "frac": ach / mma_peak, "traffic": None,
                             "algorithmic_flops_per_launch": kflops, "avg_launch_ms": dom_ms,
                             "peak_src": f"measured {mma_kind} issue rate x {n_sms} SMs x median SM clock "
                                         f"{sm_mhz:.0f} MHz"}
@@ -427,7 +432,7 @@ def run_ours(args):
                 ach = b[dom] / (dom_ms / 1e3) / 1e9
                 roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": pk["hbm_gbs"],
                             "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
-                            "traffic": measured_traffic(wl.name, dom),
+                            "traffic": measured_traffic(wl.name, dom, b[dom]),
                             "algorithmic_bytes_per_launch": b[dom], "avg_launch_ms": dom_ms,
                             "peak_src": pk["src"]}
         layer_gbs = nl * b["layer"] / (ms_step / 1e3) / 1e9  # all layers' bytes over the step
