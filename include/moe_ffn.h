@@ -167,6 +167,40 @@ moe_status moe_forward_host(moe_layer* layer, const void* x_host, int32_t T, voi
 moe_status moe_stack_forward_host(moe_layer* const* layers, int32_t n_layers, const void* x_host,
                                   int32_t T, float norm_eps, void* y_host, void* stream);
 
+/* Expert parallelism: the routed experts split over ranks (FreeToken issue
+ * #444, "Other engines": the model served on several GB300s).  The scheme is
+ * all-gather / partial / exchange: every rank routes the whole batch with the
+ * full router, computes the share of y its experts (and, on one rank, the
+ * shared experts) contribute, and the shares of each token are added on the
+ * token's owner in rank order.
+ *
+ * moe_layer_create_range: a layer that computes routed experts
+ * expert_begin .. expert_end - 1 only.  The routed banks in w hold those
+ * experts only (expert e at index e - expert_begin); the router weights cover
+ * all cfg->n_experts experts; the shared experts, if cfg->n_shared > 0, are
+ * computed by this layer (give them to one rank only).  Slots routed to other
+ * experts are skipped without an error.  Tensor-core path only:
+ * MOE_ERR_UNSUPPORTED where the shapes have none, and MOE_OPT_PATH = 1 is
+ * refused.  0 <= expert_begin < expert_end <= n_experts (MOE_ERR_INVALID_ARG
+ * otherwise). */
+moe_status moe_layer_create_range(const moe_config* cfg, const moe_weights* w, int device,
+                                  int32_t expert_begin, int32_t expert_end, moe_layer** out);
+
+/* The layer's share of y in fp32, not rounded and without a residual:
+ *   y_partial[t] = sum_shared o_s + sum over slots j whose expert the layer
+ *                  computes of topk_w[t][j] * o_{topk_idx[t][j]}
+ * (shared experts first, then j = 0..k-1).  y_partial fp32 [T][H], 16-byte
+ * aligned.  Other arguments as for moe_forward. */
+moe_status moe_forward_partial(moe_layer* layer, const void* x, int32_t T, const int32_t* topk_idx,
+                               const float* topk_w, float* y_partial, void* stream);
+
+/* Adds the ranks' shares of a layer: y[t] = bf16( sum over r = 0 .. n_parts-1,
+ * in that order, of partials[r][t] ), then with a residual (bf16 [T][H] or
+ * NULL) y[t] = bf16(residual[t] + y[t]).  partials fp32 [n_parts][T][H]
+ * (16-byte aligned), y bf16 [T][H]; H a multiple of 4.  No layer is needed. */
+moe_status moe_combine_partials(const float* partials, int32_t n_parts, int32_t T, int32_t H,
+                                const void* residual, void* y, void* stream);
+
 /* The activation quantiser alone: q [T][H] E4M3 codes and s [T][H/32] UE8M0
  * bytes, by the rule: per block of 32, e = the smallest integer with
  * max|x| <= 448 * 2^e (e = 0 for an all-zero block, limited to [-127, 127]),

@@ -27,7 +27,8 @@ PATH_AUTO, PATH_SIMT, PATH_MMA = 0, 1, 2
 EXPORTS = ("moe_layer_create", "moe_destroy", "moe_layer_destroy", "moe_route", "moe_forward", "moe_step",
            "moe_forward_host", "moe_quantize_act", "moe_quantize_act4", "moe_segments", "moe_rmsnorm", "moe_sync",
            "moe_set_option", "moe_get_kernel_times", "moe_status_string", "moe_abi_version",
-           "moe_route_static", "moe_stack_forward_host")
+           "moe_route_static", "moe_stack_forward_host", "moe_layer_create_range", "moe_forward_partial",
+           "moe_combine_partials")
 ROUTE_STATIC_MAX_TOKENS = 64
 
 
@@ -83,6 +84,10 @@ def lib():
                                            C.POINTER(C.c_int64), I32, C.POINTER(I32)]
         L.moe_route_static.argtypes = [P, I32, I32, I32, I32, P, P, P, P, P]
         L.moe_stack_forward_host.argtypes = [P, I32, P, I32, C.c_float, P, P]
+        L.moe_layer_create_range.argtypes = [C.POINTER(MoeConfig), C.POINTER(MoeWeights), C.c_int, I32, I32,
+                                             C.POINTER(P)]
+        L.moe_forward_partial.argtypes = [P, P, I32, P, P, P, P]
+        L.moe_combine_partials.argtypes = [P, I32, I32, I32, P, P, P]
         L.moe_status_string.argtypes = [C.c_int]
         L.moe_status_string.restype = C.c_char_p
         L.moe_abi_version.restype = I32
@@ -138,6 +143,24 @@ def moe_layer_create(cfg: MoeConfig, weights: MoeWeights, device: int = 0) -> in
 
 def moe_destroy(h: int) -> None:
     _check(lib().moe_destroy(h), "moe_destroy")
+
+
+def moe_layer_create_range(cfg: MoeConfig, weights: MoeWeights, expert_begin: int, expert_end: int,
+                           device: int = 0) -> int:
+    h = P()
+    _check(lib().moe_layer_create_range(C.byref(cfg), C.byref(weights), device, expert_begin, expert_end,
+                                        C.byref(h)), "moe_layer_create_range")
+    return h.value
+
+
+def moe_forward_partial(h, x, T, topk_idx, topk_w, y_partial, stream=None) -> None:
+    _check(lib().moe_forward_partial(h, ptr(x), T, ptr(topk_idx), ptr(topk_w), ptr(y_partial),
+                                     stream_handle(stream)), "moe_forward_partial")
+
+
+def moe_combine_partials(partials, n_parts, T, H, residual, y, stream=None) -> None:
+    _check(lib().moe_combine_partials(ptr(partials), n_parts, T, H, ptr(residual), ptr(y), stream_handle(stream)),
+           "moe_combine_partials")
 
 
 def moe_layer_destroy(h: int) -> None:
@@ -228,7 +251,7 @@ class Layer:
     """
 
     def __init__(self, hidden, inter, n_experts, top_k, n_shared, max_tokens, weights: dict,
-                 device: int = 0):
+                 device: int = 0, expert_range: tuple[int, int] | None = None):
         self.cfg = MoeConfig(hidden, inter, n_experts, top_k, n_shared, max_tokens)
         self.weights = weights
         w = MoeWeights()
@@ -237,7 +260,10 @@ class Layer:
         w.router_w = ptr(weights["router_w"])
         w.router_b = ptr(weights.get("router_b"))
         self._w = w
-        self.handle = moe_layer_create(self.cfg, w, device)
+        if expert_range is None:
+            self.handle = moe_layer_create(self.cfg, w, device)
+        else:  # expert parallelism: the routed banks hold experts expert_range[0] .. [1] - 1
+            self.handle = moe_layer_create_range(self.cfg, w, expert_range[0], expert_range[1], device)
 
     def route(self, x, T, idx, w, logits_in=None, logits_out=None, stream=None):
         moe_route(self.handle, x, T, logits_in, logits_out, idx, w, stream)
@@ -247,6 +273,9 @@ class Layer:
 
     def step(self, x, T, y, residual=None, idx=None, w=None, logits_out=None, stream=None):
         moe_step(self.handle, x, T, residual, y, idx, w, logits_out, stream)
+
+    def forward_partial(self, x, T, idx, w, y_partial, stream=None):
+        moe_forward_partial(self.handle, x, T, idx, w, y_partial, stream)
 
     def forward_host(self, x_host, T, y_host, stream=None):
         moe_forward_host(self.handle, x_host, T, y_host, stream)

@@ -209,13 +209,21 @@ const char* moe_status_string(moe_status s) {
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
 
-moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int device,
-                            moe_layer** out) {
+}  // extern "C"
+
+namespace {
+
+// A layer computing the routed experts [e_lo, e_hi) (all of them: 0, E),
+// whose routed banks hold those experts only.
+moe_status create_impl(const moe_config* cfg, const moe_weights* w, int device, int e_lo, int e_hi,
+                       moe_layer** out) {
   if (!out) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
   moe_status st = validate_config(cfg);
   if (st != MOE_OK) return st;
   if ((st = validate_weights(cfg, w)) != MOE_OK) return st;
+  if (e_lo < 0 || e_hi > cfg->n_experts || e_lo >= e_hi) return MOE_ERR_INVALID_ARG;
+  const bool partial = e_lo != 0 || e_hi != cfg->n_experts;
   if (fault("alloc")) return MOE_ERR_OOM;
   DeviceGuard g(device);
   if (g.status != cudaSuccess) return cuda_fail(g.status);
@@ -237,6 +245,8 @@ moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int dev
     return MOE_ERR_OOM;
   }
   carve(*cfg, L->num_sms, static_cast<char*>(base), L->ws);
+  L->ws.e_lo = e_lo;
+  L->ws.e_hi = e_hi;
   L->ws.base = base;
   L->ws.bytes = bytes;
   cudaError_t e = cudaMemset(base, 0, bytes);
@@ -253,19 +263,46 @@ moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int dev
   if (e == cudaSuccess) {
     L->maps = mma_maps_create(*cfg, *w, L->ws);  // NULL: tensor-core path unavailable
     cudaGetLastError();
-    e = router_split_weights(w->router_w, cfg->n_experts, cfg->hidden, L->ws.w3, 0);
+    // a range of experts runs on the tensor cores only (the SIMT kernels index
+    // the banks by the global expert id)
+    if (partial && !L->maps) e = cudaErrorNotSupported;
+    if (e == cudaSuccess) e = router_split_weights(w->router_w, cfg->n_experts, cfg->hidden, L->ws.w3, 0);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e == cudaSuccess)
       L->router_mma = router_map_weights(&L->router_map, L->ws.w3, cfg->n_experts, cfg->hidden);
   }
   if (e != cudaSuccess) {
     if (L->ws.err_host) cudaFreeHost(L->ws.err_host);
+    mma_maps_destroy(L->maps);
     cudaFree(base);
     delete L;
+    if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
     return cuda_fail(e);
   }
   *out = L;
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, int device,
+                            moe_layer** out) {
+  if (!cfg) {
+    if (out) *out = nullptr;
+    return MOE_ERR_INVALID_ARG;
+  }
+  return create_impl(cfg, w, device, 0, cfg->n_experts, out);
+}
+
+moe_status moe_layer_create_range(const moe_config* cfg, const moe_weights* w, int device,
+                                  int32_t expert_begin, int32_t expert_end, moe_layer** out) {
+  if (!cfg) {
+    if (out) *out = nullptr;
+    return MOE_ERR_INVALID_ARG;
+  }
+  return create_impl(cfg, w, device, expert_begin, expert_end, out);
 }
 
 moe_status moe_destroy(moe_layer* L) {
@@ -288,8 +325,9 @@ moe_status moe_set_option(moe_layer* L, int32_t option, int64_t value) {
   if (option == MOE_OPT_PATH) {
     if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
     if (value == 2 && !L->maps) return MOE_ERR_UNSUPPORTED;
-    if (value == 1 && (L->act_format == MOE_ACT_FP4 || L->shared_format == MOE_SHARED_FP8_B32))
-      return MOE_ERR_UNSUPPORTED;  // no SIMT path for either variant
+    if (value == 1 && (L->act_format == MOE_ACT_FP4 || L->shared_format == MOE_SHARED_FP8_B32 ||
+                       L->ws.e_lo != 0 || L->ws.e_hi != L->cfg.n_experts))
+      return MOE_ERR_UNSUPPORTED;  // no SIMT path for these variants, nor for a range of experts
     L->path = (int)value;
     return MOE_OK;
   }
@@ -449,8 +487,9 @@ bool act4_of(const moe_layer* L) { return L->act_format == MOE_ACT_FP4; }
 // after the preparation kernel (token-major codes, every expert in one tile):
 // gate/up reads all tokens' codes (dense) and, with shared experts, the down
 // GEMM does the combine.
+// y_f32 (expert parallelism): the fp32 sums are stored there instead of y.
 moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool small, const float* w,
-                    const void* residual, void* y, cudaStream_t st) {
+                    const void* residual, void* y, cudaStream_t st, float* y_f32 = nullptr) {
   const moe_config& c = L->cfg;
   const ExpertBank bank = bank_of(L);
   const int ns_tiles = c.n_shared * ((T + bn - 1) / bn);
@@ -461,7 +500,7 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool small, const float* w,
                        L->wait_limit);
   }
   if (e != cudaSuccess) return cuda_fail(e);
-  if (small && bn == 16 && c.n_shared > 0) {
+  if (small && bn == 16 && c.n_shared > 0 && !y_f32) {
     // up to 16 tokens: the combine runs inside the down GEMM (every token has a
     // shared-expert position, so every y row has a last writer).  With wider
     // tiles a unit is the last writer of up to 64 tokens, whose combines one
@@ -482,13 +521,14 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool small, const float* w,
   {
     TimedScope ts(L, st, "combine");
     e = launch_combine(L->ws, T, c.hidden, c.top_k, c.n_shared, w,
-                       static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(y), st);
+                       static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(y), st, y_f32);
   }
   return cuda_fail(e);
 }
 
 moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* idx,
-                        const float* w, const void* residual, void* y, cudaStream_t st) {
+                        const float* w, const void* residual, void* y, cudaStream_t st,
+                        float* y_f32 = nullptr) {
   const moe_config& c = L->cfg;
   const ExpertBank bank = bank_of(L);
   const bool mma = use_mma(L, T);
@@ -502,7 +542,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
                       act4_of(L), L->ws, st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
-    return ffn_tail(L, T, bn, true, w, residual, y, st);
+    return ffn_tail(L, T, bn, true, w, residual, y, st, y_f32);
   }
   {
     TimedScope ts(L, st, "segments");
@@ -516,7 +556,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
                                   L->ws.slot_pos, L->ws.xg, L->ws.xgs, act4_of(L), st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
-    return ffn_tail(L, T, bn, false, w, residual, y, st);
+    return ffn_tail(L, T, bn, false, w, residual, y, st, y_f32);
   } else {
     // the FP4-activation and FP8-shared-expert variants run on the tensor cores only
     if (act4_of(L) || L->shared_format == MOE_SHARED_FP8_B32) return MOE_ERR_UNSUPPORTED;
@@ -539,7 +579,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int32_t T, const int32_t* i
   {
     TimedScope ts(L, st, "combine");
     e = launch_combine(L->ws, T, c.hidden, c.top_k, c.n_shared, w,
-                       static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(y), st);
+                       static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(y), st, y_f32);
   }
   return cuda_fail(e);
 }
@@ -621,6 +661,28 @@ moe_status moe_forward(moe_layer* L, const void* x, int32_t T, const int32_t* to
   DeviceGuard g(L->device);
   if (g.status != cudaSuccess) return cuda_fail(g.status);
   return forward_impl(L, x, T, topk_idx, topk_w, residual, y, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_partial(moe_layer* L, const void* x, int32_t T, const int32_t* topk_idx,
+                               const float* topk_w, float* y_partial, void* stream) {
+  moe_status s = check_tokens(L, T);
+  if (s != MOE_OK || T == 0) return s;
+  if (!x || !topk_idx || !topk_w || !y_partial) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y_partial, 16)) return MOE_ERR_INVALID_ARG;
+  if (fault("launch")) return MOE_ERR_CUDA;
+  DeviceGuard g(L->device);
+  if (g.status != cudaSuccess) return cuda_fail(g.status);
+  return forward_impl(L, x, T, topk_idx, topk_w, nullptr, nullptr, static_cast<cudaStream_t>(stream), y_partial);
+}
+
+moe_status moe_combine_partials(const float* partials, int32_t n_parts, int32_t T, int32_t H,
+                                const void* residual, void* y, void* stream) {
+  if (n_parts < 1 || T < 0 || H <= 0 || H % 4 != 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!partials || !y || !aligned(partials, 16) || !aligned(y, 8) || (residual && !aligned(residual, 8)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_fail(launch_combine_parts(partials, n_parts, T, H, static_cast<const uint16_t*>(residual),
+                                        static_cast<uint16_t*>(y), static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_forward_host(moe_layer* L, const void* x_host, int32_t T, void* y_host,

@@ -111,7 +111,10 @@ int mma_tile_for_tokens(int T) { return T <= 16 ? 16 : (T < 512 ? 64 : 112); }
 // a row, 256 elements, one per stage; rows of K elements are K/2 bytes for
 // weights and activations alike.
 static bool format_maps(FormatMaps* m, bool a4, const moe_config& c, const moe_weights& w, const Workspace& ws) {
-  const uint64_t H = c.hidden, I = c.inter, E = c.n_experts, ns = c.n_shared;
+  // the routed banks hold the layer's own experts (all E, or its range under
+  // expert parallelism)
+  const uint64_t H = c.hidden, I = c.inter, ns = c.n_shared;
+  const uint64_t E = (uint64_t)(ws.e_hi < c.n_experts ? ws.e_hi : c.n_experts) - (uint64_t)ws.e_lo;
   const uint64_t P = (uint64_t)c.max_tokens * (c.top_k + c.n_shared);
   m->shared_fp8 = false;
   m->ch_up = a4 ? 1 : chunks_per_stage((int)H, false);
@@ -234,6 +237,7 @@ cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, 
     ch = mm.ch_down;
   }
   p.E = bk.E;
+  p.e_lo = ws.e_lo;
   p.n_active = ws.n_active;
   p.tile_prefix = ws.tile_prefix;
   p.tile_info = ws.tile_info;

@@ -45,6 +45,7 @@ struct MmaParams {
   const uint8_t* sa_shared[2];
   const uint8_t* sb;         // activation scales by position, [P][K/32]
   int E, K, rows;            // rows per expert of the weight matrices (I up, H down)
+  int e_lo;                  // the routed banks hold experts e_lo, e_lo + 1, ... (expert parallelism)
   int out_cols;              // I (h row length) in up mode, H in down mode
   const int32_t* n_active;   // [0] active experts, [1] token tiles in all
   const int32_t* tile_prefix;
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next()) {
         const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
         const bool sh = un.e >= p.E;
-        const int erow = (sh ? un.e - p.E : un.e) * p.rows + un.row0;
+        const int erow = (sh ? un.e - p.E : un.e - p.e_lo) * p.rows + un.row0;
         bool ok = true;
         const int s_end = pc.s1;
         for (int s = pc.s0; s < s_end; ++s, ++g) {
@@ -552,7 +553,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
       const int s_end = pc.s1;
       const bool sh = un.e >= p.E;
-      const size_t erow = (size_t)(sh ? un.e - p.E : un.e) * p.rows + un.row0 + 32 * q + lane;
+      const size_t erow = (size_t)(sh ? un.e - p.E : un.e - p.e_lo) * p.rows + un.row0 + 32 * q + lane;
       const uint8_t* sa_row[NA];
 #pragma unroll
       for (int m = 0; m < NA; ++m)

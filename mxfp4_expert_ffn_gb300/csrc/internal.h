@@ -63,6 +63,8 @@ struct Workspace {
   int32_t* seg_counter = nullptr; // [1]    its last-arriver counter (zero between launches)
   int32_t* seg_routed = nullptr;  // [1]    its routed slot total
   int32_t* err = nullptr;     // [1]        device error word
+  int e_lo = 0, e_hi = 1 << 30; // expert ids this layer computes (expert parallelism); others
+                                // in [0, E) belong to other ranks and are skipped silently
   int32_t* err_host = nullptr;// pinned: the error word, then (host entry point) y of small batches
   void* base = nullptr;       // single allocation holding all of the above
   size_t bytes = 0;
@@ -178,7 +180,10 @@ cudaError_t launch_ffn_down_simt(const ExpertBank& bank, int T, int k, int n_sha
                                  const Workspace& ws, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const Workspace& ws, int T, int H, int k, int n_shared,
                            const float* w, const uint16_t* residual, uint16_t* y,
-                           cudaStream_t st);
+                           cudaStream_t st, float* y_f32 = nullptr);
+// y = bf16(sum of part[r], r = 0 .. R-1 in order) (+ residual), part [R][T][H] fp32.
+cudaError_t launch_combine_parts(const float* part, int R, int T, int H, const uint16_t* residual, uint16_t* y,
+                                 cudaStream_t st);
 MmaMaps* mma_maps_create(const moe_config& c, const moe_weights& w, const Workspace& ws);
 void mma_maps_destroy(MmaMaps* m);
 int mma_tile_for_tokens(int T);

@@ -120,9 +120,12 @@ __global__ void __launch_bounds__(1024) segments_kernel(const int32_t* __restric
 // y[t] = bf16( sum_s o[S + s*T + t] + sum_j w[t][j] * o[slot_pos[t*k + j]] ),
 // accumulated in fp32 in that fixed order; optional residual added to the
 // bf16-rounded sum.  Four consecutive h per thread.
+// yf (expert parallelism): the fp32 sum itself, not rounded and without the
+// residual, is stored (the layer's share of y, added across ranks later).
 __global__ void combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_pos,
                                const float* __restrict__ w, int T, int H, int k, int ns,
-                               const uint16_t* __restrict__ res, uint16_t* __restrict__ y) {
+                               const uint16_t* __restrict__ res, uint16_t* __restrict__ y,
+                               float* __restrict__ yf) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;  // tokens on x: up to 2^31 - 1 of them
@@ -147,10 +150,49 @@ __global__ void combine_kernel(const float* __restrict__ o, const int32_t* __res
     acc.z = fmaf(wj, v.z, acc.z);
     acc.w = fmaf(wj, v.w, acc.w);
   }
+  if (yf) {
+    *reinterpret_cast<float4*>(yf + (size_t)t * H + h) = acc;
+    return;
+  }
   float r[4] = {acc.x, acc.y, acc.z, acc.w};
   uint16_t b[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) b[i] = __bfloat16_as_ushort(__float2bfloat16_rn(r[i]));
+  if (res) {
+    const uint2 rv = *reinterpret_cast<const uint2*>(res + (size_t)t * H + h);
+    const uint16_t rb[4] = {(uint16_t)(rv.x & 0xFFFF), (uint16_t)(rv.x >> 16),
+                            (uint16_t)(rv.y & 0xFFFF), (uint16_t)(rv.y >> 16)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      b[i] = __bfloat16_as_ushort(
+          __float2bfloat16_rn(bf16_bits_to_float(rb[i]) + bf16_bits_to_float(b[i])));
+  }
+  *reinterpret_cast<uint2*>(y + (size_t)t * H + h) =
+      make_uint2(b[0] | ((uint32_t)b[1] << 16), b[2] | ((uint32_t)b[3] << 16));
+}
+
+// y[t] = bf16( sum over parts r = 0 .. R-1, in that order, of part[r][t] ),
+// then with a residual bf16(residual[t] + y[t]): the ranks' shares of a layer
+// under expert parallelism, added in a fixed order.
+__global__ void combine_parts_kernel(const float* __restrict__ part, int R, int T, int H,
+                                     const uint16_t* __restrict__ res, uint16_t* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  const int h = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  if (h >= H) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r = 0; r < R; ++r) {
+    const float4 v = *reinterpret_cast<const float4*>(part + ((size_t)r * T + t) * H + h);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  const float f[4] = {acc.x, acc.y, acc.z, acc.w};
+  uint16_t b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) b[i] = __bfloat16_as_ushort(__float2bfloat16_rn(f[i]));
   if (res) {
     const uint2 rv = *reinterpret_cast<const uint2*>(res + (size_t)t * H + h);
     const uint16_t rb[4] = {(uint16_t)(rv.x & 0xFFFF), (uint16_t)(rv.x >> 16),
@@ -283,10 +325,19 @@ cudaError_t prepare_segments_kernel(int E) {
 }
 
 cudaError_t launch_combine(const Workspace& ws, int T, int H, int k, int n_shared, const float* w,
-                           const uint16_t* residual, uint16_t* y, cudaStream_t st) {
+                           const uint16_t* residual, uint16_t* y, cudaStream_t st, float* y_f32) {
   if (T == 0) return cudaSuccess;
   dim3 grid(T, (H / 4 + 255) / 256);
-  { cudaError_t le_ = launch_pdl(combine_kernel, dim3(grid), dim3(256), 0, st, ws.o, ws.slot_pos, w, T, H, k, n_shared, residual, y); if (le_ != cudaSuccess) return le_; }
+  { cudaError_t le_ = launch_pdl(combine_kernel, dim3(grid), dim3(256), 0, st, ws.o, ws.slot_pos, w, T, H, k, n_shared, residual, y, y_f32); if (le_ != cudaSuccess) return le_; }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_parts(const float* part, int R, int T, int H, const uint16_t* residual, uint16_t* y,
+                                 cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  dim3 grid(T, (H / 4 + 255) / 256);
+  cudaError_t le = launch_pdl(combine_parts_kernel, grid, dim3(256), 0, st, part, R, T, H, residual, y);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

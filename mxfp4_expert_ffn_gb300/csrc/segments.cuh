@@ -9,6 +9,11 @@
 
 namespace moe {
 
+// A slot's expert id is local (this layer computes it), remote (a valid id in
+// [0, E) outside the layer's expert range: another rank's under expert
+// parallelism, skipped without an error) or invalid (skipped and reported).
+__device__ __forceinline__ bool slot_local(int e, const Workspace& ws) { return e >= ws.e_lo && e < ws.e_hi; }
+
 // Block-wide exclusive scans over the experts (thread e for expert e; needs
 // blockDim.x == 1024 >= E) of the per-expert slot counts cnt_s[e], of the
 // "has slots" flags and of the token tiles of width bn: writes ws.cnt/off, the
@@ -143,6 +148,8 @@ __device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx, in
       if (b0 + 32 * u + lane < hi && (e < 0 || e >= E)) {
         raise_error(ws.err, kErrExpertRange);
         e = -1;
+      } else if (!slot_local(e, ws)) {
+        e = -1;
       }
       if (b0 + 32 * u + lane >= hi) e = -1;
       const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
@@ -181,7 +188,7 @@ __device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx, in
       if (b0 + 32 * u >= hi) break;  // warp-uniform
       const int s = b0 + 32 * u + lane;
       int e = er[u];
-      if (s >= hi || e < 0 || e >= E) e = -1;
+      if (s >= hi || e < 0 || e >= E || !slot_local(e, ws)) e = -1;
       const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
       if (e >= 0) {
         const int p = off_s[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
@@ -248,6 +255,8 @@ __device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ i
     if (e < 0 || e >= E) {
       raise_error(ws.err, kErrExpertRange);
       e = -1;
+    } else if (!slot_local(e, ws)) {
+      e = -1;
     }
     sid[tid] = e;
     if (e >= 0) atomicAdd(&cnt_s[e], 1);
@@ -297,7 +306,7 @@ __device__ __forceinline__ void segments_tiny(const int32_t* sid, int T, int k, 
     int c = 0, off = 0;
     for (int j = 0; j < S; ++j) {
       const int x = sid[j];
-      const bool v = x >= 0 && x < E;
+      const bool v = x >= 0 && x < E && slot_local(x, ws);
       c += v && x == e;
       off += v && x < e;
     }
@@ -308,8 +317,8 @@ __device__ __forceinline__ void segments_tiny(const int32_t* sid, int T, int k, 
   if (tid >= 32) return;
   const unsigned full = 0xFFFFFFFFu;
   const int x = lane < S ? sid[lane] : -1;
-  const bool v = lane < S && x >= 0 && x < E;
-  if (lane < S && !v) raise_error(ws.err, kErrExpertRange);
+  const bool v = lane < S && x >= 0 && x < E && slot_local(x, ws);
+  if (lane < S && (x < 0 || x >= E)) raise_error(ws.err, kErrExpertRange);
   const unsigned same = __match_any_sync(full, v ? x : -1 - lane);  // lanes with this slot's expert
   const int rank = __popc(same & ((1u << lane) - 1u));            // earlier slots of that expert
   const bool leader = v && (__ffs(same) - 1 == lane);              // the expert's first slot
@@ -371,6 +380,8 @@ __device__ __forceinline__ void count_warp_slots(const int32_t* __restrict__ idx
     int e = s < hi ? idx[s] : -1;
     if (s < hi && (e < 0 || e >= E)) {
       if (report) raise_error(ws.err, kErrExpertRange);
+      e = -1;
+    } else if (!slot_local(e, ws)) {
       e = -1;
     }
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
@@ -467,7 +478,7 @@ __device__ __forceinline__ void segments_place_cta(const int32_t* __restrict__ i
   for (int b0 = lo; b0 < hi; b0 += 32) {
     const int s = b0 + lane;
     int e = s < hi ? idx[s] : -1;
-    if (s >= hi || e < 0 || e >= E) e = -1;
+    if (s >= hi || e < 0 || e >= E || !slot_local(e, ws)) e = -1;
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
     if (e >= 0) {
       const int p = wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));

@@ -82,6 +82,26 @@ def test_create_rejects_null_and_misaligned_weights():
     w = _weights(0x1008)  # 8-byte aligned only
     assert m.lib().moe_layer_create(C.byref(cfg), C.byref(w), 0, C.byref(h)) == m.MOE_ERR_INVALID_ARG
     assert m.lib().moe_layer_create(None, C.byref(w), 0, C.byref(h)) == m.MOE_ERR_INVALID_ARG
+    assert m.lib().moe_layer_create_range(None, C.byref(w), 0, 0, 8, C.byref(h)) == m.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("lo,hi", [(-1, 8), (0, 17), (8, 8), (9, 4)])
+def test_create_range_rejects_bad_ranges(lo, hi):
+    h = C.c_void_p()
+    cfg = m.MoeConfig(256, 128, 16, 2, 1, 4)
+    assert m.lib().moe_layer_create_range(C.byref(cfg), C.byref(_weights()), 0, lo, hi, C.byref(h)) == \
+        m.MOE_ERR_INVALID_ARG
+    assert not h.value
+
+
+def test_combine_partials_rejects_bad_arguments():
+    L = m.lib()
+    buf = (C.c_float * 64)()
+    assert L.moe_combine_partials(buf, 0, 1, 8, None, buf, None) == m.MOE_ERR_INVALID_ARG   # no parts
+    assert L.moe_combine_partials(buf, 1, 1, 6, None, buf, None) == m.MOE_ERR_INVALID_ARG   # H % 4
+    assert L.moe_combine_partials(None, 1, 1, 8, None, buf, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_partials(buf, 1, 0, 8, None, None, None) == m.MOE_OK                # T = 0
+    assert L.moe_forward_partial(None, buf, 1, buf, buf, buf, None) == m.MOE_ERR_INVALID_ARG
 
 
 def test_fault_injection_alloc(monkeypatch):

@@ -327,6 +327,60 @@ def test_stack_forward_host_matches_device_loop_and_oracle(norm_eps):
         L.close()
 
 
+# ---- expert parallelism: rank layers over expert ranges, run one after the
+# other on one GPU (their kernels never wait on each other), shares added by
+# moe_combine_partials
+
+EP_CASES = [
+    (SMALL[1], 2),                                                             # 37 tokens, 16 experts
+    (Workload("ep_h512_i256_e40_k6_s1_t130", 512, 256, 40, 6, 1, 130, seed=61,  # 64-token tiles
+              scale_lo=-7, scale_hi=-3), 3),
+    (Workload("ep_h256_i128_e16_k2_s1_t5", 256, 128, 16, 2, 1, 5, seed=62,      # decode-size tiles
+              scale_lo=-6, scale_hi=-2), 4),
+]
+
+
+@pytest.mark.parametrize("wl,R", EP_CASES, ids=lambda c: getattr(c, "name", str(c)))
+def test_expert_parallel_shares_match_oracle_and_whole_layer(wl, R):
+    from mxfp4_expert_ffn_gb300 import ep
+    W = sg.device_layer(wl, 0, gu.DEV)
+    T, H, E, k = wl.tokens, wl.hidden, wl.n_experts, wl.top_k
+    x = _x(wl)
+    xt = sg.bf16_tensor(x)
+    ranges = ep.expert_ranges(E, R)
+    layers = []
+    for r, (lo, hi) in enumerate(ranges):
+        Wr = {key: (v[lo:hi] if key.split("_")[0] in ("gate", "up", "down") else v)
+              for key, v in W.items() if r == 0 or not key.startswith("s_")}
+        layers.append(m.Layer(H, wl.inter, E, k, wl.n_shared if r == 0 else 0, T, Wr, expert_range=(lo, hi)))
+    # every rank routes the batch the same way; the oracle's routing is used here
+    idx, w = _oracle_routing(wl, x)
+    it = torch.from_numpy(idx).to(gu.DEV)
+    wt = torch.from_numpy(w.astype(np.float32)).to(gu.DEV)
+    shares = torch.empty((R, T, H), dtype=torch.float32, device=gu.DEV)
+    for r, L in enumerate(layers):
+        L.forward_partial(xt, T, it, wt, shares[r])
+        assert L.sync() == m.MOE_OK  # other ranks' experts are skipped without an error
+    y = torch.empty((T, H), dtype=torch.int16, device=gu.DEV)
+    res = sg.bf16_tensor(_x(wl, stream=5))
+    m.moe_combine_partials(shares, R, T, H, res, y)
+    torch.cuda.synchronize()
+    yb = y.cpu().numpy().view(np.uint16)
+    gu.assert_y_close(yb, gu.oracle_layer(wl, 0, x, idx, w, residual=_x(wl, stream=5)), what=f"EP x{R}")
+    # the whole layer on one GPU: the same result up to the order of the fp32 sums
+    full, _ = gu.make_layer(wl, weights=W)
+    gu.assert_y_close(yb, gu.run_forward(full, x, idx, w, residual_bits=_x(wl, stream=5)), what="vs one layer")
+    # a rank's share holds exactly its own experts: rank 1's share of a token
+    # routed only to rank 0's experts is zero
+    lo1, hi1 = ranges[1]
+    only0 = [t for t in range(T) if not any(lo1 <= e < hi1 for e in idx[t])]
+    if only0:
+        assert np.all(shares[1, only0].cpu().numpy() == 0.0)
+    full.close()
+    for L in layers:
+        L.close()
+
+
 def test_fault_injection_launch_and_arg(monkeypatch):
     wl = TINY
     L, _ = gu.make_layer(wl)
