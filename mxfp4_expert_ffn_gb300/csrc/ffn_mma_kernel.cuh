@@ -459,24 +459,26 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
         const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
         const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
-        if (!mbar_wait(&acce_bar[buf], ph_acc ^ 1, p.wait_limit)) { give_up(); break; }
-        fence_after();
         const uint32_t d_tmem = tmem + buf * C::kAccCols;
         int swap = 0, NI = NI0;
-        if (NA == 2 || C::kRagged) {
+        if (C::kRagged) {
+          // the wide tiles are often part-filled: N = the tile's tokens
+          // rounded up to the instruction's step of 16, so the MMAs cost
+          // only the columns in use (the epilogue reads no column past them)
           const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
-          const int sh = un.e >= p.E;
-          if (NA == 2) swap = p.merged[sh] && p.swap_gu[sh];
-          if (C::kRagged) {
-            // the wide tiles are often part-filled: N = the tile's tokens
-            // rounded up to the instruction's step of 16, so the MMAs cost
-            // only the columns in use (the epilogue reads no column past them)
-            const int nr = min(BN, (un.m_tile + 15) & ~15);
-            NI = nr;
-          }
+          NI = min(BN, (un.m_tile + 15) & ~15);
+        }
+        if (NA == 2) {
+          // the shared experts' tiles close the table, so no table load is
+          // needed to tell them
+          const int sh = tile_of(pc.u, mt_units, rot, n_tiles) >= n_tiles - p.ns_tiles;
+          swap = p.merged[sh] && p.swap_gu[sh];
         }
         uint32_t idesc_base = A4 ? idesc_e2m1_e2m1(128, NI, 0) : idesc_e2m1_e4m3(128, NI, 0);
         if (shared_fp8_unit(pc.u)) idesc_base &= ~(7u << 7);  // A = E4M3 (FP8 shared expert)
+        // the accumulator buffer is free once the epilogue has read it out
+        if (!mbar_wait(&acce_bar[buf], ph_acc ^ 1, p.wait_limit)) { give_up(); break; }
+        fence_after();
         bool ok = true;
         const int s_beg = pc.s0, s_end = pc.s1;
         for (int s = s_beg; s < s_end; ++s, ++g) {
