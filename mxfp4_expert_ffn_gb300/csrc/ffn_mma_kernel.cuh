@@ -270,9 +270,15 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   constexpr int NC = (BN + 31) / 32;  // 32-token groups of the B scale factors
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full_bar[kMaxStages], sf_bar[kMaxStages], empty_bar[kMaxStages];
+  // full_bar[s]: stage s's copies have landed (the producer's expect-tx
+  // arrival and the bytes of the weight and activation copies) and its scale
+  // factors are in TMEM (one arrival per scale-factor warp): the MMA issuer
+  // waits on this one barrier per stage.  Under load each barrier operation
+  // costs ~0.1 us of shared-memory latency, so one wait instead of two or three
+  // shortens the time a stage holds its slot.
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar[2];
-  __shared__ __align__(8) uint64_t bfull_bar[2], bempty_bar[2];  // the separate B ring (kSepB)
+  __shared__ __align__(8) uint64_t bempty_bar[2];  // the separate B ring's slots (kSepB)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -297,7 +303,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   // and the activation rows
   const uint32_t tx_a = NA * 128 * (A4 ? 128 : 64) * CH;
   const uint32_t tx_b = (uint32_t)BR * 128 * CH;
-  const uint32_t tx_stage = tx_a + (kSepB ? 0 : tx_b);
+  const uint32_t tx_stage = tx_a + tx_b;  // the activation copy lands on the stage's barrier too
   const uint32_t sf_col0 = C::kNAcc * C::kAccCols;
 
   if (threadIdx.x == 0) {
@@ -310,15 +316,13 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     }
     prefetch_tensormap(&p.b);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&sf_bar[s], 4);
+      mbar_init(&full_bar[s], 1 + 4);
       mbar_init(&empty_bar[s], 2);  // one commit per MMA-issuing thread
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf_bar[b], 2);
       mbar_init(&acce_bar[b], 4);
       mbar_init(&drain_bar[b], 1);
-      mbar_init(&bfull_bar[b], 1);
       mbar_init(&bempty_bar[b], 2);
     }
     abort_flag = 0;
@@ -360,23 +364,20 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       uint32_t g = 0;
-      int last_parity[kMaxStages], last_bparity[2] = {-1, -1};
+      int last_parity[kMaxStages];
       int deferred_pos[kMaxStages], deferred_s[kMaxStages], n_deferred = 0;
       // dense mode runs after the preparation kernel and waited for it above
       bool waited = dense;
       // B copies issued before the previous kernel is waited for: as many as
       // there are slots to hold them
       const uint32_t defer_cap = kSepB ? 2u : (uint32_t)NS;
-      // the activation tile of stage g (slot i: the stage's own area, or the
-      // B ring's slot), one op; dense: rows 0.. of the token-major codes
-      auto load_b = [&](int i, int pos0, int st) {
+      // the activation tile of stage g, one op into the stage's own area or
+      // the B ring's slot bs, landing on the stage's full barrier fs; dense:
+      // rows 0.. of the token-major codes
+      auto load_b = [&](int bs, int fs, int pos0, int st) {
         const int row = dense ? 0 : pos0;
-        if constexpr (kSepB) {
-          mbar_expect_tx(&bfull_bar[i], tx_b);
-          tma_load_3d(bring_base + i * C::kBTile, &p.b, 0, row, st * CH, &bfull_bar[i]);
-        } else {
-          tma_load_3d(stage_base + i * stage_bytes + NA * C::kATile, &p.b, 0, row, st * CH, &full_bar[i]);
-        }
+        uint8_t* dst = kSepB ? bring_base + bs * C::kBTile : stage_base + fs * stage_bytes + NA * C::kATile;
+        tma_load_3d(dst, &p.b, 0, row, st * CH, &full_bar[fs]);
       };
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
@@ -394,7 +395,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             // ring full: wait for the previous kernel, then load the deferred activations
             pdl_wait();
             waited = true;
-            for (int i = 0; i < n_deferred; ++i) load_b(i, deferred_pos[i], deferred_s[i]);
+            for (int i = 0; i < n_deferred; ++i) load_b(i, i, deferred_pos[i], deferred_s[i]);
           }
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, p.wait_limit)) { give_up(); ok = false; break; }
           uint8_t* sa = stage_base + slot * stage_bytes;
@@ -413,15 +414,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             if constexpr (kSepB) {
               const int bs = (int)(g & 1u);
               if (!mbar_wait(&bempty_bar[bs], ((g >> 1) & 1u) ^ 1u, p.wait_limit)) { give_up(); ok = false; break; }
-              load_b(bs, un.pos0, s);
-              last_bparity[bs] = (int)((g >> 1) & 1u);
+              load_b(bs, slot, un.pos0, s);
             } else {
-              load_b(slot, un.pos0, s);
+              load_b(0, slot, un.pos0, s);
             }
           } else {
-            deferred_pos[n_deferred] = un.pos0;  // the B slot is n_deferred while g < defer_cap
+            // while g < defer_cap the B slot and the stage slot are both g
+            deferred_pos[n_deferred] = un.pos0;
             deferred_s[n_deferred++] = s;
-            if constexpr (kSepB) last_bparity[n_deferred - 1] = 0;
           }
 #pragma unroll
           for (int i = 0; i < kMaxStages; ++i)
@@ -431,16 +431,13 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       }
       if (!waited) {
         pdl_wait();
-        for (int i = 0; i < n_deferred; ++i) load_b(i, deferred_pos[i], deferred_s[i]);
+        for (int i = 0; i < n_deferred; ++i) load_b(i, i, deferred_pos[i], deferred_s[i]);
       }
-      // never leave with copies in flight: wait for the last load into each slot
+      // never leave with copies in flight: wait for the last load into each
+      // slot (the activation copies land on the same barriers)
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s)
         if (last_parity[s] >= 0) mbar_wait(&full_bar[s], (uint32_t)last_parity[s], kDrainLimit);
-      if constexpr (kSepB) {
-        for (int i = 0; i < 2; ++i)
-          if (last_bparity[i] >= 0) mbar_wait(&bfull_bar[i], (uint32_t)last_bparity[i], kDrainLimit);
-      }
     }
   } else if (warp == 1 || warp == kIssuer2Warp) {
     // ---------------------------------------------------------------- MMA
@@ -484,8 +481,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         for (int s = s_beg; s < s_end; ++s, ++g) {
           const int slot = g % NS;
           const uint32_t ph = (g / NS) & 1;
-          if (!mbar_wait(&full_bar[slot], ph, p.wait_limit) || !mbar_wait(&sf_bar[slot], ph, p.wait_limit) ||
-              (kSepB && !mbar_wait(&bfull_bar[g & 1u], (g >> 1) & 1u, p.wait_limit))) {
+          if (!mbar_wait(&full_bar[slot], ph, p.wait_limit)) {
             give_up();
             ok = false;
             break;
@@ -625,7 +621,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           tmem_st_wait();
           fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sf_bar[slot]);
+          if (lane == 0) mbar_arrive(&full_bar[slot]);
           ++g;
         }
         return true;
