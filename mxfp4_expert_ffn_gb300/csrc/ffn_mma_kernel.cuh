@@ -278,7 +278,6 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   // shortens the time a stage holds its slot.
   __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar[2];
-  __shared__ __align__(8) uint64_t bempty_bar[2];  // the separate B ring's slots (kSepB)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -323,7 +322,6 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       mbar_init(&accf_bar[b], 2);
       mbar_init(&acce_bar[b], 4);
       mbar_init(&drain_bar[b], 1);
-      mbar_init(&bempty_bar[b], 2);
     }
     abort_flag = 0;
     fence_barrier_init();
@@ -412,8 +410,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           }
           if (waited) {
             if constexpr (kSepB) {
+              // B slot g % 2 was last read by stage g - 2, whose MMAs
+              // completing is the latest phase of that stage's empty
+              // barrier (stage g + 1, its next user, is not issued yet)
               const int bs = (int)(g & 1u);
-              if (!mbar_wait(&bempty_bar[bs], ((g >> 1) & 1u) ^ 1u, p.wait_limit)) { give_up(); ok = false; break; }
+              if (g >= 2u) {
+                const uint32_t g2 = g - 2u;
+                if (!mbar_wait(&empty_bar[g2 % NS], (g2 / NS) & 1u, p.wait_limit)) { give_up(); ok = false; break; }
+              }
               load_b(bs, slot, un.pos0, s);
             } else {
               load_b(0, slot, un.pos0, s);
@@ -524,7 +528,6 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
               }
             }
           mma_commit(&empty_bar[slot]);
-          if constexpr (kSepB) mma_commit(&bempty_bar[g & 1u]);
         }
         if (!ok) break;
         mma_commit(&accf_bar[buf]);
