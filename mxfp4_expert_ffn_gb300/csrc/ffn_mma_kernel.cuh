@@ -41,6 +41,7 @@ struct MmaParams {
   CUtensorMap a_routed[2];   // up mode: gate, up banks; down mode: down bank in [0]
   CUtensorMap a_shared[2];
   CUtensorMap b;             // activations by position, 3-D view of [P][K] E4M3
+  CUtensorMap b16;           // b_ragged: the same rows, 16 per copy
   const uint8_t* sa_routed[2];
   const uint8_t* sa_shared[2];
   const uint8_t* sb;         // activation scales by position, [P][K/32]
@@ -62,6 +63,8 @@ struct MmaParams {
   int split_ok;              // part/cnt are large enough for this launch
   int dense;                 // up mode, T <= 64: B = the codes of all tokens (token-major), read by TMA
   int b_rows;                // activation rows one B copy brings (dense: T rounded up to 16; else BN)
+  int b_ragged;              // gate/up, 64-token tiles by position: a unit of up to 16 positions
+                             // copies and multiplies 16 rows (b16), a larger one its rows rounded up to 16
   int fuse_combine;          // down mode, BN <= 64: the last writer of a token's rows combines them
   int T, k, ns;              // tokens (dense, fuse_combine), top-k, shared experts (fuse_combine)
   const int32_t* slot_pos;   // fuse_combine: position of slot t*k + j (-1: invalid id)
@@ -301,8 +304,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   // 128-element chunk row, unpacked into 128; A4: 128 bytes, stored as is),
   // and the activation rows
   const uint32_t tx_a = NA * 128 * (A4 ? 128 : 64) * CH;
-  const uint32_t tx_b = (uint32_t)BR * 128 * CH;
-  const uint32_t tx_stage = tx_a + tx_b;  // the activation copy lands on the stage's barrier too
+  const uint32_t tx_b = (uint32_t)BR * 128 * CH;  // the activation copy lands on the stage's barrier too
+  // 64-token tiles by position (not dense): most units hold far fewer than 64
+  // positions, so a unit of up to 16 copies 16 rows (one 16-row copy per
+  // stage; its chunks then lie 16 rows apart in shared memory) and every unit
+  // multiplies only its rows rounded up to 16 (less shared-memory traffic per
+  // stage for the copies and the MMAs)
+  const bool ragged_b = BN == 64 && !dense && p.b_ragged;
+  auto small_b = [&](const Unit& un) { return ragged_b && un.m_tile <= 16; };
   const uint32_t sf_col0 = C::kNAcc * C::kAccCols;
 
   if (threadIdx.x == 0) {
@@ -372,11 +381,12 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       // the activation tile of stage g, one op into the stage's own area or
       // the B ring's slot bs, landing on the stage's full barrier fs; dense:
       // rows 0.. of the token-major codes
-      auto load_b = [&](int bs, int fs, int pos0, int st) {
+      auto load_b = [&](int bs, int fs, int pos0, int st, bool b16) {
         const int row = dense ? 0 : pos0;
         uint8_t* dst = kSepB ? bring_base + bs * C::kBTile : stage_base + fs * stage_bytes + NA * C::kATile;
-        tma_load_3d(dst, &p.b, 0, row, st * CH, &full_bar[fs]);
+        tma_load_3d(dst, b16 ? &p.b16 : &p.b, 0, row, st * CH, &full_bar[fs]);
       };
+      bool deferred_b16[kMaxStages];
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
       Sched sc = sc0;
@@ -384,6 +394,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
         const bool sh = un.e >= p.E;
         const int erow = (sh ? un.e - p.E : un.e - p.e_lo) * p.rows + un.row0;
+        const bool b16 = small_b(un);
         bool ok = true;
         const int s_end = pc.s1;
         for (int s = pc.s0; s < s_end; ++s, ++g) {
@@ -393,12 +404,13 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             // ring full: wait for the previous kernel, then load the deferred activations
             pdl_wait();
             waited = true;
-            for (int i = 0; i < n_deferred; ++i) load_b(i, i, deferred_pos[i], deferred_s[i]);
+            for (int i = 0; i < n_deferred; ++i) load_b(i, i, deferred_pos[i], deferred_s[i], deferred_b16[i]);
           }
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, p.wait_limit)) { give_up(); ok = false; break; }
           uint8_t* sa = stage_base + slot * stage_bytes;
           // FP8 shared weights arrive as bytes: twice the packed FP4 count
-          mbar_expect_tx(&full_bar[slot], tx_stage + (shared_fp8_unit(pc.u) ? NA * 128 * 64 * CH : 0));
+          mbar_expect_tx(&full_bar[slot], tx_a + (b16 ? 16u * 128u * CH : tx_b) +
+                                              (shared_fp8_unit(pc.u) ? NA * 128 * 64 * CH : 0));
           if (NA == 2 && p.merged[sh]) {
             // gate and up rows of the stage in one op: {chunk elems, rows, chunks, matrix}
             tma_load_4d(sa, sh ? &p.a_shared[0] : &p.a_routed[0], 0, erow, s * CH, 0, &full_bar[slot]);
@@ -418,13 +430,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
                 const uint32_t g2 = g - 2u;
                 if (!mbar_wait(&empty_bar[g2 % NS], (g2 / NS) & 1u, p.wait_limit)) { give_up(); ok = false; break; }
               }
-              load_b(bs, slot, un.pos0, s);
+              load_b(bs, slot, un.pos0, s, b16);
             } else {
-              load_b(0, slot, un.pos0, s);
+              load_b(0, slot, un.pos0, s, b16);
             }
           } else {
             // while g < defer_cap the B slot and the stage slot are both g
             deferred_pos[n_deferred] = un.pos0;
+            deferred_b16[n_deferred] = b16;
             deferred_s[n_deferred++] = s;
           }
 #pragma unroll
@@ -435,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       }
       if (!waited) {
         pdl_wait();
-        for (int i = 0; i < n_deferred; ++i) load_b(i, i, deferred_pos[i], deferred_s[i]);
+        for (int i = 0; i < n_deferred; ++i) load_b(i, i, deferred_pos[i], deferred_s[i], deferred_b16[i]);
       }
       // never leave with copies in flight: wait for the last load into each
       // slot (the activation copies land on the same barriers)
@@ -461,13 +474,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
         const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
         const uint32_t d_tmem = tmem + buf * C::kAccCols;
-        int swap = 0, NI = NI0;
-        if (C::kRagged) {
-          // the wide tiles are often part-filled: N = the tile's tokens
-          // rounded up to the instruction's step of 16, so the MMAs cost
-          // only the columns in use (the epilogue reads no column past them)
+        int swap = 0, NI = NI0, brows = BR;
+        if (C::kRagged || ragged_b) {
+          // part-filled tiles: N = the tile's tokens rounded up to the
+          // instruction's step of 16, so the MMAs cost only the columns in
+          // use (the epilogue reads no column past them)
           const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
           NI = min(BN, (un.m_tile + 15) & ~15);
+          if (small_b(un)) brows = 16;  // its B chunks lie 16 rows apart
         }
         if (NA == 2) {
           // the shared experts' tiles close the table, so no table load is
@@ -506,8 +520,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
               const int w = A4 ? k >> 1 : 0;
               const uint32_t sfid = A4 ? (uint32_t)(k & 1) * 2u : (uint32_t)k;
               const uint32_t idesc = idesc_base | (sfid << 4) | (sfid << 29);
-              // chunk c of the B tile starts after c chunks of BR rows of 128 bytes
-              const uint64_t bdesc = b_desc0 + (uint64_t)((c * BR * 128 + 32 * k) >> 4);
+              // chunk c of the B tile starts after c chunks of brows rows of 128 bytes
+              const uint64_t bdesc = b_desc0 + (uint64_t)((c * brows * 128 + 32 * k) >> 4);
               const uint32_t sfb = sf + C::sfb_col(c, w, 0);
               auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfbb, uint32_t accumulate) {
                 if constexpr (A4)
