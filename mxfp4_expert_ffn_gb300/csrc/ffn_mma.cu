@@ -202,7 +202,8 @@ cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, 
     }
     p.b = mm.xg[bi];
     p.b16 = mm.xg[0];
-    p.b_ragged = bn == 64;
+    p.b64 = mm.xg[1];
+    p.b_ragged = bn >= 64;
     p.b_rows = bn;
     p.sa_routed[0] = bk.gs;
     p.sa_routed[1] = bk.us;

@@ -41,7 +41,7 @@ struct MmaParams {
   CUtensorMap a_routed[2];   // up mode: gate, up banks; down mode: down bank in [0]
   CUtensorMap a_shared[2];
   CUtensorMap b;             // activations by position, 3-D view of [P][K] E4M3
-  CUtensorMap b16;           // b_ragged: the same rows, 16 per copy
+  CUtensorMap b16, b64;      // b_ragged: the same rows, 16 / 64 per copy
   const uint8_t* sa_routed[2];
   const uint8_t* sa_shared[2];
   const uint8_t* sb;         // activation scales by position, [P][K/32]
@@ -63,8 +63,9 @@ struct MmaParams {
   int split_ok;              // part/cnt are large enough for this launch
   int dense;                 // up mode, T <= 64: B = the codes of all tokens (token-major), read by TMA
   int b_rows;                // activation rows one B copy brings (dense: T rounded up to 16; else BN)
-  int b_ragged;              // gate/up, 64-token tiles by position: a unit of up to 16 positions
-                             // copies and multiplies 16 rows (b16), a larger one its rows rounded up to 16
+  int b_ragged;              // gate/up tiles by position: a unit of up to 16 positions copies 16
+                             // rows (b16), of up to 64 (112-token tiles) 64 rows (b64), else the
+                             // tile's; each multiplies its rows rounded up to 16
   int fuse_combine;          // down mode, BN <= 64: the last writer of a token's rows combines them
   int T, k, ns;              // tokens (dense, fuse_combine), top-k, shared experts (fuse_combine)
   const int32_t* slot_pos;   // fuse_combine: position of slot t*k + j (-1: invalid id)
@@ -302,16 +303,18 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   const int BR = p.b_rows;  // activation rows per B tile (the MMA's N, except ragged tiles)
   // bytes a stage's copies bring: the weights packed (FP4: 64 bytes per
   // 128-element chunk row, unpacked into 128; A4: 128 bytes, stored as is),
-  // and the activation rows
+  // and the activation rows (128 bytes per chunk row; the activation copy
+  // lands on the stage's barrier too)
   const uint32_t tx_a = NA * 128 * (A4 ? 128 : 64) * CH;
-  const uint32_t tx_b = (uint32_t)BR * 128 * CH;  // the activation copy lands on the stage's barrier too
-  // 64-token tiles by position (not dense): most units hold far fewer than 64
-  // positions, so a unit of up to 16 copies 16 rows (one 16-row copy per
-  // stage; its chunks then lie 16 rows apart in shared memory) and every unit
+  // Tiles by position (not dense) are often part-filled, so a unit copies
+  // the smallest of 16, 64 or BN rows that holds its positions (one copy per
+  // stage; its chunks then lie that many rows apart in shared memory) and
   // multiplies only its rows rounded up to 16 (less shared-memory traffic per
   // stage for the copies and the MMAs)
-  const bool ragged_b = BN == 64 && !dense && p.b_ragged;
-  auto small_b = [&](const Unit& un) { return ragged_b && un.m_tile <= 16; };
+  const bool ragged_b = BN >= 64 && !dense && p.b_ragged;
+  auto b_rows_of = [&](const Unit& un) {
+    return !ragged_b ? BR : un.m_tile <= 16 ? 16 : (BN > 64 && un.m_tile <= 64) ? 64 : BR;
+  };
   const uint32_t sf_col0 = C::kNAcc * C::kAccCols;
 
   if (threadIdx.x == 0) {
@@ -381,12 +384,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       // the activation tile of stage g, one op into the stage's own area or
       // the B ring's slot bs, landing on the stage's full barrier fs; dense:
       // rows 0.. of the token-major codes
-      auto load_b = [&](int bs, int fs, int pos0, int st, bool b16) {
+      auto load_b = [&](int bs, int fs, int pos0, int st, int rows) {
         const int row = dense ? 0 : pos0;
         uint8_t* dst = kSepB ? bring_base + bs * C::kBTile : stage_base + fs * stage_bytes + NA * C::kATile;
-        tma_load_3d(dst, b16 ? &p.b16 : &p.b, 0, row, st * CH, &full_bar[fs]);
+        // the 16- and 64-row maps exist only for the ragged tiles (gate/up by position)
+        const CUtensorMap* map = !ragged_b ? &p.b : rows == 16 ? &p.b16 : (BN > 64 && rows == 64) ? &p.b64 : &p.b;
+        tma_load_3d(dst, map, 0, row, st * CH, &full_bar[fs]);
       };
-      bool deferred_b16[kMaxStages];
+      int deferred_rows[kMaxStages];
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
       Sched sc = sc0;
@@ -394,7 +399,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
         const bool sh = un.e >= p.E;
         const int erow = (sh ? un.e - p.E : un.e - p.e_lo) * p.rows + un.row0;
-        const bool b16 = small_b(un);
+        const int brows_u = b_rows_of(un);
         bool ok = true;
         const int s_end = pc.s1;
         for (int s = pc.s0; s < s_end; ++s, ++g) {
@@ -404,12 +409,12 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             // ring full: wait for the previous kernel, then load the deferred activations
             pdl_wait();
             waited = true;
-            for (int i = 0; i < n_deferred; ++i) load_b(i, i, deferred_pos[i], deferred_s[i], deferred_b16[i]);
+            for (int i = 0; i < n_deferred; ++i) load_b(i, i, deferred_pos[i], deferred_s[i], deferred_rows[i]);
           }
           if (!mbar_wait(&empty_bar[slot], ph ^ 1, p.wait_limit)) { give_up(); ok = false; break; }
           uint8_t* sa = stage_base + slot * stage_bytes;
           // FP8 shared weights arrive as bytes: twice the packed FP4 count
-          mbar_expect_tx(&full_bar[slot], tx_a + (b16 ? 16u * 128u * CH : tx_b) +
+          mbar_expect_tx(&full_bar[slot], tx_a + (uint32_t)brows_u * 128u * CH +
                                               (shared_fp8_unit(pc.u) ? NA * 128 * 64 * CH : 0));
           if (NA == 2 && p.merged[sh]) {
             // gate and up rows of the stage in one op: {chunk elems, rows, chunks, matrix}
@@ -430,14 +435,14 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
                 const uint32_t g2 = g - 2u;
                 if (!mbar_wait(&empty_bar[g2 % NS], (g2 / NS) & 1u, p.wait_limit)) { give_up(); ok = false; break; }
               }
-              load_b(bs, slot, un.pos0, s, b16);
+              load_b(bs, slot, un.pos0, s, brows_u);
             } else {
-              load_b(0, slot, un.pos0, s, b16);
+              load_b(0, slot, un.pos0, s, brows_u);
             }
           } else {
             // while g < defer_cap the B slot and the stage slot are both g
             deferred_pos[n_deferred] = un.pos0;
-            deferred_b16[n_deferred] = b16;
+            deferred_rows[n_deferred] = brows_u;
             deferred_s[n_deferred++] = s;
           }
 #pragma unroll
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       }
       if (!waited) {
         pdl_wait();
-        for (int i = 0; i < n_deferred; ++i) load_b(i, i, deferred_pos[i], deferred_s[i], deferred_b16[i]);
+        for (int i = 0; i < n_deferred; ++i) load_b(i, i, deferred_pos[i], deferred_s[i], deferred_rows[i]);
       }
       // never leave with copies in flight: wait for the last load into each
       // slot (the activation copies land on the same barriers)
@@ -481,7 +486,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           // use (the epilogue reads no column past them)
           const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
           NI = min(BN, (un.m_tile + 15) & ~15);
-          if (small_b(un)) brows = 16;  // its B chunks lie 16 rows apart
+          brows = b_rows_of(un);  // its B chunks lie that many rows apart
         }
         if (NA == 2) {
           // the shared experts' tiles close the table, so no table load is
