@@ -81,9 +81,13 @@ size_t carve(const moe_config& c, int num_sms, char* base, Workspace& ws) {
   // split partition of the tensor-core GEMM (few units, e.g. decode): two
   // partial slots per CTA and one counter per (unit, row quadrant), units < 4 * SMs
   ws.part_bn = mma_tile_for_tokens(c.max_tokens) < 64 ? mma_tile_for_tokens(c.max_tokens) : 64;
-  ws.part = cv.take<float>((size_t)2 * num_sms * 2 * ws.part_bn * 128);
-  ws.split_cnt_n = 2 * 4 * kSplitUnitsPerCta * num_sms;
+  // (one region per GEMM: down may start while gate/up finishes)
+  ws.part = cv.take<float>((size_t)2 * 2 * num_sms * 2 * ws.part_bn * 128);
+  ws.split_cnt_n = 2 * 4 * kSplitUnitsPerCta * num_sms + (int)NE + 2;
   ws.split_cnt = cv.take<int32_t>((size_t)ws.split_cnt_n);
+  ws.ready = ws.split_cnt + 2 * 4 * kSplitUnitsPerCta * num_sms;
+  ws.ready_done = ws.ready + NE;
+  ws.unit_next = ws.ready_done + 1;
   ws.prep_cnt = cv.take<int32_t>(16);
   ws.comb_cnt_n = kPrepMaxTokens * (int)(H / 128) * 4;
   ws.comb_cnt = cv.take<int32_t>((size_t)ws.comb_cnt_n);
@@ -497,7 +501,7 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool small, const float* w,
   {
     TimedScope ts(L, st, "ffn_up_mma");
     e = launch_ffn_mma(*L->maps, bank, 0, bn, small ? T : 0, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles,
-                       L->wait_limit);
+                       L->wait_limit, small);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   if (small && bn == 16 && c.n_shared > 0 && !y_f32) {
@@ -510,12 +514,12 @@ moe_status ffn_tail(moe_layer* L, int32_t T, int bn, bool small, const float* w,
                           static_cast<uint16_t*>(y)};
     TimedScope ts(L, st, "ffn_down_mma");
     return cuda_fail(launch_ffn_mma(*L->maps, bank, 1, bn, 0, L->ws, L->num_sms, st, &cmb, act4_of(L), ns_tiles,
-                                    L->wait_limit));
+                                    L->wait_limit, small));
   }
   {
     TimedScope ts(L, st, "ffn_down_mma");
     e = launch_ffn_mma(*L->maps, bank, 1, bn, 0, L->ws, L->num_sms, st, nullptr, act4_of(L), ns_tiles,
-                       L->wait_limit);
+                       L->wait_limit, small);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   {

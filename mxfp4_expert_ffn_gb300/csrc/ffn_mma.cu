@@ -181,7 +181,7 @@ void mma_maps_destroy(MmaMaps* m) { delete m; }
 
 cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, int bn, int dense_T,
                            const Workspace& ws, int num_sms, cudaStream_t st, const CombineArgs* cmb, bool act4,
-                           int ns_tiles, uint32_t wait_limit) {
+                           int ns_tiles, uint32_t wait_limit, bool early) {
   const FormatMaps& mm = maps.f[act4 ? 1 : 0];
   if (!mm.ok) return cudaErrorInvalidValue;
   MmaParams p;
@@ -247,9 +247,17 @@ cudaError_t launch_ffn_mma(const MmaMaps& maps, const ExpertBank& bk, int mode, 
   p.hq = ws.hq;
   p.hs = ws.hs;
   p.o = ws.o;
-  p.part = ws.part;
-  p.cnt = ws.split_cnt + (mode == kModeUp ? 0 : ws.split_cnt_n / 2);
-  p.split_ok = bn <= ws.part_bn && ws.split_cnt_n >= 2 * 4 * kSplitUnitsPerCta * num_sms;
+  const size_t part_n = (size_t)2 * num_sms * 2 * ws.part_bn * 128, cnt_n = (size_t)4 * kSplitUnitsPerCta * num_sms;
+  p.part = ws.part + (mode == kModeUp ? 0 : part_n);
+  p.cnt = ws.split_cnt + (mode == kModeUp ? 0 : cnt_n);
+  p.split_ok = bn <= ws.part_bn && ws.split_cnt_n >= (int)(2 * cnt_n);
+  if (early && bn == 64) {  // the EARLY kernel variant (see launch_bn)
+    p.ready = ws.ready;
+    p.ready_need = (int)(bk.I / 128) * 4;
+    p.ready_done = ws.ready_done;
+    p.unit_next = ws.unit_next;
+    p.down_mt = (int)(bk.H / 128);
+  }
   p.err = ws.err;
   if (mode == kModeDown && cmb && bn <= 64) {
     p.fuse_combine = 1;

@@ -79,6 +79,13 @@ struct MmaParams {
   int ns_tiles;              // token tiles of the shared experts (the last ones of the table)
   int shared_first;          // process the shared experts' tiles first (fuse_combine: see the kernel)
   int32_t* err;
+  int32_t* ready;            // small batches: gate/up units finished per token tile (gate/up counts;
+                             // down waits per unit for its tile, not for the whole gate/up launch)
+  int ready_need;            // down: the count that makes a tile final (gate/up units per tile x 4 warps)
+  int32_t* ready_done;       // gate/up CTAs finished (each adds one as it leaves)
+  int32_t* unit_next;        // down, whole units: the launch-wide counter of units taken
+  int down_mt;               // 128-row tiles of the down matrix (H / 128): both kernels tell from
+                             // the tile count whether down runs whole units (then the above apply)
 };
 
 namespace {
@@ -90,11 +97,21 @@ constexpr int kIssuer2Warp = 10;
 // Polls for the waits that let copies and MMAs already issued complete before
 // the CTA leaves (they always end: the hardware finishes what was issued).
 constexpr uint32_t kDrainLimit = 1u << 24;
+// Polls of a tile's gate/up count before down waits for the whole gate/up
+// launch instead (always correct; the counts only let it start earlier).
+constexpr uint32_t kReadyPolls = 1u << 16;
+// Entries of the shared-memory queue that hands dynamically taken units from
+// the producer to the other roles.  Writing entry i, the producer has waited
+// for the MMAs of a stage of unit i - 1 - NS (or later), so the MMA issuer has
+// taken unit i - 1 - NS, which means the epilogue (the last reader) has taken
+// unit i - 3 - NS: with NS <= 6 no entry is overwritten before all have read it.
+constexpr int kUq = 16;
 constexpr int kSmemBudget = 227 * 1024 - 2048;
 
 constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
 
 constexpr int kMaxStages = 6;
+static_assert(kUq >= kMaxStages + 4, "unit queue depth");
 
 // A4: the FP4-activation variant (both operands packed E2M1, kind::mxf4):
 // a 128-byte chunk of a row holds 256 K elements instead of 128, and its
@@ -267,7 +284,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-template <int MODE, int BN, int CH, bool A4>
+template <int MODE, int BN, int CH, bool A4, bool EARLY>
 __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_constant__ MmaParams p) {
   using C = Cfg<MODE, BN, CH, A4>;
   constexpr int NA = C::kNA;
@@ -284,6 +301,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
   __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ uint32_t uq[kUq];  // (entry number + 1) << 16 | (unit + 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt_per_expert = p.rows / 128;
@@ -335,6 +353,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       mbar_init(&acce_bar[b], 4);
       mbar_init(&drain_bar[b], 1);
     }
+    for (int i = 0; i < kUq; ++i) uq[i] = 0u;
     abort_flag = 0;
     fence_barrier_init();
   }
@@ -369,6 +388,73 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     *(volatile int*)&abort_flag = 1;
   };
   auto aborted = [&]() { return *(volatile int*)&abort_flag != 0; };
+  // Down after a small batch's gate/up: the activations of a unit (h of its
+  // token tile) are final once gate/up has counted every unit of that tile
+  // (each epilogue warp counts its 32 rows of a unit after writing them), so
+  // each role waits for its unit's tile rather than for the whole previous
+  // launch.  h then reaches the tensor copies (async proxy) and the scale
+  // loads.  A wait that runs out of polls falls back to the launch wait.
+  // Only when down runs whole units (not the split partition of a decode
+  // step, where the counting costs more than the earlier start brings); both
+  // kernels decide from the same tile count.
+  // The code exists only in the EARLY variant (small batches with 64-token
+  // tiles): compiled into the others, even unused, it slowed them.
+  const bool early_on =
+      EARLY && p.ready != nullptr && n_tiles * p.down_mt >= kSplitUnitsPerCta * (int)gridDim.x;
+  const bool early = MODE == kModeDown && early_on;
+  auto wait_tile = [&](int u, bool& all) {
+    if (all) return;
+    // once every gate/up CTA has left, no later unit needs a look
+    if (ld_acquire_gpu(p.ready_done) >= (int)gridDim.x) {
+      fence_proxy_async_global();
+      all = true;
+      return;
+    }
+    const int32_t* r = p.ready + tile_of(u, mt_units, rot, n_tiles);
+    const uint32_t lim = p.wait_limit < kReadyPolls ? p.wait_limit : kReadyPolls;
+    for (uint32_t i = 0; i < lim; ++i) {
+      if (ld_acquire_gpu(r) >= p.ready_need) {
+        fence_proxy_async_global();
+        return;
+      }
+      __nanosleep(64);
+    }
+    pdl_wait();
+    all = true;
+  };
+  // Early down with whole units: CTAs that start while gate/up finishes
+  // take more units.  The producer takes the next unit from a launch-wide
+  // counter (one unit ahead, so the atomic's latency hides behind a unit's
+  // copies) and hands each unit to the other roles through the queue; -1 ends
+  // it.  Which CTA computes a unit changes nothing in the unit's arithmetic.
+  // Each CTA's first unit is its own index; the counter hands out the rest.
+  const bool dyn = early && !sc0.split && total < 0xFFFF;
+  int dyn_cur = 0;
+  auto uq_tag = [](uint32_t i) { return ((i & 0x7FFFu) + 1u) << 16; };
+  auto next_producer = [&](Sched& sc, uint32_t& i) -> Piece {
+    if (!dyn) return sc.next();
+    const int u = dyn_cur < total ? dyn_cur : -1;
+    if (u >= 0) dyn_cur = (int)gridDim.x + atomicAdd(p.unit_next, 1);
+    *(volatile uint32_t*)&uq[i % kUq] = uq_tag(i) | (uint32_t)(u + 1);
+    ++i;
+    return u >= 0 ? Piece{u, 0, k_stages} : Piece{-1, 0, 0};
+  };
+  auto next_reader = [&](Sched& sc, uint32_t& i) -> Piece {
+    if (!dyn) return sc.next();
+    const uint32_t want = uq_tag(i);
+    const volatile uint32_t* e = &uq[i % kUq];
+    ++i;
+    uint32_t v = *e, n = 0;
+    while ((v & 0xFFFF0000u) != want) {
+      if (++n >= p.wait_limit) {
+        give_up();
+        return Piece{-1, 0, 0};
+      }
+      v = *e;
+    }
+    const int u = (int)(v & 0xFFFFu) - 1;
+    return u >= 0 ? Piece{u, 0, k_stages} : Piece{-1, 0, 0};
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
@@ -376,8 +462,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       uint32_t g = 0;
       int last_parity[kMaxStages];
       int deferred_pos[kMaxStages], deferred_s[kMaxStages], n_deferred = 0;
-      // dense mode runs after the preparation kernel and waited for it above
-      bool waited = dense;
+      // dense mode runs after the preparation kernel and waited for it above;
+      // early down waits per unit (wait_tile) before the unit's first B copy
+      bool waited = dense || early, all_ready = false;
       // B copies issued before the previous kernel is waited for: as many as
       // there are slots to hold them
       const uint32_t defer_cap = kSepB ? 2u : (uint32_t)NS;
@@ -395,7 +482,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
       Sched sc = sc0;
-      for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next()) {
+      uint32_t qi = 0;
+      dyn_cur = (int)blockIdx.x;
+      for (Piece pc = next_producer(sc, qi); pc.u >= 0 && !aborted(); pc = next_producer(sc, qi)) {
         const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
         const bool sh = un.e >= p.E;
         const int erow = (sh ? un.e - p.E : un.e - p.e_lo) * p.rows + un.row0;
@@ -425,6 +514,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
               tma_load_3d(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
                           &full_bar[slot]);
           }
+          if (early && s == pc.s0) wait_tile(pc.u, all_ready);
           if (waited) {
             if constexpr (kSepB) {
               // B slot g % 2 was last read by stage g - 2, whose MMAs
@@ -475,7 +565,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       const int NI0 = BR;
       uint32_t g = 0, it = 0;
       Sched sc = sc0;
-      for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
+      uint32_t qi = 0;
+      for (Piece pc = next_reader(sc, qi); pc.u >= 0 && !aborted(); pc = next_reader(sc, qi), ++it) {
         const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
         const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
         const uint32_t d_tmem = tmem + buf * C::kAccCols;
@@ -565,11 +656,12 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     constexpr int KW = C::kW;                                    // scale words per row and chunk
     constexpr int NB = 4, NW = (NA * CH + NC * CH) * KW;  // words per stage
     const int q = warp & 3;
-    pdl_wait();  // the activation scales come from the previous kernel
+    if (!early) pdl_wait();  // the activation scales come from the previous kernel
     uint32_t g = 0;
-    bool ok = true;
+    bool ok = true, all_ready = false;
     Sched sc = sc0;
-    for (Piece pc = sc.next(); ok && pc.u >= 0 && !aborted(); pc = sc.next()) {
+    uint32_t qi = 0;
+    for (Piece pc = next_reader(sc, qi); ok && pc.u >= 0 && !aborted(); pc = next_reader(sc, qi)) {
       const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
       const int s_end = pc.s1;
       const bool sh = un.e >= p.E;
@@ -616,7 +708,11 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
 #pragma unroll
                 for (int cb = 0; cb < NC; ++cb)
                   w[i][(NA * CH + c * NC + cb) * KW + v] =
-                      sb_row[cb] ? __ldg(reinterpret_cast<const uint32_t*>(sb_row[cb] + kb)) : 0x7F7F7F7Fu;
+                      !sb_row[cb] ? 0x7F7F7F7Fu
+                      // early down: written by the running gate/up launch, so not through
+                      // the read-only cache (a line may hold an earlier tile's scales)
+                      : (early && !all_ready) ? __ldcg(reinterpret_cast<const uint32_t*>(sb_row[cb] + kb))
+                              : __ldg(reinterpret_cast<const uint32_t*>(sb_row[cb] + kb));
               }
           }
         }
@@ -649,6 +745,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         return true;
       };
       uint32_t w0[NB][NW], w1[NB][NW];
+      if (early) wait_tile(pc.u, all_ready);
       load(w0, pc.s0);
       for (int s0 = pc.s0; s0 < s_end; s0 += 2 * NB) {
         if (s0 + NB < s_end) load(w1, s0 + NB);
@@ -662,7 +759,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;        // TMEM lane quadrant of this warp
     const int rl = 32 * q + lane;  // row within the 128-row tile
-    pdl_wait();
+    // early down writes nothing the running gate/up reads (its partial tiles
+    // have a region of their own)
+    if (!early) pdl_wait();
     // h of one position at this lane's row, given the 32-row block maximum:
     // FP8 one code per row; FP4 (A4) two rows per byte, the even lane writing
     // its row (low nibble) and the next one's.  Lane 0 writes the scale.
@@ -808,9 +907,21 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
       }
       tmem_ld_wait();
     };
+    // small batches, gate/up: count this warp's 32 rows of a finished unit
+    // toward its tile (down reads them by tensor copies: proxy fence first)
+    auto count_tile = [&](int u) {
+      if constexpr (MODE == kModeUp) {
+        if (!early_on) return;
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.ready + tile_of(u, mt_units, rot, n_tiles), 1);
+      }
+    };
     uint32_t it = 0;
     Sched sc = sc0;
-    for (Piece pc = sc.next(); pc.u >= 0 && !aborted(); pc = sc.next(), ++it) {
+    uint32_t qi = 0;
+    for (Piece pc = next_reader(sc, qi); pc.u >= 0 && !aborted(); pc = next_reader(sc, qi), ++it) {
       const Unit un = decode_unit(p, pc.u, mt_units, rot, n_tiles);
       const int buf = C::kNAcc == 2 ? (int)(it & 1) : 0;
       const uint32_t ph_acc = C::kNAcc == 2 ? ((it >> 1) & 1) : (it & 1);
@@ -834,6 +945,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
           }
           emit16(un, i0, v, vu);  // down split-K: the two K halves, in fixed order
         }
+        count_tile(pc.u);
         combine_tail(un);
         continue;
       }
@@ -891,26 +1003,35 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
             emit(un, col, a, b);
           }
           if (lane == 0) p.cnt[pc.u * 4 + q] = 0;
+          count_tile(pc.u);
           combine_tail(un);
         }
       }
     }
   }
+  // early down: this launch completes only after gate/up's (as the launch
+  // order promises the kernels after it)
+  if (early && threadIdx.x == 0) pdl_wait();
   fence_before();
   __syncthreads();
+  if (MODE == kModeUp && early_on && threadIdx.x == 0) {
+    // every unit of this CTA is counted (its warps' counts came before the barrier)
+    __threadfence();
+    atomicAdd(p.ready_done, 1);
+  }
   if (warp == 1) {
     fence_after();
     tmem_dealloc(tmem, C::kTmemAlloc);
   }
 }
 
-template <int MODE, int BN, int CH, bool A4>
+template <int MODE, int BN, int CH, bool A4, bool EARLY = false>
 cudaError_t launch_one(MmaParams& p, int num_sms, cudaStream_t st) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_mma_kernel<MODE, BN, CH, A4>,
+    cudaError_t e = cudaFuncSetAttribute(ffn_mma_kernel<MODE, BN, CH, A4, EARLY>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -918,7 +1039,7 @@ cudaError_t launch_one(MmaParams& p, int num_sms, cudaStream_t st) {
   int smem = 0;
   geometry<MODE, BN, CH, A4>(p.K, &p.n_stages, &smem);
   if (p.n_stages < 2) return cudaErrorInvalidConfiguration;
-  cudaError_t e = launch_pdl(ffn_mma_kernel<MODE, BN, CH, A4>, dim3(num_sms), dim3(kThreadsMma), smem, st, p);
+  cudaError_t e = launch_pdl(ffn_mma_kernel<MODE, BN, CH, A4, EARLY>, dim3(num_sms), dim3(kThreadsMma), smem, st, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -926,7 +1047,11 @@ cudaError_t launch_one(MmaParams& p, int num_sms, cudaStream_t st) {
 template <int MODE, int CH, bool A4>
 cudaError_t launch_bn(MmaParams& p, int bn, int num_sms, cudaStream_t st) {
   if (bn == 16) return launch_one<MODE, 16, CH, A4>(p, num_sms, st);
-  if (bn == 64) return launch_one<MODE, 64, CH, A4>(p, num_sms, st);
+  // small batches with 64-token tiles (17 to 64 tokens): the variant whose
+  // down starts per token tile (the code costs the other launches time even
+  // unused, so it is a variant of its own)
+  if (bn == 64)
+    return p.ready ? launch_one<MODE, 64, CH, A4, true>(p, num_sms, st) : launch_one<MODE, 64, CH, A4, false>(p, num_sms, st);
   return launch_one<MODE, 112, CH, A4>(p, num_sms, st);
 }
 

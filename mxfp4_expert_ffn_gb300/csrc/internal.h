@@ -52,9 +52,12 @@ struct Workspace {
   float* w = nullptr;         // [T][k]
   uint16_t* x = nullptr;      // [T][H]     bf16 staging (host entry point)
   uint16_t* y = nullptr;      // [T][H]
-  float* part = nullptr;      // [2*SMs][2][part_bn][128] split-partition partial tiles
-  int32_t* split_cnt = nullptr; // [2][16*SMs] split-partition counters (up, down)
-  int split_cnt_n = 0;        // entries of split_cnt (zeroed by the segments kernel)
+  float* part = nullptr;      // [2][2*SMs][2][part_bn][128] split-partition partial tiles (up, down)
+  int32_t* split_cnt = nullptr; // [2][16*SMs] split-partition counters (up, down), then ready
+  int split_cnt_n = 0;        // entries of split_cnt and ready (zeroed by the segments kernel)
+  int32_t* ready = nullptr;   // [NE]       gate/up units finished per token tile (small batches)
+  int32_t* ready_done = nullptr; // [1]     gate/up CTAs finished (small batches)
+  int32_t* unit_next = nullptr;  // [1]     down: units taken (small batches, whole units)
   int part_bn = 0;            // token-tile width the partial slots are sized for
   int32_t* prep_cnt = nullptr;// [16]       small-batch preparation counters (zero between launches)
   int32_t* comb_cnt = nullptr;// [64][H/128][4] fused-combine counters (zeroed by the segments)
@@ -201,10 +204,14 @@ struct CombineArgs {
 // act4: the FP4-activation variant (xg/xq/hq hold packed E2M1 codes).
 // ns_tiles: token tiles of the shared experts (n_shared x ceil(T / bn)).
 // wait_limit: polls after which a pipeline wait gives up (MOE_OPT_WAIT_LIMIT).
+// early: with 64-token tiles, gate/up counts its finished units per token
+// tile in ws.ready and down takes whole units dynamically, each waiting for
+// its tile instead of for the whole gate/up launch (the small-batch path: the
+// preparation kernel zeroed the counts; at most NE tiles).
 cudaError_t launch_ffn_mma(const MmaMaps& mm, const ExpertBank& bk, int mode, int bn, int dense_T,
                            const Workspace& ws, int num_sms, cudaStream_t st,
                            const CombineArgs* cmb = nullptr, bool act4 = false, int ns_tiles = 0,
-                           uint32_t wait_limit = 1u << 24);
+                           uint32_t wait_limit = 1u << 24, bool early = false);
 // Re-encodes the shared experts' maps for MXFP4 or FP8 (32 x 32 block) weights.
 bool mma_maps_set_shared_format(MmaMaps* m, const moe_config& c, const moe_weights& w, bool fp8);
 // FP4 activations need H and I multiples of 256 (whole 128-byte chunks).
