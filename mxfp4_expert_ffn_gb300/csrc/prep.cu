@@ -90,15 +90,13 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
     }
   }
 
-  // ---- 1b. FP8 codes of x by token, 8 values per thread, spread over all CTAs
-  // (and, for the one-warp segments, the zeroing of the GEMMs' arrival counters)
+  // ---- 1b. FP8 codes of x by token, 8 values per thread, spread over all CTAs,
+  // and the zeroing of the GEMMs' arrival counters (off the serial segments)
   {
     const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
     const int stride = gridDim.x * gridDim.y * gridDim.z * blockDim.x;
-    if (tiny) {
-      for (int i = cta * blockDim.x + threadIdx.x; i < p.ws.split_cnt_n; i += stride) p.ws.split_cnt[i] = 0;
-      for (int i = cta * blockDim.x + threadIdx.x; i < p.ws.comb_cnt_n; i += stride) p.ws.comb_cnt[i] = 0;
-    }
+    for (int i = cta * blockDim.x + threadIdx.x; i < p.ws.split_cnt_n; i += stride) p.ws.split_cnt[i] = 0;
+    for (int i = cta * blockDim.x + threadIdx.x; i < p.ws.comb_cnt_n; i += stride) p.ws.comb_cnt[i] = 0;
     const int n8 = p.parts_ready ? 0 : p.T * (p.H / 8);  // a multiple of 4: whole quads stay in or out
     const unsigned quad = 0xFu << (lane & ~3);
     const uint4* x8 = reinterpret_cast<const uint4*>(p.x);
@@ -170,9 +168,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
   if (tiny)
     segments_tiny(sid_s, p.T, p.k, p.E, p.ns, p.ws);
   else if (p.T * p.k <= (int)blockDim.x)
-    segments_small_cta(p.idx, p.T, p.k, p.E, p.ns, p.bn, p.ws, sm);
+    segments_small_cta(p.idx, p.T, p.k, p.E, p.ns, p.bn, p.ws, sm, false);
   else
-    segments_cta(p.idx, p.T, p.k, p.E, p.ns, p.bn, p.ws, sm);
+    segments_cta(p.idx, p.T, p.k, p.E, p.ns, p.bn, p.ws, sm, false, false);
 }
 
 size_t prep_smem_bytes(int E, int H) {

@@ -110,9 +110,12 @@ __device__ __forceinline__ void scan_experts(const int32_t* cnt_s, int E, int T,
 // stable counting sort, identical on every run.
 // Needs blockDim.x == 1024 and sm = 36 * E + 2 * ns + 1 ints of shared memory; every
 // thread of the CTA must call it.
+// zero_counts: zero the GEMMs' split-partition (and per-tile) counters and the
+// fused-combine counters here (the preparation kernel does it in its parallel
+// phase instead).
 __device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx, int T, int k, int E,
                                              int ns, int bn, const Workspace& ws, int32_t* sm,
-                                             bool scatter_smem = false) {
+                                             bool scatter_smem = false, bool zero_counts = true) {
   const int NE = E + ns;
   int32_t* wcnt = sm;                  // [32][E] per-warp counts, then running bases
   int32_t* stot = sm + 32 * E;         // [E]     slots per expert
@@ -124,10 +127,12 @@ __device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx, in
   const int S = T * k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
-  // the tensor-core GEMM's split-partition counters start every forward at zero
-  for (int i = threadIdx.x; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
-  // and so do the fused-combine counters
-  for (int i = threadIdx.x; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
+  if (zero_counts) {
+    // the tensor-core GEMM's split-partition counters start every forward at zero
+    for (int i = threadIdx.x; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
+    // and so do the fused-combine counters
+    for (int i = threadIdx.x; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
+  }
   __syncthreads();
   // Each warp owns slots [lo, hi) and reads their expert ids eight rows of 32
   // at a time (all eight loads in flight before they are used).
@@ -237,7 +242,8 @@ __device__ __forceinline__ void segments_cta(const int32_t* __restrict__ idx, in
 // the earlier equal slots (so the order is the stable one above, bit for bit).
 // sm needs 4 * E + 2 * ns + T * k + 1 ints.
 __device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ idx, int T, int k, int E,
-                                                   int ns, int bn, const Workspace& ws, int32_t* sm) {
+                                                   int ns, int bn, const Workspace& ws, int32_t* sm,
+                                                   bool zero_counts = true) {
   const int NE = E + ns, S = T * k, tid = threadIdx.x;
   int32_t* cnt_s = sm;             // [E]     slots per expert
   int32_t* off_s = sm + E;         // [E]     first position per expert
@@ -245,8 +251,10 @@ __device__ __forceinline__ void segments_small_cta(const int32_t* __restrict__ i
   int32_t* tp_s = sm + 2 * E + NE; // [NE+1]  token tiles before each active expert
   int32_t* sid = tp_s + NE + 1;    // [S]     expert of each slot (-1: invalid)
   __shared__ int n_act_s, routed_total_s;
-  for (int i = tid; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
-  for (int i = tid; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
+  if (zero_counts) {
+    for (int i = tid; i < ws.split_cnt_n; i += blockDim.x) ws.split_cnt[i] = 0;
+    for (int i = tid; i < ws.comb_cnt_n; i += blockDim.x) ws.comb_cnt[i] = 0;
+  }
   for (int e = tid; e < E; e += blockDim.x) cnt_s[e] = 0;
   __syncthreads();
   int e = -1;

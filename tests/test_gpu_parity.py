@@ -483,6 +483,47 @@ def test_step_equals_route_then_forward_and_matches_oracle(wl, path):
     L.close()
 
 
+# ---- 17 to 64 tokens with 64-token tiles and many down units: the kernel
+# variant in which down starts per token tile (gate/up counts its finished
+# units per tile) and takes whole units dynamically (units >= 4 per CTA:
+# 40 row tiles of H = 5120 times ~60 active tiles)
+EARLY = Workload("early_h5120_i256_e64_k6_t40", 5120, 256, 64, 6, 1, 40, seed=29, scale_lo=-8, scale_hi=-4)
+
+
+def test_down_per_tile_matches_oracle_deterministic_and_equivariant():
+    """The per-tile down start with dynamically taken units: y within the
+    layer tolerance of the oracle, the same bits on every repeat (which CTA
+    takes a unit changes nothing), moe_route + moe_forward bit for bit, and a
+    permutation of the tokens permutes y bit for bit."""
+    wl = EARLY
+    L, _ = gu.make_layer(wl)
+    x = _x(wl)
+    T, E, k = wl.tokens, wl.n_experts, wl.top_k
+    xt = sg.bf16_tensor(x)
+    y = torch.empty(xt.shape, dtype=torch.int16, device=gu.DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=gu.DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=gu.DEV)
+    lo = torch.empty((T, E), dtype=torch.float32, device=gu.DEV)
+    L.step(xt, T, y, idx=idx, w=w, logits_out=lo)
+    assert L.sync() == m.MOE_OK
+    y1 = y.cpu().numpy().view(np.uint16).copy()
+    idx, w, lo = idx.cpu().numpy(), w.cpu().numpy(), lo.cpu().numpy()
+    assert len(np.unique(idx)) * (wl.hidden // 128) >= 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    for _ in range(3):
+        L.step(xt, T, y)
+        assert L.sync() == m.MOE_OK
+        assert np.array_equal(y.cpu().numpy().view(np.uint16), y1)
+    idx2, w2, lo2 = gu.run_route(L, x, T, E, k)
+    assert np.array_equal(lo, lo2) and np.array_equal(idx, idx2) and np.array_equal(w, w2)
+    assert np.array_equal(gu.run_forward(L, x, idx2, w2), y1)
+    ridx, rw = oracle.topk(lo.astype(np.float32), k)
+    assert np.array_equal(idx, ridx)
+    gu.assert_y_close(y1, gu.oracle_layer(wl, 0, x, idx, rw))
+    p = np.random.default_rng(3).permutation(T)
+    assert np.array_equal(gu.run_forward(L, x[p], idx[p], w[p]), y1[p])
+    L.close()
+
+
 # ---- sigmoid scoring with a selection-only bias and a routed scaling factor
 
 SIG_ZIPF = Workload("sig_h512_i256_e64_k6_t20_zipf", 512, 256, 64, 6, 1, 20, seed=26, zipf=1.1,
