@@ -116,12 +116,14 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
   // (one acquire-release atomic per CTA: it publishes the CTA's writes, which
   // the barrier made its own, and the last arriver acquires everyone's)
   __syncthreads();
-  if (threadIdx.x == 0) {
-    last = atomic_add_acq_rel(&p.counters[blockIdx.y], 1) == (int)(gridDim.x * gridDim.z) - 1;
-    if (last) p.counters[blockIdx.y] = 0;
+  if (gridDim.x * gridDim.z > 1) {  // (alone in its token block, a CTA is its last)
+    if (threadIdx.x == 0) {
+      last = atomic_add_acq_rel(&p.counters[blockIdx.y], 1) == (int)(gridDim.x * gridDim.z) - 1;
+      if (last) p.counters[blockIdx.y] = 0;
+    }
+    __syncthreads();
+    if (!last) return;
   }
-  __syncthreads();
-  if (!last) return;
   if (p.route) {
     // every thread: logits, then their selection codes and scores (so the
     // selecting warp only compares)

@@ -149,13 +149,15 @@ __global__ void __launch_bounds__(kRtWarps * 32, 1) router_tile_kernel(const __g
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   __syncthreads();
   pdl_trigger();  // the next kernel may start its prologue; it waits for all of this
-  if (p.xq && blockIdx.x == 0) {
-    // the codes of x for this chunk: 8 values per thread, a quad per 32-block
-    // (the count and the stride are multiples of 4, so a quad stays together)
+  if (p.xq) {
+    // the codes of x for this chunk: 8 values per thread, a quad of lanes per
+    // 32-block, the blocks spread over the chunk's expert-group CTAs (one
+    // trip count per quad, so a quad stays together)
     const unsigned quad = 0xFu << (lane & ~3);
-    const int n8 = nt * kc8;
+    const int n32 = nt * kc8 / 4;
     const uint4* x8 = reinterpret_cast<const uint4*>(xsm);
-    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+    for (int b = blockIdx.x + gridDim.x * (int)(threadIdx.x >> 2); b < n32; b += gridDim.x * (int)(blockDim.x >> 2)) {
+      const int i = 4 * b + (lane & 3);
       const int t = i / kc8, g = i - t * kc8;
       const size_t gi = (size_t)(t0 + t) * (p.H / 8) + (size_t)c * kc8 + g;  // 8-value group of x
       int ex;
