@@ -268,6 +268,35 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Small batches read every weight tile exactly once: their copies carry an L2
+// evict-first policy, so that streaming the weights leaves the small reused
+// data of the launches around them (activation codes, tile tables, h, the
+// serial kernels' code) in L2.  (Where a tile is read by several token tiles
+// the second read would then miss.)
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                 int32_t c2, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 // h = silu(g) * u = g / (1 + e^-g) * u with the SFU exponential and the fast
 // divide: a few ulp from the correctly rounded form, far inside the FP8
 // rounding of h that follows (one E4M3 step is 2^-3 relative).
@@ -478,6 +507,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
         const CUtensorMap* map = !ragged_b ? &p.b : rows == 16 ? &p.b16 : (BN > 64 && rows == 64) ? &p.b64 : &p.b;
         tma_load_3d(dst, map, 0, row, st * CH, &full_bar[fs]);
       };
+      const uint64_t wpol = EARLY ? l2_evict_first_policy() : 0;
       int deferred_rows[kMaxStages];
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
@@ -507,12 +537,20 @@ __global__ void __launch_bounds__(kThreadsMma, 1) ffn_mma_kernel(const __grid_co
                                               (shared_fp8_unit(pc.u) ? NA * 128 * 64 * CH : 0));
           if (NA == 2 && p.merged[sh]) {
             // gate and up rows of the stage in one op: {chunk elems, rows, chunks, matrix}
-            tma_load_4d(sa, sh ? &p.a_shared[0] : &p.a_routed[0], 0, erow, s * CH, 0, &full_bar[slot]);
+            if constexpr (EARLY)
+              tma_load_4d_hint(sa, sh ? &p.a_shared[0] : &p.a_routed[0], 0, erow, s * CH, 0, &full_bar[slot], wpol);
+            else
+              tma_load_4d(sa, sh ? &p.a_shared[0] : &p.a_routed[0], 0, erow, s * CH, 0, &full_bar[slot]);
           } else {
 #pragma unroll
-            for (int m = 0; m < NA; ++m)
-              tma_load_3d(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
-                          &full_bar[slot]);
+            for (int m = 0; m < NA; ++m) {
+              if constexpr (EARLY)
+                tma_load_3d_hint(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
+                                 &full_bar[slot], wpol);
+              else
+                tma_load_3d(sa + m * C::kATile, sh ? &p.a_shared[m] : &p.a_routed[m], 0, erow, s * CH,
+                            &full_bar[slot]);
+            }
           }
           if (early && s == pc.s0) wait_tile(pc.u, all_ready);
           if (waited) {
