@@ -160,12 +160,12 @@ def layer_bytes(wl, n_experts_touched: int, T: int, shared_fp8: bool = False) ->
 # same way (one 64-token tile per active expert), so the traffic scales with the experts touched:
 # traffic = ratio x algorithmic bytes.  Valid only for the kernel source the capture was taken on.
 _TRAFFIC_SRC = ("mxfp4_expert_ffn_gb300/csrc/ffn_mma_kernel.cuh", "mxfp4_expert_ffn_gb300/csrc/ffn_mma.cu")
-_TRAFFIC_SHA256 = "5495d56c5bfd77e20878e2a77dae45bdb85880ef28bb5ce9e7cda09c4de611fb"
+_TRAFFIC_SHA256 = "43238bab094a43e7bc8bd8f4ff4fe51a4d4eca07537d156305b4d70d0ff7b393"
 # (dram__bytes_read.sum + dram__bytes_write.sum) / algorithmic bytes of one gate/up launch:
 # 64 tokens over a 128-expert bank (stack-shaped layer, Zipf routing) and one decode token
 # over a 24-expert bank; each streams the same bytes per selected expert as the full layer.
-_T64_RATIO = (703.367680 + 3.700224) / 715.826688
-_T1_RATIO = (88.945664 + 2.026752) / 87.758232
+_T64_RATIO = (702.981632 + 3.166720) / 715.826688
+_T1_RATIO = (88.943104 + 2.243584) / 87.758232
 _TRAFFIC_RATIO = {("v41_stack8_decode_t64_zipf", "ffn_up_mma"): _T64_RATIO,
                   ("ncu_v41_e128_decode_t64_zipf", "ffn_up_mma"): _T64_RATIO,
                   ("v41_layer_decode_t1", "ffn_up_mma"): _T1_RATIO,
