@@ -88,7 +88,7 @@ size_t carve(const moe_config& c, int num_sms, char* base, Workspace& ws) {
   ws.ready = ws.split_cnt + 2 * 4 * kSplitUnitsPerCta * num_sms;
   ws.ready_done = ws.ready + NE;
   ws.unit_next = ws.ready_done + 1;
-  ws.prep_cnt = cv.take<int32_t>(16);
+  ws.prep_cnt = cv.take<int32_t>(32);  // one per token block (at most 16) and one for the blocks
   ws.comb_cnt_n = kPrepMaxTokens * (int)(H / 128) * 4;
   ws.comb_cnt = cv.take<int32_t>((size_t)ws.comb_cnt_n);
   ws.seg_cbase = cv.take<int32_t>((size_t)kSegCtas * E);

@@ -59,7 +59,7 @@ struct Workspace {
   int32_t* ready_done = nullptr; // [1]     gate/up CTAs finished (small batches)
   int32_t* unit_next = nullptr;  // [1]     down: units taken (small batches, whole units)
   int part_bn = 0;            // token-tile width the partial slots are sized for
-  int32_t* prep_cnt = nullptr;// [16]       small-batch preparation counters (zero between launches)
+  int32_t* prep_cnt = nullptr;// [32]       small-batch preparation counters (zero between launches)
   int32_t* comb_cnt = nullptr;// [64][H/128][4] fused-combine counters (zeroed by the segments)
   int comb_cnt_n = 0;
   int32_t* seg_cbase = nullptr; // [kSegCtas][E] large-batch segments: per-CTA counts, then bases

@@ -30,6 +30,8 @@ namespace {
 
 constexpr int kPrepWarps = 32;  // experts per CTA (one warp each)
 constexpr int kPrepTT = 8;      // tokens per block
+constexpr int kPrepTTSel = 4;   // tokens per block when the partial sums are given (9-64
+                                // tokens: selection only, so more blocks sum fewer logits)
 
 struct PrepParams {
   const uint16_t* x;
@@ -127,7 +129,8 @@ __global__ void __launch_bounds__(1024) prep_kernel(const __grid_constant__ Prep
   if (p.route) {
     // every thread: logits, then their selection codes and scores (so the
     // selecting warp only compares)
-    const int t0 = blockIdx.y * kPrepTT, nt = min(kPrepTT, p.T - t0);
+    const int tb = p.parts_ready ? kPrepTTSel : kPrepTT;
+    const int t0 = blockIdx.y * tb, nt = min(tb, p.T - t0);
     uint32_t* okey = reinterpret_cast<uint32_t*>(sm);             // [nt][E]
     float* osc = reinterpret_cast<float*>(sm) + kPrepTT * p.E;    // [nt][E]
     for (int i = threadIdx.x; i < nt * p.E; i += blockDim.x) {
@@ -219,7 +222,7 @@ cudaError_t launch_prep(const uint16_t* x, int T, int H, int E, int k, int ns, i
   p.ws = ws;
   dim3 grid;
   if (p.parts_ready) {
-    grid = dim3(1, (T + kPrepTT - 1) / kPrepTT, 1);
+    grid = dim3(1, (T + kPrepTTSel - 1) / kPrepTTSel, 1);
   } else if (route) {
     grid = dim3((E + kPrepWarps - 1) / kPrepWarps, (T + kPrepTT - 1) / kPrepTT, p.ks);
   } else {
